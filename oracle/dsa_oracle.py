@@ -1,0 +1,252 @@
+"""Oracle for the indexer -> Top-K -> sparse-attention chain (TEST INFRASTRUCTURE).
+
+A plain, slow, fp64 CPU statement of what the chain computes, written from the
+source pages, used only by ``tests/``, the smoke check and the CPU-baseline leg
+of ``bench.py``.  Nothing in the product path imports it, and it shares no code
+with the CUDA kernels: it reads the same stored bytes (bf16 bits, E4M3 codes,
+E8M0 exponents, fp32 scales) and decodes them with its own code.
+
+Method, as the pages state it ("Day 0 Support for New LLM Architectures",
+Step 1, the sparse attention modules; Key Optimization 1): a lightweight
+indexer scores the relevance of every historical position, the Top-K positions
+are selected, and a sparse-attention kernel reads only the selected entries of
+the low-rank (latent) KV cache and computes exact attention over them.  The
+score of position s for query t is
+
+    I[t, s] = sum_h  w[t, h] * ReLU( q_idx[t, h, :] . k_idx[s, :] )
+
+(per-head dot product, ReLU, head-weighted sum: "relevance scoring, head-weight
+application, and Top-K selection").  Storage formats follow Key Optimization 2
+of the same page: MXFP8 for the indexer (groups of 32 elements share one scale
+factor) and FP8 for the sparse-attention KV cache.
+
+Every function below is the plain definition; numpy's matmul and sort serve as
+library primitives for the inner sums and the ordering.
+
+Pinning: every function is pinned by ``tests/test_oracle_pins.py`` against
+hand-worked fixtures (``tests/golden``), closed forms, library routines that
+are independent of this file and brute force on tiny inputs.
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, Optional, Sequence
+
+import numpy as np
+
+__all__ = [
+    "bf16_bits_to_f64", "e4m3_to_f64", "e8m0_to_f64", "dequant_mxfp8", "dequant_fp8_rows",
+    "index_scores", "topk_positions", "sparse_attention", "visible_length", "query_sequence",
+    "Chain", "chain_query",
+]
+
+
+# ----------------------------------------------------------------------------------------------
+# Stored formats -> exact fp64 values
+# (Day 0 Support for New LLM Architectures, Key Optimization 2: MXFP8 index path with groups of
+#  32 sharing one scale factor; FP8 sparse-attention KV cache.)
+
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> fp64.  A bf16 value is the top half of the fp32 with the
+    same bits, so widening is exact."""
+    b = np.asarray(bits).astype(np.uint32)
+    return (b << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    """E4M3 ('fn' variant: no infinities, S.1111.111 is NaN) codes -> fp64.
+
+    value = (-1)^s * 2^(e-7) * (1 + m/8)   for exponent field e in 1..15
+          = (-1)^s * 2^(-6)  * (m/8)       for e = 0 (subnormal)
+    NaN codes are rejected: they never appear in valid caches.
+    """
+    c = np.asarray(codes).astype(np.int64)
+    if np.any((c & 0x7F) == 0x7F):
+        raise ValueError("E4M3 NaN code in input")
+    s = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    normal = np.ldexp(1.0 + m / 8.0, (e - 7).astype(np.int64))
+    sub = np.ldexp(m / 8.0, -6)
+    return s * np.where(e == 0, sub, normal)
+
+
+def e8m0_to_f64(codes) -> np.ndarray:
+    """E8M0 exponent bytes -> 2^(code - 127).  Code 255 (NaN) is rejected."""
+    c = np.asarray(codes).astype(np.int64)
+    if np.any(c == 255):
+        raise ValueError("E8M0 NaN code in input")
+    return np.ldexp(1.0, c - 127)
+
+
+def dequant_mxfp8(codes, sf, group: int = 32) -> np.ndarray:
+    """MXFP8 tensor -> fp64: every element times 2^(shared exponent of its group of 32)."""
+    v = e4m3_to_f64(codes)
+    scale = e8m0_to_f64(sf)
+    return v * np.repeat(scale, group, axis=-1)
+
+
+def dequant_fp8_rows(codes, row_scale) -> np.ndarray:
+    """FP8 E4M3 cache rows with one fp32 scale per row (token) -> fp64."""
+    return e4m3_to_f64(codes) * np.asarray(row_scale, dtype=np.float64)[..., None]
+
+
+# ----------------------------------------------------------------------------------------------
+# The three steps
+
+
+def index_scores(q_idx: np.ndarray, w: np.ndarray, k_idx: np.ndarray) -> np.ndarray:
+    """Indexer score of every visible position for one query.
+
+    q_idx [H_idx, d_idx], w [H_idx], k_idx [n, d_idx] (all fp64) -> I [n]:
+    I[s] = sum_h w[h] * max(0, q_idx[h] . k_idx[s]).
+    (Day 0 Support for New LLM Architectures, Step 1 and Key Optimization 1: the indexer scores
+    every historical position; relevance scoring, then head-weight application.)
+    """
+    logits = k_idx @ q_idx.T            # [n, H_idx]: per-head q.k
+    return np.maximum(logits, 0.0) @ w  # ReLU, then the head-weighted sum
+
+
+def topk_positions(scores: np.ndarray, K: int) -> np.ndarray:
+    """Top-K selection by a full sort.
+
+    Positions are ordered by score (descending), exact ties by position (ascending); the first
+    min(K, n) are returned and the rest of the K slots hold -1.
+    (Day 0 Support for New LLM Architectures, Step 1: select the Top-K positions.)
+    """
+    n = scores.shape[0]
+    order = np.lexsort((np.arange(n), -scores))
+    out = np.full(K, -1, dtype=np.int64)
+    m = min(K, n)
+    out[:m] = order[:m]
+    return out
+
+
+def sparse_attention(q: np.ndarray, k_rows: np.ndarray, v_rows: np.ndarray, sm_scale: float):
+    """Exact softmax attention of H heads over the selected rows only.
+
+    q [H, D_qk], k_rows [m, D_qk], v_rows [m, D_v] -> out [H, D_v], lse [H] where
+    logits = sm_scale * q . k, out = softmax(logits) @ v and lse = log(sum exp(logits)).
+    With no selected rows (m = 0) the output is 0 and the lse is -inf.
+    (Day 0 Support for New LLM Architectures, Step 1: the sparse-attention kernel reads only the
+    selected KV entries and performs exact computation.)
+    """
+    H, D_v = q.shape[0], v_rows.shape[1]
+    if k_rows.shape[0] == 0:
+        return np.zeros((H, D_v)), np.full(H, -np.inf)
+    logits = sm_scale * (q @ k_rows.T)           # [H, m]
+    mx = logits.max(axis=1, keepdims=True)
+    p = np.exp(logits - mx)
+    l = p.sum(axis=1, keepdims=True)
+    out = (p @ v_rows) / l
+    lse = (mx + np.log(l))[:, 0]
+    return out, lse
+
+
+# ----------------------------------------------------------------------------------------------
+# Which positions a query sees
+
+
+def query_sequence(t: int, q_per_seq: int) -> int:
+    """Queries are grouped by cache: query t reads sequence t // q_per_seq."""
+    return t // q_per_seq
+
+
+def visible_length(t: int, L: int, q_per_seq: int, q_pos0: int, n_valid=None) -> int:
+    """Number of positions query t may attend to.
+
+    Decode (q_pos0 < 0): positions 0 .. n_valid[t]-1, or the whole cache of length L.
+    Causal chunk (q_pos0 >= 0): query t sits at position q_pos0 + t % q_per_seq and sees that
+    position and everything before it ("Achieving Day-0 Readiness...", section 2.3: prefill
+    computes scores for all queries in a batch; "Day 0 Support for New LLM Architectures",
+    Key Optimization 3: the later a position, the more history it sees).
+    """
+    if q_pos0 < 0:
+        n = L if n_valid is None else int(n_valid[t])
+    else:
+        n = q_pos0 + (t % q_per_seq) + 1
+    return max(0, min(n, L))
+
+
+# ----------------------------------------------------------------------------------------------
+# One query through the chain
+
+
+class Chain:
+    """Decoded view of one set of stored inputs (the dict ``synth.make_inputs`` returns, with
+    tensors converted to numpy raw bits) plus the workload parameters.
+
+    Decoding of the big caches is lazy and per sequence, so a query only pays for its own rows.
+    """
+
+    def __init__(self, arrays: Dict[str, Optional[np.ndarray]], *, L: int, K: int, q_per_seq: int,
+                 q_pos0: int, idx_dtype: str, kv_dtype: str, sm_scale: float):
+        self.a = arrays
+        self.L, self.K, self.q_per_seq, self.q_pos0 = L, K, q_per_seq, q_pos0
+        self.idx_dtype, self.kv_dtype, self.sm_scale = idx_dtype, kv_dtype, sm_scale
+        self._kidx_cache: Dict[int, np.ndarray] = {}
+
+    # stored -> fp64
+    def q_idx(self, t: int) -> np.ndarray:
+        if self.idx_dtype == "bf16":
+            return bf16_bits_to_f64(self.a["q_idx"][t])
+        return dequant_mxfp8(self.a["q_idx"][t], self.a["q_idx_sf"][t])
+
+    def k_idx(self, seq: int, n: int) -> np.ndarray:
+        if self.idx_dtype == "bf16":
+            return bf16_bits_to_f64(self.a["k_idx"][seq, :n])
+        return dequant_mxfp8(self.a["k_idx"][seq, :n], self.a["k_idx_sf"][seq, :n])
+
+    def kv_rows(self, seq: int, rows: np.ndarray):
+        kv = self.a["kv"][seq, rows]
+        if self.kv_dtype == "bf16":
+            k = bf16_bits_to_f64(kv)
+        else:
+            k = dequant_fp8_rows(kv, self.a["kv_scale"][seq, rows])
+        if self.a.get("kv_v") is not None:
+            v = bf16_bits_to_f64(self.a["kv_v"][seq, rows])
+        else:
+            v = None
+        return k, v
+
+    def n_visible(self, t: int) -> int:
+        return visible_length(t, self.L, self.q_per_seq, self.q_pos0, self.a.get("n_valid"))
+
+    def scores(self, t: int) -> np.ndarray:
+        seq = query_sequence(t, self.q_per_seq)
+        n = self.n_visible(t)
+        w = np.asarray(self.a["w"][t], dtype=np.float64)
+        qi = self.q_idx(t)
+        out = np.empty(n)
+        step = 1 << 16  # bounded memory for million-row caches; each score is computed alone
+        for r0 in range(0, n, step):
+            r1 = min(n, r0 + step)
+            if self.idx_dtype == "bf16":
+                kk = bf16_bits_to_f64(self.a["k_idx"][seq, r0:r1])
+            else:
+                kk = dequant_mxfp8(self.a["k_idx"][seq, r0:r1], self.a["k_idx_sf"][seq, r0:r1])
+            out[r0:r1] = index_scores(qi, w, kk)
+        return out
+
+    def attention(self, t: int, idx: np.ndarray, D_v: int):
+        """Attention of query t over the positions in ``idx`` (entries < 0 are padding)."""
+        seq = query_sequence(t, self.q_per_seq)
+        rows = np.asarray(idx, dtype=np.int64)
+        rows = rows[rows >= 0]
+        q = bf16_bits_to_f64(self.a["q"][t])
+        k, v = self.kv_rows(seq, rows)
+        if v is None:  # latent cache: V is the first D_v columns of the same row
+            v = k[:, :D_v]
+        return sparse_attention(q, k, v, self.sm_scale)
+
+
+def chain_query(chain: Chain, t: int, D_v: int):
+    """Indexer scores -> Top-K -> sparse attention for query t.
+
+    Returns a dict with the scores [n_t], idx [K] (-1 padded), out [H, D_v] and lse [H].
+    """
+    s = chain.scores(t)
+    idx = topk_positions(s, chain.K)
+    out, lse = chain.attention(t, idx, D_v)
+    return {"scores": s, "idx": idx, "out": out, "lse": lse}
