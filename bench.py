@@ -1,0 +1,514 @@
+"""Throughput of the fused indexer -> Top-K -> sparse-attention decode chain on one GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+A step is one call of the fused chain (dsa_decode / dsa_prefill through the C ABI) over one batch
+of seeded synthetic inputs already resident in HBM.  The default workload is the batch-8 decode at
+L = 32768 (bf16 indexer 64 x 128, K = 2048, 16 heads over a 576-wide latent row).  Steps rotate
+over several independent input sets whose total size is several times the 129 MB L2, so every
+step reads its caches from HBM.  Rank 0 prints one JSON line.
+
+--impl reference times the oracle (plain fp64 CPU code) on the host cores on the same workload.
+Under torchrun every rank runs an independent replica (no data-path collective); the barrier and
+the max over ranks only frame the timing.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "indexer+TopK+sparse-attn queries/s; achieved HBM GB/s vs ~8 TB/s roofline"
+NOMINAL_HBM_GBS = 8000.0
+L2_BYTES = 129 * 1024 * 1024
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------------------------------------
+# algorithmic bytes (what the method must move; scratch and the index round trip excluded)
+
+
+def idx_elem_bytes(wl):
+    return 2 if wl.idx_dtype == "bf16" else 1
+
+
+def bytes_per_query(wl, n_visible=None):
+    """Compulsory HBM bytes for one query: the indexer keys (+E8M0 scales) of every visible
+    position, the query-side indexer inputs, the K gathered KV rows (+scales) and q + out."""
+    n = wl.L if n_visible is None else n_visible
+    e = idx_elem_bytes(wl)
+    k_idx = n * wl.d_idx * e + (n * wl.d_idx // 32 if wl.idx_dtype == "mxfp8" else 0)
+    q_side = wl.H_idx * wl.d_idx * e + (wl.H_idx * wl.d_idx // 32 if wl.idx_dtype == "mxfp8" else 0) + wl.H_idx * 4
+    kv_e = 2 if wl.kv_dtype == "bf16" else 1
+    rows = min(wl.K, n)
+    if wl.separate_v:
+        kv = rows * (wl.D_qk + wl.D_v) * kv_e
+    else:
+        kv = rows * wl.D_qk * kv_e + (rows * 4 if wl.kv_dtype == "fp8" else 0)
+    q_out = wl.H * wl.D_qk * 2 + wl.H * wl.D_v * 2
+    return k_idx + q_side + kv + q_out
+
+
+def index_score_bytes(wl, T):
+    """Compulsory bytes of one index-score launch over T decode queries: keys (+scales) read,
+    query-side inputs read, fp32 scores written."""
+    e = idx_elem_bytes(wl)
+    per_q = wl.L * wl.d_idx * e + wl.H_idx * wl.d_idx * e + wl.H_idx * 4 + wl.L * 4
+    if wl.idx_dtype == "mxfp8":
+        per_q += wl.L * wl.d_idx // 32 + wl.H_idx * wl.d_idx // 32
+    return T * per_q
+
+
+# ------------------------------------------------------------------------------------------------
+# helpers
+
+
+def measured_hbm_peak():
+    try:
+        with open(PEAKS_FILE) as f:
+            v = json.load(f).get("hbm_gbs")
+        if v:
+            return float(v), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_bf16_peak():
+    try:
+        with open(PEAKS_FILE) as f:
+            v = json.load(f).get("bf16_tflops")
+        if v:
+            return float(v), "measured (burst)"
+    except (OSError, ValueError):
+        pass
+    return 1900.0, "fallback"
+
+
+def index_score_flops(wl):
+    """Algorithmic FLOPs of one index-score launch: 2 * H_idx * d_idx per visible (query,
+    position) pair (the ReLU / weighting epilogue is not counted)."""
+    pairs = 0
+    for t in range(wl.T):
+        pairs += (min(wl.L, wl.q_pos0 + t % wl.q_per_seq + 1) if wl.q_pos0 >= 0 else wl.L)
+    return 2 * wl.H_idx * wl.d_idx * pairs
+
+
+def kernel_source_hash():
+    path = os.path.join(ROOT, "top_sparse_attention_gb300", "csrc", "index_score.cu")
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per index-score launch from the committed ncu summary, if it was taken on the
+    current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"index_score_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
+    m_val = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not m_hash or not m_val or m_hash.group(1) != kernel_source_hash():
+        return None
+    return int(m_val.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self._stop = threading.Event()
+        self._t = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                out = subprocess.run(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                      "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                                     timeout=5).stdout.strip()
+                if out:
+                    self.samples.append([x.strip() for x in out.split(",")])
+            except (OSError, subprocess.SubprocessError):
+                return
+            self._stop.wait(0.05)
+
+    def __enter__(self):
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._t:
+            self._t.join(timeout=10)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+def blas_threads():
+    """Threads numpy's BLAS uses (what the oracle's matmuls run on)."""
+    try:
+        import ctypes
+
+        for line in open("/proc/self/maps"):
+            if "openblas" in line.lower():
+                lib = ctypes.CDLL(line.split()[-1])
+                for fn in ("openblas_get_num_threads64_", "scipy_openblas_get_num_threads64_",
+                           "openblas_get_num_threads"):
+                    if hasattr(lib, fn):
+                        return int(getattr(lib, fn)())
+    except OSError:
+        pass
+    return os.cpu_count()
+
+
+def cpu_oracle_rate(wl, cpu_inputs, budget_s):
+    """Oracle queries/s on the host: whole chain (scores, full-sort Top-K, attention) for the
+    queries of one input set, repeated until `budget_s` seconds of work are done."""
+    import numpy as np  # noqa: F401
+
+    import oracle
+
+    a = synth.to_numpy_bits(cpu_inputs)
+    ch = oracle.Chain(a, L=wl.L, K=wl.K, q_per_seq=wl.q_per_seq, q_pos0=wl.q_pos0,
+                      idx_dtype=wl.idx_dtype, kv_dtype=wl.kv_dtype, sm_scale=wl.sm_scale)
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.chain_query(ch, n % wl.T, wl.D_v)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s and n >= 1:
+            break
+    return n / el, n, el
+
+
+# ------------------------------------------------------------------------------------------------
+# arms
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, wl):
+    """The oracle as it stands, on the host cores: each step is one query of the workload through
+    the whole chain (fp64 scores, full-sort Top-K, exact attention)."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+
+    cpu = synth.make_inputs(wl)
+    a = synth.to_numpy_bits(cpu)
+    ch = oracle.Chain(a, L=wl.L, K=wl.K, q_per_seq=wl.q_per_seq, q_pos0=wl.q_pos0,
+                      idx_dtype=wl.idx_dtype, kv_dtype=wl.kv_dtype, sm_scale=wl.sm_scale)
+    for i in range(args.warmup):
+        oracle.chain_query(ch, i % wl.T, wl.D_v)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.chain_query(ch, i % wl.T, wl.D_v)
+    el = time.perf_counter() - t0
+    rate = args.steps / el
+    cores = blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": "queries/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "config": {"workload": wl.name},
+        "cpu_baseline": {"value": rate, "unit": "queries/s", "cores": cores, "kind": "oracle",
+                         "sample": f"one query of {wl.name} per step, {args.steps} steps "
+                                   f"(fp64 numpy oracle, BLAS threads={cores})"},
+        "e2e": {"value": rate, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, wl):
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    import top_sparse_attention_gb300 as dsa
+    from top_sparse_attention_gb300 import build as _build
+
+    _build.build()
+
+    # input sets: each rank draws its own (seed offset by rank) and rotates over R of them
+    per_step = bytes_per_query(wl) * wl.T
+    n_sets = max(3, min(8, -(-3 * L2_BYTES // max(per_step, 1))))
+    if args.sets:
+        n_sets = args.sets
+    cpu_sets = [synth.make_inputs(wl, seed_offset=rank * 100 + i) for i in range(n_sets)]
+    dev_sets = [{k: (v.to(dev) if v is not None else None) for k, v in s.items()} for s in cpu_sets]
+    calls = [dsa.call_from_tensors(s, K=wl.K, sm_scale=wl.sm_scale, q_per_seq=wl.q_per_seq,
+                                   q_pos0=wl.q_pos0) for s in dev_sets]
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+
+    # warm-up (also the first call of every set outside any graph capture)
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, n_sets)):
+            calls[i % n_sets](stream)
+    torch.cuda.synchronize()
+
+    graphs = None
+    if not args.no_graph:
+        graphs = []
+        for c in calls:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                c(stream)
+            graphs.append(g)
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                graphs[i % n_sets].replay()
+        torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    # ---- timed region: exactly K steps
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for i in range(args.steps):
+                if graphs is not None:
+                    graphs[i % n_sets].replay()
+                else:
+                    calls[i % n_sets](stream)
+            ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    err = dsa.dsa_get_device_error(stream)
+    queries = wl.T * world
+    value = queries / (ms * 1e-3)
+    launches_per_step = 3 + (1 if _attn_splits(wl) > 1 else 0)
+
+    # ---- per-kernel durations (component entry points, same kernels and launch shapes), events
+    # on the launching stream over `reps` launches each
+    kern = kernel_times(dsa, wl, dev_sets, stream, reps=max(5, min(200, args.steps)))
+    if wl.q_pos0 < 0:
+        peak, peak_kind = measured_hbm_peak()
+        a_bytes = index_score_bytes(wl, wl.T)
+        achieved = a_bytes / (kern["index_score_us"] * 1e-6) / 1e9
+        roofline = {"bound": "hbm", "kernel": "index_score", "achieved": achieved, "peak": peak,
+                    "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
+                    "algorithmic_bytes": a_bytes, "traffic": profiled_traffic(wl.name)}
+    else:
+        peak, peak_kind = measured_bf16_peak()
+        flops = index_score_flops(wl)
+        achieved = flops / (kern["index_score_us"] * 1e-6) / 1e12
+        roofline = {"bound": "tensor", "kernel": "index_score", "achieved": achieved, "peak": peak,
+                    "unit": "TFLOP/s", "frac": achieved / peak, "peak_kind": peak_kind,
+                    "algorithmic_flops": flops, "traffic": profiled_traffic(wl.name)}
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    e2e = end_to_end(dsa, wl, cpu_sets[0], dev_sets[0], stream, steps=max(10, min(args.steps, 200)))
+
+    line = None
+    if rank == 0:
+        chain_gbs = per_step * world / (ms * 1e-3) / 1e9
+        cpu_base = None
+        if world == 1 and not args.no_cpu_baseline:
+            rate, n, el = cpu_oracle_rate(wl, cpu_sets[0], args.cpu_seconds)
+            cores = blas_threads()
+            cpu_base = {"value": rate, "unit": "queries/s", "cores": cores, "kind": "oracle",
+                        "sample": f"{n} queries of {wl.name} in {el:.1f} s (fp64 numpy oracle, BLAS threads={cores})"}
+        line = {
+            "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if wl.idx_dtype == "bf16" else "fp8(e4m3)+bf16",
+            "data": "synthetic (seeded N(0,1) inputs, U(0,1) head weights)",
+            "config": {"workload": wl.name, "batch": wl.T, "L": wl.L, "K": wl.K, "H_idx": wl.H_idx,
+                       "d_idx": wl.d_idx, "idx_dtype": wl.idx_dtype, "H": wl.H, "D_qk": wl.D_qk,
+                       "D_v": wl.D_v, "kv_dtype": wl.kv_dtype, "cuda_graph": graphs is not None,
+                       "l2": f"rotating {n_sets} input sets, {n_sets * per_step / 1e6:.0f} MB compulsory bytes > 129 MB L2"},
+            "hbm_gbs": chain_gbs, "hbm_frac_of_8tbs": chain_gbs / NOMINAL_HBM_GBS,
+            "hbm_frac_of_measured": chain_gbs / peak,
+            "roofline": roofline,
+            "kernels_us": kern,
+            "cpu_baseline": cpu_base,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks.summary(),
+            "device_error": err,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def _attn_splits(wl):
+    import top_sparse_attention_gb300 as dsa  # noqa: F401
+
+    blocks = -(-wl.K // 64)
+    groups = -(-wl.H // 16)
+    per = wl.T * groups
+    return max(1, min(blocks, 64, -(-304 // per)))
+
+
+def kernel_times(dsa, wl, dev_sets, stream, reps):
+    """Average device time of each step's kernel(s), launched alone through the component entry
+    points on the same inputs, rotating over the input sets."""
+    n = len(dev_sets)
+    L = wl.L
+    scores = [torch.empty(wl.T, dsa.ld_scores_for(L), dtype=torch.float32, device=s["q"].device) for s in dev_sets]
+    idx = [torch.empty(wl.T, wl.K, dtype=torch.int32, device=s["q"].device) for s in dev_sets]
+    out = {}
+
+    def timed(fn):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                fn(i % n)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for i in range(reps):
+                fn(i % n)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    def score(i):
+        s = dev_sets[i]
+        dsa.dsa_index_score(s["q_idx"], s["w"], s["k_idx"], q_idx_sf=s["q_idx_sf"], k_idx_sf=s["k_idx_sf"],
+                            q_per_seq=wl.q_per_seq, q_pos0=wl.q_pos0, n_valid=s["n_valid"], scores=scores[i],
+                            stream=stream)
+
+    def topk(i):
+        dsa.dsa_topk(scores[i], wl.K, L=L, q_per_seq=wl.q_per_seq, q_pos0=wl.q_pos0, idx=idx[i], stream=stream)
+
+    outs = [torch.empty(wl.T, wl.H, wl.D_v, dtype=torch.bfloat16, device=s["q"].device) for s in dev_sets]
+    lses = [torch.empty(wl.T, wl.H, dtype=torch.float32, device=s["q"].device) for s in dev_sets]
+    from top_sparse_attention_gb300 import _native as N
+
+    ws = torch.zeros(max(16, N.lib.dsa_sparse_attn_workspace_size(wl.T, wl.H, wl.K, wl.D_v)),
+                     dtype=torch.uint8, device=dev_sets[0]["q"].device)
+
+    def attn(i):
+        s = dev_sets[i]
+        dsa.dsa_sparse_attn(s["q"], s["kv"], idx[i], sm_scale=wl.sm_scale, kv_v=s["kv_v"], kv_scale=s["kv_scale"],
+                            D_v=wl.D_v, q_per_seq=wl.q_per_seq, out=outs[i], lse=lses[i], ws=ws, stream=stream)
+
+    out["index_score_us"] = timed(score)
+    out["topk_us"] = timed(topk)
+    out["sparse_attn_us"] = timed(attn)
+    return out
+
+
+def end_to_end(dsa, wl, cpu, dev, stream, steps):
+    """queries/s through the C ABI with the per-step query-side inputs (q, q_idx (+scales), w)
+    copied from pinned host memory and the outputs (out, lse) read back, inside the timed region.
+    The caches are device-resident state, as in decode."""
+    keys_in = [k for k in ("q", "q_idx", "q_idx_sf", "w") if cpu[k] is not None]
+    host_in = {k: cpu[k].pin_memory() for k in keys_in}
+    call = dsa.call_from_tensors(dev, K=wl.K, sm_scale=wl.sm_scale, q_per_seq=wl.q_per_seq, q_pos0=wl.q_pos0)
+    host_out = torch.empty(call.out.shape, dtype=call.out.dtype).pin_memory()
+    host_lse = torch.empty(call.lse.shape, dtype=call.lse.dtype).pin_memory()
+    h2d = sum(host_in[k].numel() * host_in[k].element_size() for k in keys_in)
+    d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
+
+    def step():
+        for k in keys_in:
+            dev[k].copy_(host_in[k], non_blocking=True)
+        call(stream)
+        host_out.copy_(call.out, non_blocking=True)
+        host_lse.copy_(call.lse, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        stream.synchronize()
+        wall = time.perf_counter() - t0
+    ms = max(e0.elapsed_time(e1), wall * 1e3) / steps
+    return {"value": wl.T / (ms * 1e-3), "unit": "queries/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode_b8_l32k_bf16", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--sets", type=int, default=0, help="input sets to rotate over (0 = auto)")
+    ap.add_argument("--no-graph", action="store_true", help="launch through the C ABI each step, no CUDA graph")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    wl = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,196 @@
+/*
+ * dsa.h -- C ABI of the GB300 (sm_103a) sparse-attention decode/prefill chain:
+ *          lightweight indexer -> Top-K selection -> gather-driven sparse attention.
+ *
+ * Method ("Day 0 Support for New LLM Architectures", Step 1 and Key Optimization 1): an indexer
+ * scores every historical position of a query, the Top-K positions are selected, and a
+ * sparse-attention kernel reads only those K rows of the low-rank (latent) KV cache and computes
+ * exact softmax attention over them.  The score of position s for query t is
+ *
+ *     I[t, s] = sum_{h < H_idx} w[t, h] * ReLU( q_idx[t, h, :] . k_idx[s, :] ).
+ *
+ * Conventions shared by every entry point
+ *  - Pointers named as device data must be device (or managed) memory visible to the current
+ *    device.  The caller owns every buffer.  The library never allocates or frees device memory,
+ *    never synchronises the stream, and enqueues all work on `stream` (a cudaStream_t passed as
+ *    void*; NULL = the legacy default stream).
+ *  - Arrays are row-major.  Strides are in BYTES unless stated otherwise.
+ *  - Queries are grouped by cache: query t reads sequence  t / q_per_seq  of each cache
+ *    (q_per_seq = 1 for batched decode, = T for one prefill chunk).
+ *  - Visible positions of query t (n_t):  if q_pos0 < 0 (decode), n_t = n_valid[t] when n_valid
+ *    is given (device int32 [T]) else L;  if q_pos0 >= 0 (causal chunk), query t sits at position
+ *    q_pos0 + t % q_per_seq and n_t = q_pos0 + t % q_per_seq + 1.  n_t is clamped to [0, L].
+ *  - Index rows hold positions within the query's own sequence; -1 marks an empty slot.
+ *  - Validation happens before any launch; a rejected call launches nothing.  Launch failures
+ *    return DSA_ERR_CUDA.  Device-side faults are never raised on purpose: kernels that meet an
+ *    out-of-range index or a wait that exceeds its time limit record a code in a device error
+ *    word, skip the offending access and finish; dsa_get_device_error() reads and clears it.
+ *  - No C++ exception crosses this interface.  All entry points are thread-safe.
+ */
+#ifndef DSA_H
+#define DSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSA_ABI_VERSION 1
+
+typedef enum dsa_status {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer or stride */
+  DSA_ERR_UNSUPPORTED = 2, /* valid but not implemented (shape, dtype, device arch) */
+  DSA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than dsa_workspace_size() */
+  DSA_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch, attribute, symbol) */
+  DSA_ERR_DEVICE = 5       /* a kernel recorded an error (see dsa_get_device_error) */
+} dsa_status;
+
+typedef enum dsa_dtype {
+  DSA_BF16 = 0,       /* bfloat16 elements */
+  DSA_FP8_E4M3 = 1,   /* E4M3 ("fn") codes with one fp32 scale per cache row (KV cache) */
+  DSA_MXFP8_E4M3 = 2  /* E4M3 codes with one E8M0 exponent byte per 32 elements (indexer) */
+} dsa_dtype;
+
+/* Device error codes recorded by kernels (read with dsa_get_device_error). */
+#define DSA_DEVERR_NONE 0
+#define DSA_DEVERR_INDEX_RANGE 1  /* an index outside [-1, L) reached the attention gather */
+#define DSA_DEVERR_WAIT_TIMEOUT 2 /* a bounded pipeline wait gave up */
+
+/* Human-readable name of a status code.  Never NULL. */
+const char* dsa_status_string(int status);
+
+/* DSA_ABI_VERSION of the loaded library. */
+int dsa_abi_version(void);
+
+/* Reads and clears the device error word of the current device.  Synchronises `stream` first
+ * (this is the one call that blocks the host).  *code receives DSA_DEVERR_*. */
+dsa_status dsa_get_device_error(int* code, void* stream);
+
+/* --------------------------------------------------------------------------------------------
+ * dsa_index_score -- step 1: indexer relevance scores ("relevance scoring, head-weight
+ * application", Day 0 Support for New LLM Architectures, Key Optimization 1; MXFP8 index path
+ * with groups of 32 sharing one scale, Key Optimization 2).
+ *
+ *   scores[t * ld_scores + s] = sum_h w[t,h] * max(0, sum_j q_idx[t,h,j] * k_idx[seq(t), s, j])
+ *
+ * for 0 <= s < n_t (fp32, products of the stored values, fp32 accumulation).  Entries with
+ * s >= n_t are left unspecified.
+ *   q_idx     device [T, H_idx, d_idx]: bf16 (DSA_BF16) or E4M3 codes (DSA_MXFP8_E4M3)
+ *   q_idx_sf  device [T, H_idx, d_idx/32] E8M0 bytes for DSA_MXFP8_E4M3, else NULL
+ *   w         device fp32 [T, H_idx] head weights (any sign)
+ *   k_idx     device: sequence q of the indexer-key cache starts at k_idx + q*k_seq_stride bytes
+ *             and holds L rows of d_idx elements, rows packed (row pitch = d_idx * elem size)
+ *   k_idx_sf  device, DSA_MXFP8_E4M3 only: sequence q at k_idx_sf + q*k_sf_seq_stride bytes,
+ *             L rows of d_idx/32 bytes, packed; else NULL
+ *   scores    device fp32, row t at scores + t*ld_scores (ld_scores in ELEMENTS, >= L)
+ * Supported: idx_dtype DSA_BF16 with d_idx in {64, 128}; DSA_MXFP8_E4M3 with d_idx = 128;
+ * 1 <= H_idx <= 64.  Pointers 16-byte aligned; k_seq_stride a multiple of 16.
+ * ------------------------------------------------------------------------------------------ */
+dsa_status dsa_index_score(const void* q_idx, const uint8_t* q_idx_sf, const float* w,
+                           const void* k_idx, const uint8_t* k_idx_sf, int64_t k_seq_stride,
+                           int64_t k_sf_seq_stride, int T, int q_per_seq, int q_pos0,
+                           const int32_t* n_valid, int L, int H_idx, int d_idx,
+                           dsa_dtype idx_dtype, float* scores, int64_t ld_scores, void* stream);
+
+/* --------------------------------------------------------------------------------------------
+ * dsa_topk -- step 2: Top-K selection ("select the Top-K positions", Day 0 Support for New LLM
+ * Architectures, Step 1; the Top-k selection operator of "Achieving Day-0 Readiness...",
+ * section 2.1).
+ *
+ * For each query t: idx[t*K .. t*K+K) receives the min(K, n_t) positions s < n_t with the
+ * largest scores[t*ld_scores + s], exact ties resolved toward the lower position, written in
+ * ascending position order, followed by -1 in the remaining slots.  Scores are compared as
+ * fp32 with -0 equal to +0; NaN scores are not supported.
+ *   ws / ws_bytes  device workspace of at least dsa_topk_workspace_size(T, L, K) bytes
+ *                  (may be NULL when that size is 0)
+ * Supported: 1 <= K <= 4096.
+ * ------------------------------------------------------------------------------------------ */
+dsa_status dsa_topk(const float* scores, int64_t ld_scores, int T, int q_per_seq, int q_pos0,
+                    const int32_t* n_valid, int L, int K, int32_t* idx, void* ws,
+                    size_t ws_bytes, void* stream);
+size_t dsa_topk_workspace_size(int T, int L, int K);
+
+/* --------------------------------------------------------------------------------------------
+ * dsa_sparse_attn -- step 3: gather the selected rows of the latent KV cache and compute exact
+ * softmax attention over them ("a sparse-attention kernel then reads only the selected KV
+ * entries to perform exact computation", Day 0 Support for New LLM Architectures, Step 1;
+ * gather by index then attention, "Achieving Day-0 Readiness...", section 2.3; FP8 KV cache,
+ * Key Optimization 2).
+ *
+ * For query t, head h, with R = the valid entries (0 <= i < L) of idx[t*K .. t*K+K):
+ *   logit[r] = sm_scale * sum_j q[t,h,j] * Kv[r, j]                 (j < D_qk)
+ *   out[t,h,:] = sum_r softmax(logit)[r] * V[r, :D_v]               (bf16 result)
+ *   lse[t,h]   = ln sum_r exp(logit[r])                             (fp32; -inf if R is empty)
+ * where Kv[r] = kv row r of sequence seq(t) (times kv_scale[r] for DSA_FP8_E4M3) and V[r] =
+ * the first D_v columns of that same row when kv_v is NULL (latent cache), else row r of kv_v.
+ * An out-of-range entry (< -1 or >= L) is skipped and recorded as DSA_DEVERR_INDEX_RANGE.
+ *   q         device bf16 [T, H, D_qk]
+ *   kv        device: row r of sequence q at kv + q*kv_seq_stride + r*kv_row_stride (bytes);
+ *             bf16 or E4M3 codes per kv_dtype
+ *   kv_v      device bf16 rows (row pitch v_row_stride, sequence pitch v_seq_stride) or NULL
+ *   kv_scale  device fp32, DSA_FP8_E4M3 only: scale of row r of sequence q at
+ *             kv_scale[q*L + r]; else NULL
+ *   idx       device int32 [T, K]
+ *   out       device bf16 [T, H, D_v];  lse  device fp32 [T, H] or NULL
+ *   ws        device workspace of at least dsa_sparse_attn_workspace_size(T, H, K, D_v)
+ *             bytes, zero-filled once before its first use (the kernels leave it reusable)
+ * Supported: kv_dtype DSA_BF16 or DSA_FP8_E4M3; (D_qk, D_v) in {(576, 512), (64, 64)};
+ * H <= 128; row strides multiples of 16 bytes; pointers 16-byte aligned.
+ * ------------------------------------------------------------------------------------------ */
+dsa_status dsa_sparse_attn(const void* q, const void* kv, const void* kv_v, const float* kv_scale,
+                           int64_t kv_row_stride, int64_t kv_seq_stride, int64_t v_row_stride,
+                           int64_t v_seq_stride, const int32_t* idx, int T, int q_per_seq, int L,
+                           int K, int H, int D_qk, int D_v, float sm_scale, dsa_dtype kv_dtype,
+                           void* out, float* lse, void* ws, size_t ws_bytes, void* stream);
+size_t dsa_sparse_attn_workspace_size(int T, int H, int K, int D_v);
+
+/* --------------------------------------------------------------------------------------------
+ * Fused chain: dsa_decode / dsa_prefill run steps 1-3 back to back on `stream` (the indexer's
+ * "score-weight-TopK" chain followed by the sparse gather kernel, Day 0 Support for New LLM
+ * Architectures, Key Optimization 1), keeping the scores in the workspace.  dsa_decode expects
+ * q_pos0 < 0; dsa_prefill expects q_pos0 >= 0 (a causal chunk, "Achieving Day-0 Readiness...",
+ * section 2.3: prefill scores all queries in a batch) and processes the queries in slices so
+ * the score scratch stays bounded.
+ * ------------------------------------------------------------------------------------------ */
+typedef struct dsa_args {
+  /* shapes */
+  int T, q_per_seq, q_pos0, L, K;
+  int H_idx, d_idx;
+  int H, D_qk, D_v;
+  float sm_scale;
+  dsa_dtype idx_dtype, kv_dtype;
+  const int32_t* n_valid; /* device [T] or NULL (decode only) */
+  /* indexer inputs (see dsa_index_score) */
+  const void* q_idx;
+  const uint8_t* q_idx_sf;
+  const float* w;
+  const void* k_idx;
+  const uint8_t* k_idx_sf;
+  int64_t k_seq_stride, k_sf_seq_stride;
+  /* attention inputs (see dsa_sparse_attn) */
+  const void* q;
+  const void* kv;
+  const void* kv_v;
+  const float* kv_scale;
+  int64_t kv_row_stride, kv_seq_stride, v_row_stride, v_seq_stride;
+  /* outputs */
+  void* out;          /* bf16 [T, H, D_v] */
+  float* lse;         /* fp32 [T, H] or NULL */
+  int32_t* idx_out;   /* int32 [T, K] or NULL (then kept in the workspace) */
+  const void* block_table; /* reserved for a paged cache layout; must be NULL */
+} dsa_args;
+
+/* Workspace bytes that dsa_decode (prefill = 0) or dsa_prefill (prefill = 1) needs for `a`. */
+dsa_status dsa_workspace_size(const dsa_args* a, int prefill, size_t* bytes);
+
+dsa_status dsa_decode(const dsa_args* a, void* ws, size_t ws_bytes, void* stream);
+dsa_status dsa_prefill(const dsa_args* a, void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H */

@@ -1,0 +1,36 @@
+"""Shared helpers of the GPU parity tests: upload seeded inputs, build the oracle view, and the
+tolerances the tests enforce."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import synth
+
+# Attention max-abs tolerances on outputs (bf16 path / FP8 KV path)
+ATTN_TOL = {"bf16": 2e-2, "fp8": 6e-2}
+# Tighter regression guard for the same comparison (the observed errors sit well below it)
+ATTN_GUARD = {"bf16": 4e-3, "fp8": 4e-3}
+LSE_TOL = 2e-3
+
+
+def to_device(inputs, device="cuda"):
+    return {k: (v.to(device) if v is not None else None) for k, v in inputs.items()}
+
+
+def oracle_chain(wl: synth.Workload, cpu_inputs):
+    a = synth.to_numpy_bits(cpu_inputs)
+    return oracle.Chain(a, L=wl.L, K=wl.K, q_per_seq=wl.q_per_seq, q_pos0=wl.q_pos0,
+                        idx_dtype=wl.idx_dtype, kv_dtype=wl.kv_dtype, sm_scale=wl.sm_scale), a
+
+
+def score_error_bound(q_idx: np.ndarray, w: np.ndarray, k_idx: np.ndarray) -> np.ndarray:
+    """Bound on |fp32 score - exact score| for one query: the per-head dots accumulate d products
+    in fp32 (products of bf16/E4M3 values are exact in fp32) and the head sum accumulates H terms,
+    so |error| <= u * (d + H + 2) * sum_h |w_h| * sum_j |q_hj k_sj| with u = 2^-22 (twice the fp32
+    unit roundoff, covering accumulators that truncate instead of rounding)."""
+    u = 2.0 ** -22
+    d, H = q_idx.shape[1], q_idx.shape[0]
+    mag = np.abs(k_idx) @ np.abs(q_idx).T  # [n, H]
+    return u * (d + H + 2) * (mag @ np.abs(w)) + 1e-30

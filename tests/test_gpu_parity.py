@@ -1,0 +1,291 @@
+"""Parity of the CUDA path (through the C ABI) with the oracle on the same seeded inputs.
+
+Step-level checks isolate each kernel:
+  * dsa_index_score vs the oracle's fp64 scores, within an fp32 accumulation bound,
+  * dsa_topk on identical fp32 scores: the index set must be bit-exact (integer work),
+  * dsa_sparse_attn on identical indices: max-abs 2e-2 (bf16) / 6e-2 (FP8) and a tighter guard.
+The fused chain is checked on all five workloads: indices under the near-tie rule against the
+oracle's fp64 scores, attention against the oracle evaluated on the GPU's own indices.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_helpers import ATTN_GUARD, ATTN_TOL, LSE_TOL, oracle_chain, score_error_bound, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dsa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from top_sparse_attention_gb300 import build
+
+    build.build()
+    import top_sparse_attention_gb300 as m
+
+    torch.cuda.set_device(0)
+    yield m
+    torch.cuda.synchronize()
+    assert m.dsa_get_device_error() == 0
+
+
+# ------------------------------------------------------------------------------------------------
+# step 1: index scores
+
+SCORE_CASES = [
+    # name, base workload, overrides, n_valid
+    ("bf16_d128_h64_ragged", "decode_b8_l32k_bf16", dict(T=3, L=1000), None),
+    ("bf16_d64_h4_tiny", "tiny_decode_l2k", dict(), None),
+    ("bf16_d128_h1", "decode_b8_l32k_bf16", dict(T=2, L=300, H_idx=1), None),
+    ("bf16_d128_h17", "decode_b8_l32k_bf16", dict(T=2, L=513, H_idx=17), None),
+    ("bf16_d128_h33", "decode_b8_l32k_bf16", dict(T=2, L=257, H_idx=33), None),
+    ("mxfp8_d128_h64", "decode_b8_l32k_mxfp8", dict(T=2, L=777), None),
+    ("mxfp8_d128_h20", "decode_b8_l32k_mxfp8", dict(T=3, L=200, H_idx=20), None),
+    ("varlen", "decode_b8_l32k_bf16", dict(T=4, L=1000), [0, 1, 129, 1000]),
+    ("prefill_grouped", "prefill_t4096_l128k_bf16", dict(T=8, q_per_seq=8, L=600, q_pos0=400), None),
+    ("prefill_ungrouped_t6", "prefill_t4096_l128k_bf16", dict(T=6, q_per_seq=6, L=700, q_pos0=10), None),
+    ("prefill_mx", "decode_b8_l32k_mxfp8", dict(T=5, q_per_seq=5, L=300, q_pos0=200), None),
+]
+
+
+@pytest.mark.parametrize("name,base,kw,n_valid", SCORE_CASES, ids=[c[0] for c in SCORE_CASES])
+def test_index_score_parity(dsa, name, base, kw, n_valid):
+    wl = synth.small_workload(base, name=name, **kw)
+    cpu = synth.make_inputs(wl, n_valid=n_valid)
+    if name == "bf16_d128_h17":
+        cpu["w"] = cpu["w"] - 0.5  # negative head weights
+    dev = to_device(cpu)
+    scores = dsa.dsa_index_score(dev["q_idx"], dev["w"], dev["k_idx"], q_idx_sf=dev["q_idx_sf"],
+                                 k_idx_sf=dev["k_idx_sf"], q_per_seq=wl.q_per_seq, q_pos0=wl.q_pos0,
+                                 n_valid=dev["n_valid"]).cpu().numpy()
+    ch, a = oracle_chain(wl, cpu)
+    for t in range(wl.T):
+        n = ch.n_visible(t)
+        ref = ch.scores(t)
+        seq = t // wl.q_per_seq
+        bound = score_error_bound(ch.q_idx(t), a["w"][t].astype(np.float64), ch.k_idx(seq, n))
+        err = np.abs(scores[t, :n].astype(np.float64) - ref)
+        assert np.all(err <= bound), f"t={t}: worst error/bound {np.max(err / bound):.3g}"
+
+
+# ------------------------------------------------------------------------------------------------
+# step 2: Top-K on identical fp32 scores (bit-exact)
+
+
+def _topk_case(dsa, scores_np, K, L, q_per_seq=1, q_pos0=-1, n_valid=None):
+    T = scores_np.shape[0]
+    ld = dsa.ld_scores_for(L)
+    buf = np.full((T, ld), np.nan, dtype=np.float32)  # entries beyond n_t must not be read
+    buf[:, :L] = scores_np
+    dev = torch.from_numpy(buf).cuda()
+    nv = None if n_valid is None else torch.tensor(n_valid, dtype=torch.int32).cuda()
+    idx = dsa.dsa_topk(dev, K, L=L, q_per_seq=q_per_seq, q_pos0=q_pos0, n_valid=nv).cpu().numpy()
+    for t in range(T):
+        n = oracle.visible_length(t, L, q_per_seq, q_pos0, n_valid)
+        buf[t, n:] = 0  # the oracle sees only the visible prefix
+        want = oracle.topk_positions(scores_np[t, :n].astype(np.float64), K)
+        m = min(K, n)
+        got = idx[t]
+        assert np.all(got[m:] == -1), f"t={t}: padding"
+        assert np.all(np.diff(got[:m]) > 0), f"t={t}: positions must be ascending"
+        assert np.array_equal(np.sort(want[:m]), got[:m]), f"t={t}: index set differs"
+
+
+def test_topk_random_scores(dsa):
+    rng = np.random.default_rng(11)
+    _topk_case(dsa, rng.standard_normal((4, 32768)).astype(np.float32) * 30 + 140, 2048, 32768)
+
+
+def test_topk_heavy_ties_and_negatives(dsa):
+    rng = np.random.default_rng(12)
+    s = (np.round(rng.standard_normal((3, 5000)) * 3) / 4).astype(np.float32)  # few distinct values
+    s[1] = -np.abs(s[1])
+    s[2, ::2] = -0.0
+    s[2, 1::2] = 0.0
+    _topk_case(dsa, s, 700, 5000)
+
+
+def test_topk_all_equal_and_tiny_k(dsa):
+    s = np.full((2, 3000), 1.5, dtype=np.float32)
+    _topk_case(dsa, s, 1, 3000)
+    _topk_case(dsa, s, 2048, 3000)
+
+
+def test_topk_n_at_and_around_k(dsa):
+    rng = np.random.default_rng(13)
+    s = rng.standard_normal((5, 300)).astype(np.float32)
+    _topk_case(dsa, s, 100, 300, n_valid=[0, 1, 99, 100, 101])
+    _topk_case(dsa, s, 300, 300)
+    _topk_case(dsa, s, 4096, 300)
+
+
+def test_topk_long_rows_uncached_path(dsa):
+    rng = np.random.default_rng(14)
+    s = rng.standard_normal((2, 70001)).astype(np.float32)
+    _topk_case(dsa, s, 4096, 70001)
+
+
+def test_topk_causal_rows(dsa):
+    rng = np.random.default_rng(15)
+    s = rng.standard_normal((6, 2600)).astype(np.float32)
+    _topk_case(dsa, s, 512, 2600, q_per_seq=3, q_pos0=2000)
+
+
+# ------------------------------------------------------------------------------------------------
+# step 3: sparse attention on identical indices
+
+
+def _attn_case(dsa, wl, idx_np, kv_kind):
+    cpu = synth.make_inputs(wl)
+    dev = to_device(cpu)
+    idx = torch.from_numpy(idx_np.astype(np.int32)).cuda()
+    out, lse = dsa.dsa_sparse_attn(dev["q"], dev["kv"], idx, sm_scale=wl.sm_scale, kv_v=dev["kv_v"],
+                                   kv_scale=dev["kv_scale"], D_v=wl.D_v, q_per_seq=wl.q_per_seq)
+    out = out.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    ch, _ = oracle_chain(wl, cpu)
+    worst = 0.0
+    for t in range(wl.T):
+        ref, ref_lse = ch.attention(t, idx_np[t], wl.D_v)
+        err = float(np.max(np.abs(out[t] - ref)))
+        worst = max(worst, err)
+        assert err <= ATTN_TOL[kv_kind], f"t={t}: max-abs {err}"
+        fin = np.isfinite(ref_lse)
+        assert np.array_equal(fin, np.isfinite(lse[t]))
+        assert np.all(np.abs(lse[t][fin] - ref_lse[fin]) <= LSE_TOL)
+    assert worst <= ATTN_GUARD[kv_kind], f"max-abs {worst} above the regression guard"
+    return worst
+
+
+def _random_idx(T, K, L, seed, pad=0):
+    rng = np.random.default_rng(seed)
+    idx = np.stack([np.sort(rng.choice(L, size=K, replace=False)) for _ in range(T)])
+    if pad:
+        idx[:, K - pad:] = -1
+    return idx
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("K,pad", [(2048, 0), (2048, 37), (100, 0), (64, 64)])
+def test_sparse_attn_mla(dsa, kv, K, pad):
+    base = "decode_b8_l32k_bf16" if kv == "bf16" else "decode_b8_l32k_mxfp8"
+    wl = synth.small_workload(base, T=3, L=4000, K=K)
+    _attn_case(dsa, wl, _random_idx(3, K, 4000, K + pad, pad), kv)
+
+
+def test_sparse_attn_head_groups_and_ragged_heads(dsa):
+    wl = synth.small_workload("decode_b8_l32k_bf16", T=2, L=3000, K=512, H=20)
+    _attn_case(dsa, wl, _random_idx(2, 512, 3000, 5), "bf16")
+
+
+def test_sparse_attn_small_head_separate_v(dsa):
+    wl = synth.WORKLOADS["tiny_decode_l2k"]
+    _attn_case(dsa, wl, _random_idx(1, 64, 2048, 6), "bf16")
+
+
+def test_sparse_attn_repeated_rows(dsa):
+    wl = synth.small_workload("decode_b8_l32k_bf16", T=2, L=500, K=256)
+    idx = np.tile(np.arange(8), (2, 32))
+    _attn_case(dsa, wl, idx, "bf16")
+
+
+def test_sparse_attn_out_of_range_index_is_skipped_and_recorded(dsa):
+    wl = synth.small_workload("decode_b8_l32k_bf16", T=1, L=500, K=128)
+    cpu = synth.make_inputs(wl)
+    dev = to_device(cpu)
+    good = _random_idx(1, 128, 500, 7)
+    bad = good.copy()
+    bad[0, 5] = 500          # one past the end: checked by the kernel, never read
+    bad[0, 9] = -7
+    dsa.dsa_get_device_error()  # clear
+    out, _ = dsa.dsa_sparse_attn(dev["q"], dev["kv"], torch.from_numpy(bad.astype(np.int32)).cuda(),
+                                 sm_scale=wl.sm_scale)
+    assert dsa.dsa_get_device_error() == 1
+    ch, _ = oracle_chain(wl, cpu)
+    ref, _ = ch.attention(0, np.where((bad[0] >= 0) & (bad[0] < 500), bad[0], -1), wl.D_v)
+    assert np.max(np.abs(out[0].float().cpu().numpy() - ref)) <= ATTN_TOL["bf16"]
+
+
+# ------------------------------------------------------------------------------------------------
+# fused chain
+
+
+def _check_chain(dsa, wl, cpu, queries=None):
+    dev = to_device(cpu)
+    call = dsa.call_from_tensors(dev, K=wl.K, sm_scale=wl.sm_scale, q_per_seq=wl.q_per_seq, q_pos0=wl.q_pos0)
+    out, lse, idx = call()
+    torch.cuda.synchronize()
+    out = out.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    idx = idx.cpu().numpy()
+    ch, _ = oracle_chain(wl, cpu)
+    kind = wl.kv_dtype
+    report = {"band": 0, "swaps": 0, "worst_attn": 0.0}
+    for t in (range(wl.T) if queries is None else queries):
+        rep = oracle.parity.check_topk(idx[t], ch.scores(t), wl.K)
+        report["band"] += rep["band"]
+        report["swaps"] += rep["swaps"]
+        ref, ref_lse = ch.attention(t, idx[t], wl.D_v)
+        err = float(np.max(np.abs(out[t] - ref)))
+        report["worst_attn"] = max(report["worst_attn"], err)
+        assert err <= ATTN_TOL[kind], f"t={t}: attention max-abs {err}"
+        fin = np.isfinite(ref_lse)
+        assert np.all(np.abs(lse[t][fin] - ref_lse[fin]) <= LSE_TOL)
+    assert report["worst_attn"] <= ATTN_GUARD[kind]
+    print(wl.name, report)
+    return report
+
+
+@pytest.mark.parametrize("name", ["tiny_decode_l2k", "decode_b8_l32k_bf16", "decode_b8_l32k_mxfp8"])
+def test_chain_full_decode_workloads(dsa, name):
+    wl = synth.WORKLOADS[name]
+    _check_chain(dsa, wl, synth.make_inputs(wl))
+
+
+def test_chain_long_context_decode(dsa):
+    wl = synth.WORKLOADS["decode_b1_l1m_mxfp8"]
+    _check_chain(dsa, wl, synth.make_inputs(wl))
+
+
+def test_chain_prefill_chunk_sampled_rows(dsa):
+    wl = synth.WORKLOADS["prefill_t4096_l128k_bf16"]
+    rng = np.random.default_rng(16)
+    rows = sorted({0, 1, 2, 3, 4095, 2048} | set(rng.choice(4096, size=10, replace=False).tolist()))
+    _check_chain(dsa, wl, synth.make_inputs(wl), queries=rows)
+
+
+@pytest.mark.parametrize("case", ["short_context", "varlen", "small_causal", "ragged_fp8"])
+def test_chain_edge_cases(dsa, case):
+    if case == "short_context":   # L < K: every position then -1
+        wl = synth.small_workload("decode_b8_l32k_bf16", T=2, L=100, K=256)
+        cpu = synth.make_inputs(wl)
+    elif case == "varlen":        # an empty query, one below K, one above
+        wl = synth.small_workload("decode_b8_l32k_bf16", T=3, L=3000, K=512)
+        cpu = synth.make_inputs(wl, n_valid=[0, 300, 2999])
+    elif case == "small_causal":  # prefix shorter than K for the first queries
+        wl = synth.small_workload("prefill_t4096_l128k_bf16", T=12, q_per_seq=12, L=700, K=256, q_pos0=250)
+        cpu = synth.make_inputs(wl)
+    else:
+        wl = synth.small_workload("decode_b8_l32k_mxfp8", T=3, L=2345, K=333)
+        cpu = synth.make_inputs(wl)
+    _check_chain(dsa, wl, cpu)
+    if case == "varlen":
+        dev = to_device(cpu)
+        call = dsa.call_from_tensors(dev, K=wl.K, sm_scale=wl.sm_scale)
+        out, lse, idx = call()
+        assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))
+        assert torch.all(idx[0] == -1)
+
+
+def test_chain_empty_batch_is_a_no_op(dsa):
+    wl = synth.small_workload("decode_b8_l32k_bf16", T=1, L=256, K=64)
+    dev = to_device(synth.make_inputs(wl))
+    dev = {k: (v[:0] if (v is not None and k in ("q_idx", "w", "q")) else v) for k, v in dev.items()}
+    dev["k_idx"] = dev["k_idx"][:0]
+    dev["kv"] = dev["kv"][:0]
+    out, lse, idx = dsa.call_from_tensors(dev, K=64, sm_scale=wl.sm_scale)()
+    assert out.shape[0] == 0 and idx.shape[0] == 0

@@ -1,0 +1,105 @@
+// Internal declarations shared by the kernel translation units and the C ABI layer.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <utility>
+
+#include "dsa_common.cuh"
+
+namespace dsa {
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Launch with cudaLaunchKernelEx; `pdl` lets the kernel start while the previous kernel in the
+// stream finishes (the kernel then calls griddepcontrol.wait before reading its inputs).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// ---------------------------------------------------------------------------------------------
+// step 1: indexer scores
+
+struct IndexScoreParams {
+  const float* w;          // [T, H_idx]
+  const uint8_t* q_sf;     // [T, H_idx, d/32] (MXFP8) or null
+  const uint8_t* k_sf;     // sequence q at k_sf + q * k_sf_seq_stride (MXFP8) or null
+  int64_t k_sf_seq_stride;
+  const int32_t* n_valid;
+  float* scores;
+  int64_t ld_scores;
+  int T, q_per_seq, q_pos0, L, H_idx;
+  int t_off;               // global index of local query 0 (visibility and sequence use t + t_off)
+  int tiles;               // ceil(L / 128) position tiles per query
+  int* err;                // device error word
+};
+
+cudaError_t launch_index_score(const void* q_idx, const void* k_idx, int64_t k_seq_stride,
+                               int n_seq, int d_idx, bool mx, const IndexScoreParams& p,
+                               cudaStream_t stream, bool pdl);
+
+// ---------------------------------------------------------------------------------------------
+// step 2: Top-K
+
+struct TopkParams {
+  const float* scores;
+  int64_t ld_scores;
+  const int32_t* n_valid;
+  int32_t* idx;
+  int T, q_per_seq, q_pos0, L, K;
+  int t_off;               // global index of local query 0
+  int* err;                // device error word
+};
+
+cudaError_t launch_topk(const TopkParams& p, void* ws, cudaStream_t stream, bool pdl);
+size_t topk_ws_bytes(int T, int L, int K);
+
+// ---------------------------------------------------------------------------------------------
+// step 3: sparse attention
+
+struct SparseAttnParams {
+  const __nv_bfloat16* q;  // [T, H, D_qk]
+  const uint8_t* kv;
+  const uint8_t* kv_v;
+  const float* kv_scale;
+  int64_t kv_row_stride, kv_seq_stride, v_row_stride, v_seq_stride;
+  const int32_t* idx;      // [T, K]
+  int T, q_per_seq, L, K, H;
+  int t_off;               // global index of local query 0 (selects the sequence)
+  float scale_log2;        // sm_scale * log2(e)
+  __nv_bfloat16* out;      // [T, H, D_v]
+  float* lse;              // [T, H] or null
+  float* part_o;           // [T, H, splits, D_v] when splits > 1
+  float* part_ml;          // [T, H, splits, 2]
+  int splits;
+  int rows_per_split;
+  int* err;                // device error word
+};
+
+int sparse_attn_splits(int T, int H, int K);
+size_t sparse_attn_ws_bytes(int T, int H, int K, int D_v);
+cudaError_t launch_sparse_attn(SparseAttnParams p, int D_qk, int D_v, bool fp8, bool sepv,
+                               void* ws, cudaStream_t stream, bool pdl);
+
+// Driver entry point for tensor-map encoding (resolved once through the runtime).
+CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, cuuint32_t rank,
+                           void* addr, const cuuint64_t* dims, const cuuint64_t* strides,
+                           const cuuint32_t* box, CUtensorMapSwizzle swizzle);
+
+}  // namespace dsa

@@ -1,0 +1,377 @@
+// Step 1 of the chain: indexer relevance scores,
+//   I[t, s] = sum_h w[t, h] * ReLU(q_idx[t, h, :] . k_idx[s, :])
+// ("relevance scoring, head-weight application", Day 0 Support for New LLM Architectures,
+// Key Optimization 1; MXFP8 index path with groups of 32 sharing a scale, Key Optimization 2).
+//
+// The contraction runs on the 5th-generation tensor cores: a tile of 128 cache positions is the
+// M = 128 side of tcgen05.mma (A = k_idx rows, K-major, streamed by TMA with 128-byte swizzle),
+// the G queries x H_idx heads of one query group are the N side (B = q_idx rows, staged once per
+// group), and the fp32 accumulator lives in tensor memory.  Each epilogue thread owns one TMEM
+// lane = one position and all of its head columns, so ReLU, the head weights and (for MXFP8) the
+// per-group E8M0 scales are applied in registers with no cross-thread reduction.
+//
+// Warp roles (192 threads): warp 0 = producer (TMA for A, plain loads for B), warp 1 = TMEM
+// owner and MMA issuer, warps 2-5 = epilogue.  A ring of shared-memory stages decouples loads
+// from MMAs; two TMEM accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
+// The grid is persistent: CTA c processes a contiguous range of (query group, tile) units.
+//
+// MXFP8: one kind::f8f6f4 MMA covers K = 32 = one scale group, so each group accumulates into
+// its own TMEM columns and the epilogue forms  sum_g 2^(ea_g) 2^(eb_g) D_g  (exact scaling of
+// fp32 partial sums by powers of two), i.e. the dequantisation happens in registers.
+#include <utility>
+
+#include "dsa_internal.h"
+
+namespace dsa {
+namespace {
+
+constexpr int kTileM = 128;
+constexpr int kThreads = 192;
+constexpr int kSmemBudget = 225 * 1024;
+
+constexpr int pow2_at_least(int x) {
+  int p = 32;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+template <bool MX, int D, int G, int NPAD>
+struct Cfg {
+  static constexpr int ELEM = MX ? 1 : 2;
+  static constexpr int ROW_BYTES = D * ELEM;
+  static constexpr int BOXES = ROW_BYTES / 128;  // 128-byte swizzle atoms per row
+  static constexpr int BOX_COLS = 128 / ELEM;
+  static constexpr int KSTEPS = ROW_BYTES / 32;  // MMAs per tile (32 bytes of K each)
+  static constexpr int N = G * NPAD;              // MMA N
+  static constexpr int A_BYTES = kTileM * ROW_BYTES;
+  static constexpr int B_BYTES = N * ROW_BYTES;
+  static constexpr int B_BUFS = (2 * B_BYTES <= 64 * 1024) ? 2 : 1;
+  static constexpr int GROUPS = MX ? D / 32 : 1;  // accumulators per tile
+  static constexpr int ACC_COLS = GROUPS * N;
+  static constexpr int TMEM_COLS = pow2_at_least(2 * ACC_COLS);
+  static constexpr int AUX_BYTES = 1024 + 4096 + G * NPAD * 4 + G * NPAD * GROUPS * 4;
+  static constexpr int STAGES_FIT = (kSmemBudget - B_BUFS * B_BYTES - AUX_BYTES) / A_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int OFF_B = STAGES * A_BYTES;
+  static constexpr int OFF_BAR = OFF_B + B_BUFS * B_BYTES;
+  static constexpr int OFF_W = OFF_BAR + 1024;
+  static constexpr int OFF_QS = OFF_W + G * NPAD * 4;
+  static constexpr int SMEM = OFF_QS + G * NPAD * GROUPS * 4 + 1024;  // + alignment slack
+  static_assert(N % 16 == 0 && N >= 16 && N <= 256, "MMA N out of range");
+  static_assert(2 * ACC_COLS <= 512, "accumulators exceed tensor memory");
+  static_assert(STAGES >= 2, "not enough shared memory for the pipeline");
+  static_assert(ROW_BYTES % 128 == 0, "rows must fill whole swizzle atoms");
+};
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// E8M0 byte -> 2^(e - 127) as an fp32 bit pattern (e = 0 is the subnormal 2^-127).
+__device__ __forceinline__ float e8m0_value(uint32_t e) {
+  return e == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(e << 23);
+}
+
+// Unit u -> (first query of its group, tile).  Returns false when the tile holds no position
+// visible to any query of the group.
+struct Unit {
+  int t0, tile, n_max;
+};
+
+template <int G>
+__device__ __forceinline__ bool unit_of(const IndexScoreParams& p, int64_t u, Unit& x) {
+  const int g = (int)(u / p.tiles);
+  x.tile = (int)(u % p.tiles);
+  x.t0 = g * G;
+  int n_max = 0;
+#pragma unroll
+  for (int j = 0; j < G; ++j)
+    if (x.t0 + j < p.T)
+      n_max = max(n_max, visible_len(x.t0 + j + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid));
+  x.n_max = n_max;
+  return x.tile * kTileM < n_max;
+}
+
+template <bool MX, int D, int G, int NPAD>
+__global__ void __launch_bounds__(kThreads, 1)
+index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const uint8_t* __restrict__ q_idx,
+                   const IndexScoreParams p) {
+  using C = Cfg<MX, D, G, NPAD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* a_s = smem;
+  uint8_t* b_s = smem + C::OFF_B;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* bfull = empty + C::STAGES;
+  uint64_t* bempty = bfull + 2;
+  uint64_t* tfull = bempty + 2;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  float* w_s = reinterpret_cast<float*>(smem + C::OFF_W);    // [G][NPAD]
+  float* qs_s = reinterpret_cast<float*>(smem + C::OFF_QS);  // [G][NPAD][GROUPS]
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+  const int n_groups = (p.T + G - 1) / G;
+  const int64_t U = (int64_t)n_groups * p.tiles;
+  const int64_t u_begin = U * blockIdx.x / gridDim.x;
+  const int64_t u_end = U * (blockIdx.x + 1) / gridDim.x;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bfull[i], 1);
+      mbar_init(&bempty[i], 1);
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 128);
+    }
+    fence_mbar_init();
+    prefetch_tmap(&tm_k);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  pdl_wait();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    int it = 0, qn = -1, cur_t0 = -1;
+    bool ok = true;
+    for (int64_t u = u_begin; u < u_end && ok; ++u) {
+      Unit x;
+      if (!unit_of<G>(p, u, x)) continue;
+      if (x.t0 != cur_t0) {
+        cur_t0 = x.t0;
+        ++qn;
+        const int bb = qn % C::B_BUFS;
+        if (qn >= C::B_BUFS) ok = mbar_wait(&bempty[bb], ((qn - C::B_BUFS) / C::B_BUFS) & 1, p.err);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        // B tile: rows j*NPAD + h <- q_idx row (t0 + j) * H_idx + h, zero past H_idx / T,
+        // written in the 128-byte swizzled K-major layout the MMA descriptor expects.
+        uint8_t* bdst = b_s + bb * C::B_BYTES;
+        constexpr int CH = C::ROW_BYTES / 16;
+        for (int i = lane; i < C::N * CH; i += 32) {
+          const int r = i / CH, c = i % CH;
+          const int j = r / NPAD, h = r % NPAD;
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (h < p.H_idx && x.t0 + j < p.T)
+            v = *reinterpret_cast<const uint4*>(q_idx + ((int64_t)(x.t0 + j) * p.H_idx + h) * C::ROW_BYTES + c * 16);
+          const int box = c >> 3, cc = c & 7;
+          *reinterpret_cast<uint4*>(bdst + box * (C::N * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bfull[bb]);
+      }
+      const int s = it % C::STAGES;
+      if (it >= C::STAGES) ok = mbar_wait(&empty[s], ((it / C::STAGES) - 1) & 1, p.err);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&full[s], C::A_BYTES);
+        const int seq = (x.t0 + p.t_off) / p.q_per_seq;
+#pragma unroll
+        for (int b = 0; b < C::BOXES; ++b)
+          tma_load_3d(a_s + s * C::A_BYTES + b * (kTileM * 128), &tm_k, &full[s], b * C::BOX_COLS,
+                      x.tile * kTileM, seq);
+      }
+      __syncwarp();
+      ++it;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = MX ? make_idesc(0, 0, kTileM, C::N) : make_idesc(1, 1, kTileM, C::N);
+    int it = 0, qn = -1, cur_t0 = -1, ai = 0;
+    bool ok = true;
+    for (int64_t u = u_begin; u < u_end && ok; ++u) {
+      Unit x;
+      if (!unit_of<G>(p, u, x)) continue;
+      if (x.t0 != cur_t0) {
+        if (qn >= 0 && lane == 0) tc_commit(&bempty[qn % C::B_BUFS]);
+        cur_t0 = x.t0;
+        ++qn;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bfull[qn % C::B_BUFS], (qn / C::B_BUFS) & 1, p.err));
+        if (!ok) break;
+      }
+      const int s = it % C::STAGES;
+      ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (it / C::STAGES) & 1, p.err));
+      const int ab = ai & 1;
+      if (ok && ai >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&tempty[ab], ((ai - 2) >> 1) & 1, p.err));
+      if (!ok) break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t a_base = smem_u32(a_s + s * C::A_BYTES);
+        const uint32_t b_base = smem_u32(b_s + (qn % C::B_BUFS) * C::B_BYTES);
+        const uint32_t d0 = tmem + ab * C::ACC_COLS;
+#pragma unroll
+        for (int k = 0; k < C::KSTEPS; ++k) {
+          const int box = k >> 2, off = (k & 3) * 32;
+          const uint64_t ad = smem_desc_sw128(a_base + box * (kTileM * 128) + off);
+          const uint64_t bd = smem_desc_sw128(b_base + box * (C::N * 128) + off);
+          if (MX)
+            mma_f8(d0 + k * C::N, ad, bd, idesc, 0u);
+          else
+            mma_f16(d0, ad, bd, idesc, k > 0 ? 1u : 0u);
+        }
+        tc_commit(&empty[s]);
+        tc_commit(&tfull[ab]);
+      }
+      __syncwarp();
+      ++it;
+      ++ai;
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int q4 = warp & 3;  // the TMEM lane quarter this warp may access
+    const int row = q4 * 32 + lane;
+    const int et = threadIdx.x - 64;
+    int ai = 0, cur_t0 = -1;
+    bool ok = true;
+    for (int64_t u = u_begin; u < u_end && ok; ++u) {
+      Unit x;
+      if (!unit_of<G>(p, u, x)) continue;
+      if (x.t0 != cur_t0) {
+        cur_t0 = x.t0;
+        epi_bar();
+        for (int i = et; i < G * NPAD; i += 128) {
+          const int j = i / NPAD, h = i % NPAD;
+          const bool valid = h < p.H_idx && x.t0 + j < p.T;
+          w_s[i] = valid ? p.w[(int64_t)(x.t0 + j) * p.H_idx + h] : 0.f;
+          if (MX) {
+#pragma unroll
+            for (int g = 0; g < C::GROUPS; ++g)
+              qs_s[i * C::GROUPS + g] =
+                  valid ? e8m0_value(p.q_sf[((int64_t)(x.t0 + j) * p.H_idx + h) * C::GROUPS + g]) : 0.f;
+          }
+        }
+        epi_bar();
+      }
+      const int pos = x.tile * kTileM + row;
+      const int seq = (x.t0 + p.t_off) / p.q_per_seq;
+      float ks[C::GROUPS];
+      if (MX) {
+        uint32_t raw = 0;
+        if (pos < x.n_max) {
+          const uint8_t* src = p.k_sf + (int64_t)seq * p.k_sf_seq_stride + (int64_t)pos * C::GROUPS;
+          if (C::GROUPS == 4) raw = *reinterpret_cast<const uint32_t*>(src);
+          else
+            for (int g = 0; g < C::GROUPS; ++g) raw |= (uint32_t)src[g] << (8 * g);
+        }
+#pragma unroll
+        for (int g = 0; g < C::GROUPS; ++g) ks[g] = e8m0_value((raw >> (8 * g)) & 0xFFu);
+      }
+      const int ab = ai & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&tfull[ab], (ai >> 1) & 1, p.err));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tb = tmem + ((uint32_t)(q4 * 32) << 16) + ab * C::ACC_COLS;
+      float score[G];
+#pragma unroll
+      for (int j = 0; j < G; ++j) score[j] = 0.f;
+      constexpr int CW = C::N < 32 ? C::N : 32;  // columns per TMEM load
+#pragma unroll
+      for (int c = 0; c < C::N / CW; ++c) {
+        const int j = (c * CW) / NPAD;  // query of the group these columns belong to
+        float v[CW];
+        if (!MX) {
+          tmem_ld_sync(tb + c * CW, v);
+        } else {
+#pragma unroll
+          for (int i = 0; i < CW; ++i) v[i] = 0.f;
+#pragma unroll
+          for (int g = 0; g < C::GROUPS; ++g) {
+            float d[CW];
+            tmem_ld_sync(tb + g * C::N + c * CW, d);
+#pragma unroll
+            for (int i = 0; i < CW; ++i) v[i] = fmaf(ks[g] * qs_s[(c * CW + i) * C::GROUPS + g], d[i], v[i]);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < CW; ++i) score[j] = fmaf(w_s[c * CW + i], fmaxf(v[i], 0.f), score[j]);
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[ab]);
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        const int t = x.t0 + j;
+        if (t < p.T && pos < visible_len(t + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid))
+          p.scores[(int64_t)t * p.ld_scores + pos] = score[j];
+      }
+      ++ai;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+  pdl_launch_dependents();
+}
+
+template <bool MX, int D, int G, int NPAD>
+cudaError_t launch_cfg(const void* q_idx, const void* k_idx, int64_t k_seq_stride, int n_seq,
+                       const IndexScoreParams& p, cudaStream_t stream, bool pdl) {
+  using C = Cfg<MX, D, G, NPAD>;
+  CUtensorMap tm;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.L, (cuuint64_t)n_seq};
+  const cuuint64_t seq_stride = n_seq > 1 ? (cuuint64_t)k_seq_stride : (cuuint64_t)p.L * C::ROW_BYTES;
+  const cuuint64_t strides[2] = {(cuuint64_t)C::ROW_BYTES, seq_stride};
+  const cuuint32_t box[3] = {(cuuint32_t)C::BOX_COLS, (cuuint32_t)kTileM, 1};
+  CUresult r = encode_tensor_map(&tm, MX ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                 3, const_cast<void*>(k_idx), dims, strides, box,
+                                 CU_TENSOR_MAP_SWIZZLE_128B);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  auto kern = index_score_kernel<MX, D, G, NPAD>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t units = (int64_t)((p.T + G - 1) / G) * p.tiles;
+  const int grid = (int)(units < sms ? units : sms);
+  if (grid <= 0) return cudaSuccess;
+  return launch_kernel(kern, dim3(grid), dim3(kThreads), C::SMEM, stream, pdl, tm,
+                       reinterpret_cast<const uint8_t*>(q_idx), p);
+}
+
+}  // namespace
+
+cudaError_t launch_index_score(const void* q_idx, const void* k_idx, int64_t k_seq_stride, int n_seq,
+                               int d_idx, bool mx, const IndexScoreParams& p, cudaStream_t stream,
+                               bool pdl) {
+  const int npad = p.H_idx <= 16 ? 16 : (p.H_idx <= 32 ? 32 : 64);
+  // queries that share one cache are scored four at a time (N = 4 x 64) when they can be
+  const bool grouped = !mx && npad == 64 && p.q_per_seq % 4 == 0 && p.T >= 4;
+  if (mx) {
+    if (d_idx != 128) return cudaErrorNotSupported;
+    if (npad == 16) return launch_cfg<true, 128, 1, 16>(q_idx, k_idx, k_seq_stride, n_seq, p, stream, pdl);
+    if (npad == 32) return launch_cfg<true, 128, 1, 32>(q_idx, k_idx, k_seq_stride, n_seq, p, stream, pdl);
+    return launch_cfg<true, 128, 1, 64>(q_idx, k_idx, k_seq_stride, n_seq, p, stream, pdl);
+  }
+  if (d_idx == 128) {
+    if (grouped) return launch_cfg<false, 128, 4, 64>(q_idx, k_idx, k_seq_stride, n_seq, p, stream, pdl);
+    if (npad == 16) return launch_cfg<false, 128, 1, 16>(q_idx, k_idx, k_seq_stride, n_seq, p, stream, pdl);
+    if (npad == 32) return launch_cfg<false, 128, 1, 32>(q_idx, k_idx, k_seq_stride, n_seq, p, stream, pdl);
+    return launch_cfg<false, 128, 1, 64>(q_idx, k_idx, k_seq_stride, n_seq, p, stream, pdl);
+  }
+  if (d_idx == 64) {
+    if (npad == 16) return launch_cfg<false, 64, 1, 16>(q_idx, k_idx, k_seq_stride, n_seq, p, stream, pdl);
+    if (npad == 32) return launch_cfg<false, 64, 1, 32>(q_idx, k_idx, k_seq_stride, n_seq, p, stream, pdl);
+    return launch_cfg<false, 64, 1, 64>(q_idx, k_idx, k_seq_stride, n_seq, p, stream, pdl);
+  }
+  return cudaErrorNotSupported;
+}
+
+}  // namespace dsa
