@@ -337,7 +337,7 @@ def run_ours(args, wl):
     err = dsa.dsa_get_device_error(stream)
     queries = wl.T * world
     value = queries / (ms * 1e-3)
-    launches_per_step = 3 + (1 if _attn_splits(wl) > 1 else 0)
+    launches_per_step = 3 * (-(-wl.T // slice_queries(wl)))  # index score, Top-K, attention
 
     # ---- per-kernel durations (component entry points, same kernels and launch shapes), events
     # on the launching stream over `reps` launches each
@@ -396,13 +396,13 @@ def run_ours(args, wl):
     return 0
 
 
-def _attn_splits(wl):
-    import top_sparse_attention_gb300 as dsa  # noqa: F401
-
-    blocks = -(-wl.K // 64)
-    groups = -(-wl.H // 16)
-    per = wl.T * groups
-    return max(1, min(blocks, 64, -(-304 // per)))
+def slice_queries(wl):
+    """Queries per launch of the chain (prefill runs in slices whose fp32 scores fit 256 MB)."""
+    if wl.q_pos0 < 0:
+        return wl.T
+    ld = max(4, (wl.L + 3) // 4 * 4)
+    tc = max(4, (256 * 2 ** 20 // (ld * 4)) // 4 * 4)
+    return min(tc, wl.T)
 
 
 def kernel_times(dsa, wl, dev_sets, stream, reps):
@@ -438,15 +438,10 @@ def kernel_times(dsa, wl, dev_sets, stream, reps):
 
     outs = [torch.empty(wl.T, wl.H, wl.D_v, dtype=torch.bfloat16, device=s["q"].device) for s in dev_sets]
     lses = [torch.empty(wl.T, wl.H, dtype=torch.float32, device=s["q"].device) for s in dev_sets]
-    from top_sparse_attention_gb300 import _native as N
-
-    ws = torch.zeros(max(16, N.lib.dsa_sparse_attn_workspace_size(wl.T, wl.H, wl.K, wl.D_v)),
-                     dtype=torch.uint8, device=dev_sets[0]["q"].device)
-
     def attn(i):
         s = dev_sets[i]
         dsa.dsa_sparse_attn(s["q"], s["kv"], idx[i], sm_scale=wl.sm_scale, kv_v=s["kv_v"], kv_scale=s["kv_scale"],
-                            D_v=wl.D_v, q_per_seq=wl.q_per_seq, out=outs[i], lse=lses[i], ws=ws, stream=stream)
+                            D_v=wl.D_v, q_per_seq=wl.q_per_seq, out=outs[i], lse=lses[i], stream=stream)
 
     out["index_score_us"] = timed(score)
     out["topk_us"] = timed(topk)

@@ -84,10 +84,11 @@ dsa_status dsa_get_device_error(int* code, void* stream);
  *   k_idx     device: sequence q of the indexer-key cache starts at k_idx + q*k_seq_stride bytes
  *             and holds L rows of d_idx elements, rows packed (row pitch = d_idx * elem size)
  *   k_idx_sf  device, DSA_MXFP8_E4M3 only: sequence q at k_idx_sf + q*k_sf_seq_stride bytes,
- *             L rows of d_idx/32 bytes, packed; else NULL
+ *             L rows of d_idx/32 bytes, packed; 4-byte aligned, k_sf_seq_stride a multiple
+ *             of 4; else NULL
  *   scores    device fp32, row t at scores + t*ld_scores (ld_scores in ELEMENTS, >= L)
  * Supported: idx_dtype DSA_BF16 with d_idx in {64, 128}; DSA_MXFP8_E4M3 with d_idx = 128;
- * 1 <= H_idx <= 64.  Pointers 16-byte aligned; k_seq_stride a multiple of 16.
+ * 1 <= H_idx <= 64.  q_idx, w, k_idx and scores 16-byte aligned; k_seq_stride a multiple of 16.
  * ------------------------------------------------------------------------------------------ */
 dsa_status dsa_index_score(const void* q_idx, const uint8_t* q_idx_sf, const float* w,
                            const void* k_idx, const uint8_t* k_idx_sf, int64_t k_seq_stride,
@@ -104,8 +105,9 @@ dsa_status dsa_index_score(const void* q_idx, const uint8_t* q_idx_sf, const flo
  * largest scores[t*ld_scores + s], exact ties resolved toward the lower position, written in
  * ascending position order, followed by -1 in the remaining slots.  Scores are compared as
  * fp32 with -0 equal to +0; NaN scores are not supported.
- *   ws / ws_bytes  device workspace of at least dsa_topk_workspace_size(T, L, K) bytes
- *                  (may be NULL when that size is 0)
+ *   ws / ws_bytes  device workspace of at least dsa_topk_workspace_size(T, L, K) bytes,
+ *                  zero-filled once before its first use (every completed call leaves it zero);
+ *                  calls sharing a workspace must not run concurrently
  * Supported: 1 <= K <= 4096.
  * ------------------------------------------------------------------------------------------ */
 dsa_status dsa_topk(const float* scores, int64_t ld_scores, int T, int q_per_seq, int q_pos0,
@@ -183,7 +185,10 @@ typedef struct dsa_args {
   const void* block_table; /* reserved for a paged cache layout; must be NULL */
 } dsa_args;
 
-/* Workspace bytes that dsa_decode (prefill = 0) or dsa_prefill (prefill = 1) needs for `a`. */
+/* Workspace bytes that dsa_decode (prefill = 0) or dsa_prefill (prefill = 1) needs for `a`.
+ * The workspace is device memory owned by the caller.  It must be zero-filled once before its
+ * first use (e.g. cudaMemsetAsync); every completed call leaves it ready for the next one.  Two
+ * calls that share a workspace must not run concurrently. */
 dsa_status dsa_workspace_size(const dsa_args* a, int prefill, size_t* bytes);
 
 dsa_status dsa_decode(const dsa_args* a, void* ws, size_t ws_bytes, void* stream);

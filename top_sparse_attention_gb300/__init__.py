@@ -2,15 +2,31 @@
 gather-driven sparse attention over a latent KV cache.
 
 The compute lives in libdsa.so (C ABI in include/dsa.h); this package is its thin Python binding.
-Importing it fails loudly when the library is not built.
+The library is loaded on first use of any entry point, and that use fails loudly when the library
+is not built (`top_sparse_attention_gb300.build` builds it; importing that submodule does not
+need the library).
 """
-from .api import (DsaCall, dsa_decode, dsa_get_device_error, dsa_index_score, dsa_prefill,  # noqa: F401
-                  dsa_sparse_attn, dsa_topk, dsa_workspace_size, ld_scores_for)
-from ._native import DsaError, LIB_PATH, EXPORTS  # noqa: F401
+import importlib
+
+_API = ("DsaCall", "dsa_decode", "dsa_get_device_error", "dsa_index_score", "dsa_prefill",
+        "dsa_sparse_attn", "dsa_topk", "dsa_workspace_size", "ld_scores_for")
+_NATIVE = ("DsaError", "LIB_PATH", "EXPORTS")
 
 INPUT_KEYS = ("q_idx", "q_idx_sf", "w", "k_idx", "k_idx_sf", "q", "kv", "kv_scale", "kv_v", "n_valid")
 
+__all__ = list(_API + _NATIVE) + ["call_from_tensors", "INPUT_KEYS"]
 
-def call_from_tensors(tensors: dict, **kw) -> DsaCall:
+
+def __getattr__(name):
+    if name in _API:
+        return getattr(importlib.import_module(".api", __name__), name)
+    if name in _NATIVE:
+        return getattr(importlib.import_module("._native", __name__), name)
+    raise AttributeError(name)
+
+
+def call_from_tensors(tensors: dict, **kw):
     """DsaCall from a dict holding the input tensors under the names of dsa_args."""
+    from .api import DsaCall
+
     return DsaCall(**{k: tensors.get(k) for k in INPUT_KEYS}, **kw)

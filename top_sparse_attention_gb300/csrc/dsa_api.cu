@@ -83,8 +83,9 @@ dsa_status check_index_score(const void* q_idx, const uint8_t* q_idx_sf, const f
   if (n_seq > 1 && (k_seq_stride % 16 != 0 || k_seq_stride < (int64_t)L * row_bytes))
     return DSA_ERR_INVALID_ARG;
   if (idx_dtype == DSA_MXFP8_E4M3) {
-    if (!q_idx_sf || !k_idx_sf || !aligned16(k_idx_sf)) return DSA_ERR_INVALID_ARG;
-    if (n_seq > 1 && (k_sf_seq_stride % 16 != 0 || k_sf_seq_stride < (int64_t)L * (d_idx / 32)))
+    // the scale rows are read with 4-byte loads (4 groups of 32 per row)
+    if (!q_idx_sf || !k_idx_sf || (reinterpret_cast<uintptr_t>(k_idx_sf) & 3u) != 0) return DSA_ERR_INVALID_ARG;
+    if (n_seq > 1 && (k_sf_seq_stride % 4 != 0 || k_sf_seq_stride < (int64_t)L * (d_idx / 32)))
       return DSA_ERR_INVALID_ARG;
   }
   return DSA_OK;
@@ -133,7 +134,7 @@ dsa_status check_sparse_attn(const void* q, const void* kv, const void* kv_v, co
 // launches of the three steps for queries [t_off, t_off + T)
 
 cudaError_t run_index_score(const dsa_args& a, int t_off, int T, float* scores, int64_t ld,
-                            cudaStream_t st, bool pdl) {
+                            uint32_t* hist, bool* hist_filled, cudaStream_t st, bool pdl) {
   const int64_t row_bytes = (int64_t)a.d_idx * (a.idx_dtype == DSA_BF16 ? 2 : 1);
   IndexScoreParams p = {};
   p.w = a.w + (int64_t)t_off * a.H_idx;
@@ -151,13 +152,14 @@ cudaError_t run_index_score(const dsa_args& a, int t_off, int T, float* scores, 
   p.t_off = t_off;
   p.tiles = (a.L + 127) / 128;
   p.err = device_error_ptr();
+  p.hist = hist;
   const uint8_t* qi = reinterpret_cast<const uint8_t*>(a.q_idx) + (int64_t)t_off * a.H_idx * row_bytes;
   return launch_index_score(qi, a.k_idx, a.k_seq_stride, a.T / a.q_per_seq, a.d_idx,
-                            a.idx_dtype == DSA_MXFP8_E4M3, p, st, pdl);
+                            a.idx_dtype == DSA_MXFP8_E4M3, p, st, pdl, hist_filled);
 }
 
 cudaError_t run_topk(const dsa_args& a, int t_off, int T, const float* scores, int64_t ld,
-                     int32_t* idx, cudaStream_t st, bool pdl) {
+                     int32_t* idx, uint32_t* hist, void* ws, cudaStream_t st, bool pdl) {
   TopkParams p = {};
   p.scores = scores;
   p.ld_scores = ld;
@@ -170,7 +172,8 @@ cudaError_t run_topk(const dsa_args& a, int t_off, int T, const float* scores, i
   p.K = a.K;
   p.t_off = t_off;
   p.err = device_error_ptr();
-  return launch_topk(p, nullptr, st, pdl);
+  p.hist = hist;
+  return launch_topk(p, ws, st, pdl);
 }
 
 cudaError_t run_sparse_attn(const dsa_args& a, int t_off, int T, const int32_t* idx, void* ws,
@@ -199,7 +202,9 @@ cudaError_t run_sparse_attn(const dsa_args& a, int t_off, int T, const int32_t* 
 }
 
 // ------------------------------------------------------------------------------------------
-// fused chain: workspace = [scores (Tc x ld fp32)] [idx (T x K int32) unless idx_out] [attn]
+// fused chain: workspace = [scores (Tc x ld fp32)] [idx (T x K int32) unless idx_out]
+//                          [score histograms (Tc x 4096 u32)] [Top-K level histograms]
+//                          [attention partials]; the histogram regions are zero between calls
 
 constexpr size_t kPrefillScoreBudget = 256ull << 20;  // score scratch per prefill slice
 
@@ -212,7 +217,7 @@ int slice_queries(const dsa_args& a, int prefill) {
 }
 
 struct Layout {
-  size_t scores, idx, attn, total;
+  size_t scores, idx, hist, topk, attn, total;
   int tc;
 };
 
@@ -224,6 +229,10 @@ Layout layout_of(const dsa_args& a, int prefill) {
   off += align_up((size_t)l.tc * ld_for(a.L) * sizeof(float), 256);
   l.idx = off;
   if (!a.idx_out) off += align_up((size_t)a.T * a.K * sizeof(int32_t), 256);
+  l.hist = off;
+  off += align_up((size_t)l.tc * kHistBins * sizeof(uint32_t), 256);
+  l.topk = off;
+  off += align_up(topk_ws_bytes(l.tc, a.L, a.K), 256);
   l.attn = off;
   off += align_up(sparse_attn_ws_bytes(l.tc, a.H, a.K, a.D_v), 256);
   l.total = off;
@@ -260,16 +269,19 @@ dsa_status run_chain(const dsa_args* a, void* ws, size_t ws_bytes, void* stream,
   float* scores = reinterpret_cast<float*>(base + l.scores);
   int32_t* idx = a->idx_out ? a->idx_out : reinterpret_cast<int32_t*>(base + l.idx);
   const int64_t ld = ld_for(a->L);
-  bool first = true;
   for (int t0 = 0; t0 < a->T; t0 += l.tc) {
     const int tn = (a->T - t0) < l.tc ? (a->T - t0) : l.tc;
     int32_t* idx_slice = idx + (int64_t)t0 * a->K;
+    uint32_t* hist = reinterpret_cast<uint32_t*>(base + l.hist);
     cudaError_t e = cudaSuccess;
-    if (a->L > 0) e = run_index_score(*a, t0, tn, scores, ld, st, !first);
-    if (e == cudaSuccess) e = run_topk(*a, t0, tn, scores, ld, idx_slice, st, a->L > 0);
+    bool filled = false;
+    // every launch may overlap its predecessor's tail (programmatic dependent launch); each
+    // kernel waits for its predecessor before reading anything that predecessor could write
+    if (a->L > 0) e = run_index_score(*a, t0, tn, scores, ld, hist, &filled, st, true);
+    if (e == cudaSuccess)
+      e = run_topk(*a, t0, tn, scores, ld, idx_slice, filled ? hist : nullptr, base + l.topk, st, true);
     if (e == cudaSuccess) e = run_sparse_attn(*a, t0, tn, idx_slice, base + l.attn, st, true);
     if (e != cudaSuccess) return from_cuda(e);
-    first = false;
   }
   return DSA_OK;
 }
@@ -351,7 +363,8 @@ dsa_status dsa_index_score(const void* q_idx, const uint8_t* q_idx_sf, const flo
   a.k_idx_sf = k_idx_sf;
   a.k_seq_stride = k_seq_stride;
   a.k_sf_seq_stride = k_sf_seq_stride;
-  return from_cuda(run_index_score(a, 0, T, scores, ld_scores, reinterpret_cast<cudaStream_t>(stream), false));
+  return from_cuda(run_index_score(a, 0, T, scores, ld_scores, nullptr, nullptr,
+                                   reinterpret_cast<cudaStream_t>(stream), false));
 }
 
 size_t dsa_topk_workspace_size(int T, int L, int K) { return topk_ws_bytes(T, L, K); }
@@ -361,7 +374,7 @@ dsa_status dsa_topk(const float* scores, int64_t ld_scores, int T, int q_per_seq
                     void* stream) {
   dsa_status s = check_topk(scores, ld_scores, T, q_per_seq, q_pos0, n_valid, L, K, idx);
   if (s != DSA_OK || T == 0) return s;
-  if (ws_bytes < topk_ws_bytes(T, L, K)) return DSA_ERR_WORKSPACE;
+  if (!ws || ws_bytes < topk_ws_bytes(T, L, K) || !aligned16(ws)) return DSA_ERR_WORKSPACE;
   if ((s = check_device()) != DSA_OK) return s;
   dsa_args a = {};
   a.T = T;
@@ -370,8 +383,7 @@ dsa_status dsa_topk(const float* scores, int64_t ld_scores, int T, int q_per_seq
   a.n_valid = n_valid;
   a.L = L;
   a.K = K;
-  (void)ws;
-  return from_cuda(run_topk(a, 0, T, scores, ld_scores, idx, reinterpret_cast<cudaStream_t>(stream), false));
+  return from_cuda(run_topk(a, 0, T, scores, ld_scores, idx, nullptr, ws, reinterpret_cast<cudaStream_t>(stream), false));
 }
 
 size_t dsa_sparse_attn_workspace_size(int T, int H, int K, int D_v) {

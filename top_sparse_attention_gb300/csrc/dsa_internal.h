@@ -48,11 +48,17 @@ struct IndexScoreParams {
   int t_off;               // global index of local query 0 (visibility and sequence use t + t_off)
   int tiles;               // ceil(L / 128) position tiles per query
   int* err;                // device error word
+  uint32_t* hist;          // [T][4096] histograms of the top 12 key bits of the scores (added
+                           // to; zero on entry), or null
 };
 
+constexpr int kHistBins = 4096;
+
+// Launches the index-score kernel.  *hist_filled reports whether p.hist was filled (only the
+// one-query-per-tile variants build it).
 cudaError_t launch_index_score(const void* q_idx, const void* k_idx, int64_t k_seq_stride,
-                               int n_seq, int d_idx, bool mx, const IndexScoreParams& p,
-                               cudaStream_t stream, bool pdl);
+                               int n_seq, int d_idx, bool mx, IndexScoreParams p,
+                               cudaStream_t stream, bool pdl, bool* hist_filled);
 
 // ---------------------------------------------------------------------------------------------
 // step 2: Top-K
@@ -65,6 +71,9 @@ struct TopkParams {
   int T, q_per_seq, q_pos0, L, K;
   int t_off;               // global index of local query 0
   int* err;                // device error word
+  uint32_t* hist;          // [T][4096] top-12-bit histograms from the index-score kernel, or
+                           // null (then built here); zeroed after use
+  uint32_t* work;          // per-query level histograms (set by launch_topk from its workspace)
 };
 
 cudaError_t launch_topk(const TopkParams& p, void* ws, cudaStream_t stream, bool pdl);

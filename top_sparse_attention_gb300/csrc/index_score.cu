@@ -10,14 +10,20 @@
 // lane = one position and all of its head columns, so ReLU, the head weights and (for MXFP8) the
 // per-group E8M0 scales are applied in registers with no cross-thread reduction.
 //
-// Warp roles (192 threads): warp 0 = producer (TMA for A, plain loads for B), warp 1 = TMEM
+// Warp roles (192 threads): warp 0 = producer (TMA for A and B), warp 1 = TMEM
 // owner and MMA issuer, warps 2-5 = epilogue.  A ring of shared-memory stages decouples loads
 // from MMAs; two TMEM accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
 // The grid is persistent: CTA c processes a contiguous range of (query group, tile) units.
 //
+// For the Top-K step, the epilogue also builds a histogram of the top 12 bits of each score's
+// order-preserving key (shared memory, flushed to a per-query global histogram with atomics on
+// non-zero bins), so selection starts with its first digit pass done.
+//
 // MXFP8: one kind::f8f6f4 MMA covers K = 32 = one scale group, so each group accumulates into
 // its own TMEM columns and the epilogue forms  sum_g 2^(ea_g) 2^(eb_g) D_g  (exact scaling of
 // fp32 partial sums by powers of two), i.e. the dequantisation happens in registers.
+#include <string.h>
+
 #include <utility>
 
 #include "dsa_internal.h"
@@ -49,14 +55,16 @@ struct Cfg {
   static constexpr int GROUPS = MX ? D / 32 : 1;  // accumulators per tile
   static constexpr int ACC_COLS = GROUPS * N;
   static constexpr int TMEM_COLS = pow2_at_least(2 * ACC_COLS);
-  static constexpr int AUX_BYTES = 1024 + 4096 + G * NPAD * 4 + G * NPAD * GROUPS * 4;
+  static constexpr int HIST_BYTES = G == 1 ? kHistBins * 4 : 0;  // fused score histogram
+  static constexpr int AUX_BYTES = 1024 + 4096 + G * NPAD * 4 + G * NPAD * GROUPS * 4 + HIST_BYTES;
   static constexpr int STAGES_FIT = (kSmemBudget - B_BUFS * B_BYTES - AUX_BYTES) / A_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int OFF_B = STAGES * A_BYTES;
   static constexpr int OFF_BAR = OFF_B + B_BUFS * B_BYTES;
   static constexpr int OFF_W = OFF_BAR + 1024;
   static constexpr int OFF_QS = OFF_W + G * NPAD * 4;
-  static constexpr int SMEM = OFF_QS + G * NPAD * GROUPS * 4 + 1024;  // + alignment slack
+  static constexpr int OFF_HIST = OFF_QS + G * NPAD * GROUPS * 4;
+  static constexpr int SMEM = OFF_HIST + HIST_BYTES + 1024;  // + alignment slack
   static_assert(N % 16 == 0 && N >= 16 && N <= 256, "MMA N out of range");
   static_assert(2 * ACC_COLS <= 512, "accumulators exceed tensor memory");
   static_assert(STAGES >= 2, "not enough shared memory for the pipeline");
@@ -77,9 +85,9 @@ struct Unit {
 };
 
 template <int G>
-__device__ __forceinline__ bool unit_of(const IndexScoreParams& p, int64_t u, Unit& x) {
-  const int g = (int)(u / p.tiles);
-  x.tile = (int)(u % p.tiles);
+__device__ __forceinline__ bool unit_of(const IndexScoreParams& p, int u, Unit& x) {
+  const int g = u / p.tiles;
+  x.tile = u - g * p.tiles;
   x.t0 = g * G;
   int n_max = 0;
 #pragma unroll
@@ -92,8 +100,8 @@ __device__ __forceinline__ bool unit_of(const IndexScoreParams& p, int64_t u, Un
 
 template <bool MX, int D, int G, int NPAD>
 __global__ void __launch_bounds__(kThreads, 1)
-index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const uint8_t* __restrict__ q_idx,
-                   const IndexScoreParams p) {
+index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+                   const uint8_t* __restrict__ q_idx, const int q_by_tma, const IndexScoreParams p) {
   using C = Cfg<MX, D, G, NPAD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -109,13 +117,15 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const uint8_t* __re
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   float* w_s = reinterpret_cast<float*>(smem + C::OFF_W);    // [G][NPAD]
   float* qs_s = reinterpret_cast<float*>(smem + C::OFF_QS);  // [G][NPAD][GROUPS]
+  uint32_t* hist_s = reinterpret_cast<uint32_t*>(smem + C::OFF_HIST);  // G == 1 only
+  const bool build_hist = G == 1 && p.hist != nullptr;
 
   const int warp = warp_id();
   const int lane = lane_id();
   const int n_groups = (p.T + G - 1) / G;
-  const int64_t U = (int64_t)n_groups * p.tiles;
-  const int64_t u_begin = U * blockIdx.x / gridDim.x;
-  const int64_t u_end = U * (blockIdx.x + 1) / gridDim.x;
+  const int64_t U = (int64_t)n_groups * p.tiles;  // < 2^31 (checked on the host)
+  const int u_begin = (int)(U * blockIdx.x / gridDim.x);
+  const int u_end = (int)(U * (blockIdx.x + 1) / gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -126,10 +136,11 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const uint8_t* __re
       mbar_init(&bfull[i], 1);
       mbar_init(&bempty[i], 1);
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 128);
+      mbar_init(&tempty[i], 4);  // one arrival per epilogue warp
     }
     fence_mbar_init();
     prefetch_tmap(&tm_k);
+    if (q_by_tma) prefetch_tmap(&tm_q);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -140,13 +151,16 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const uint8_t* __re
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // let the next kernel in the stream launch now: its CTAs take SMs as this grid's CTAs retire
+  // and wait (griddepcontrol.wait) for this grid's results before reading them
+  pdl_launch_dependents();
   pdl_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
     int it = 0, qn = -1, cur_t0 = -1;
     bool ok = true;
-    for (int64_t u = u_begin; u < u_end && ok; ++u) {
+    for (int u = u_begin; u < u_end && ok; ++u) {
       Unit x;
       if (!unit_of<G>(p, u, x)) continue;
       if (x.t0 != cur_t0) {
@@ -156,22 +170,34 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const uint8_t* __re
         if (qn >= C::B_BUFS) ok = mbar_wait(&bempty[bb], ((qn - C::B_BUFS) / C::B_BUFS) & 1, p.err);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        // B tile: rows j*NPAD + h <- q_idx row (t0 + j) * H_idx + h, zero past H_idx / T,
-        // written in the 128-byte swizzled K-major layout the MMA descriptor expects.
         uint8_t* bdst = b_s + bb * C::B_BYTES;
-        constexpr int CH = C::ROW_BYTES / 16;
-        for (int i = lane; i < C::N * CH; i += 32) {
-          const int r = i / CH, c = i % CH;
-          const int j = r / NPAD, h = r % NPAD;
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (h < p.H_idx && x.t0 + j < p.T)
-            v = *reinterpret_cast<const uint4*>(q_idx + ((int64_t)(x.t0 + j) * p.H_idx + h) * C::ROW_BYTES + c * 16);
-          const int box = c >> 3, cc = c & 7;
-          *reinterpret_cast<uint4*>(bdst + box * (C::N * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
+        if (q_by_tma) {
+          // B tile = q_idx rows t0*H_idx .. t0*H_idx + N - 1 (G*NPAD rows; rows past the last query
+          // arrive zero-filled; rows of a following query meet zero head weights)
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&bfull[bb], C::B_BYTES);
+#pragma unroll
+            for (int b = 0; b < C::BOXES; ++b)
+              tma_load_2d(bdst + b * (C::N * 128), &tm_q, &bfull[bb], b * C::BOX_COLS, x.t0 * p.H_idx);
+          }
+          __syncwarp();
+        } else {
+          // few query rows: rows j*NPAD + h <- q_idx row (t0 + j) * H_idx + h, zero past H_idx / T,
+          // written in the 128-byte swizzled K-major layout the MMA descriptor expects
+          constexpr int CH = C::ROW_BYTES / 16;
+          for (int i = lane; i < C::N * CH; i += 32) {
+            const int r = i / CH, c = i % CH;
+            const int j = r / NPAD, h = r % NPAD;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (h < p.H_idx && x.t0 + j < p.T)
+              v = *reinterpret_cast<const uint4*>(q_idx + ((int64_t)(x.t0 + j) * p.H_idx + h) * C::ROW_BYTES + c * 16);
+            const int box = c >> 3, cc = c & 7;
+            *reinterpret_cast<uint4*>(bdst + box * (C::N * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bfull[bb]);
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bfull[bb]);
       }
       const int s = it % C::STAGES;
       if (it >= C::STAGES) ok = mbar_wait(&empty[s], ((it / C::STAGES) - 1) & 1, p.err);
@@ -193,7 +219,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const uint8_t* __re
     constexpr uint32_t idesc = MX ? make_idesc(0, 0, kTileM, C::N) : make_idesc(1, 1, kTileM, C::N);
     int it = 0, qn = -1, cur_t0 = -1, ai = 0;
     bool ok = true;
-    for (int64_t u = u_begin; u < u_end && ok; ++u) {
+    for (int u = u_begin; u < u_end && ok; ++u) {
       Unit x;
       if (!unit_of<G>(p, u, x)) continue;
       if (x.t0 != cur_t0) {
@@ -237,12 +263,30 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const uint8_t* __re
     const int et = threadIdx.x - 64;
     int ai = 0, cur_t0 = -1;
     bool ok = true;
-    for (int64_t u = u_begin; u < u_end && ok; ++u) {
+    // flushes the shared histogram of query t into the global one (non-zero bins only)
+    auto flush_hist = [&](int t) {
+      for (int b = et; b < kHistBins; b += 128) {
+        const uint32_t v = hist_s[b];
+        if (v) {
+          atomicAdd(&p.hist[(int64_t)t * kHistBins + b], v);
+          hist_s[b] = 0;
+        }
+      }
+    };
+    if (build_hist)
+      for (int b = et; b < kHistBins; b += 128) hist_s[b] = 0;
+    // after a timed-out wait the epilogue warps keep walking the units (so that every named
+    // barrier below is reached by all 128 threads) but skip the waits and the tile work
+    for (int u = u_begin; u < u_end; ++u) {
       Unit x;
       if (!unit_of<G>(p, u, x)) continue;
       if (x.t0 != cur_t0) {
-        cur_t0 = x.t0;
         epi_bar();
+        if (build_hist && cur_t0 >= 0) {
+          flush_hist(cur_t0);
+          epi_bar();
+        }
+        cur_t0 = x.t0;
         for (int i = et; i < G * NPAD; i += 128) {
           const int j = i / NPAD, h = i % NPAD;
           const bool valid = h < p.H_idx && x.t0 + j < p.T;
@@ -256,6 +300,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const uint8_t* __re
         }
         epi_bar();
       }
+      if (!ok) continue;
       const int pos = x.tile * kTileM + row;
       const int seq = (x.t0 + p.t_off) / p.q_per_seq;
       float ks[C::GROUPS];
@@ -272,7 +317,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const uint8_t* __re
       }
       const int ab = ai & 1;
       ok = __all_sync(0xffffffffu, mbar_wait(&tfull[ab], (ai >> 1) & 1, p.err));
-      if (!ok) break;
+      if (!ok) continue;
       tc_fence_after();
       const uint32_t tb = tmem + ((uint32_t)(q4 * 32) << 16) + ab * C::ACC_COLS;
       float score[G];
@@ -300,14 +345,24 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const uint8_t* __re
         for (int i = 0; i < CW; ++i) score[j] = fmaf(w_s[c * CW + i], fmaxf(v[i], 0.f), score[j]);
       }
       tc_fence_before();
-      mbar_arrive(&tempty[ab]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[ab]);
 #pragma unroll
       for (int j = 0; j < G; ++j) {
         const int t = x.t0 + j;
-        if (t < p.T && pos < visible_len(t + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid))
-          p.scores[(int64_t)t * p.ld_scores + pos] = score[j];
+        const bool vis = t < p.T && pos < visible_len(t + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid);
+        if (vis) p.scores[(int64_t)t * p.ld_scores + pos] = score[j];
+        if (build_hist) {
+          const uint32_t bin = vis ? (float_key(score[j]) >> 20) : 0xFFFFFFFFu;
+          const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+          if (vis && lane == __ffs(peers) - 1) atomicAdd(&hist_s[bin], __popc(peers));
+        }
       }
       ++ai;
+    }
+    if (build_hist && cur_t0 >= 0) {
+      epi_bar();
+      flush_hist(cur_t0);
     }
   }
 
@@ -317,7 +372,6 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const uint8_t* __re
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
-  pdl_launch_dependents();
 }
 
 template <bool MX, int D, int G, int NPAD>
@@ -333,6 +387,18 @@ cudaError_t launch_cfg(const void* q_idx, const void* k_idx, int64_t k_seq_strid
                                  3, const_cast<void*>(k_idx), dims, strides, box,
                                  CU_TENSOR_MAP_SWIZZLE_128B);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  // q_idx rows by TMA when the box of N rows fits inside the T * H_idx rows of the tensor
+  CUtensorMap tq;
+  memset(&tq, 0, sizeof(tq));
+  const int q_by_tma = (int64_t)p.T * p.H_idx >= C::N ? 1 : 0;
+  if (q_by_tma) {
+    const cuuint64_t qdims[2] = {(cuuint64_t)D, (cuuint64_t)p.T * p.H_idx};
+    const cuuint64_t qstrides[1] = {(cuuint64_t)C::ROW_BYTES};
+    const cuuint32_t qbox[2] = {(cuuint32_t)C::BOX_COLS, (cuuint32_t)C::N};
+    r = encode_tensor_map(&tq, MX ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                          const_cast<void*>(q_idx), qdims, qstrides, qbox, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
   auto kern = index_score_kernel<MX, D, G, NPAD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
@@ -340,20 +406,23 @@ cudaError_t launch_cfg(const void* q_idx, const void* k_idx, int64_t k_seq_strid
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t units = (int64_t)((p.T + G - 1) / G) * p.tiles;
+  if (units >= (1ll << 31)) return cudaErrorNotSupported;
   const int grid = (int)(units < sms ? units : sms);
   if (grid <= 0) return cudaSuccess;
-  return launch_kernel(kern, dim3(grid), dim3(kThreads), C::SMEM, stream, pdl, tm,
-                       reinterpret_cast<const uint8_t*>(q_idx), p);
+  return launch_kernel(kern, dim3(grid), dim3(kThreads), C::SMEM, stream, pdl, tm, tq,
+                       reinterpret_cast<const uint8_t*>(q_idx), q_by_tma, p);
 }
 
 }  // namespace
 
 cudaError_t launch_index_score(const void* q_idx, const void* k_idx, int64_t k_seq_stride, int n_seq,
-                               int d_idx, bool mx, const IndexScoreParams& p, cudaStream_t stream,
-                               bool pdl) {
+                               int d_idx, bool mx, IndexScoreParams p, cudaStream_t stream, bool pdl,
+                               bool* hist_filled) {
   const int npad = p.H_idx <= 16 ? 16 : (p.H_idx <= 32 ? 32 : 64);
   // queries that share one cache are scored four at a time (N = 4 x 64) when they can be
   const bool grouped = !mx && npad == 64 && p.q_per_seq % 4 == 0 && p.T >= 4;
+  if (grouped) p.hist = nullptr;  // the fused histogram is built by the one-query variants only
+  if (hist_filled) *hist_filled = p.hist != nullptr;
   if (mx) {
     if (d_idx != 128) return cudaErrorNotSupported;
     if (npad == 16) return launch_cfg<true, 128, 1, 16>(q_idx, k_idx, k_seq_stride, n_seq, p, stream, pdl);

@@ -4,50 +4,55 @@
 // K/V by the index table then runs a small matrix multiply, "Achieving Day-0 Readiness...",
 // section 2.3; FP8 KV cache, Key Optimization 2 of the first page).
 //
-// One CTA = (query t, split of the K selected rows, group of 16 heads).  Rows arrive in blocks
-// of 64 by 16-byte copies straight into shared memory (no DRAM staging buffer); the 16 heads
-// form the M = 16 side of warp-level bf16 tensor-core MMAs, so every gathered row is read from
-// HBM once and used by all heads.  Softmax is online across blocks (running max / sum); when K
-// is split over several CTAs each writes (o, m, l) partials and a second kernel merges them
-// with a log-sum-exp combine.  FP8 rows are widened to bf16 in registers on the way into shared
-// memory (exact: every E4M3 value is a bf16 value); the per-row scale is folded into the logit
-// and into the probability that multiplies V.
+// One CTA = (split of the K selected rows, query t, group of 16 heads).  Each selected row is
+// fetched by a single bulk copy on the TMA engine (cp.async.bulk, completion counted on an
+// mbarrier) straight into shared memory; rows are padded by 16 bytes so that ldmatrix reads of 8
+// consecutive rows hit distinct banks.  Blocks of 64 rows go to two load slots, so two blocks
+// are always in flight.  The 16 heads form the M = 16 side of warp-level bf16 tensor-core MMAs,
+// so every gathered row is read from HBM once and used by all heads; softmax is online across
+// blocks (running max / sum, log2 domain).
+//
+// bf16 rows: two groups of 4 warps work on the two slots at the same time and merge their
+// (m, l, o) in shared memory at the end.  E4M3 rows (one group): the raw block is widened to bf16
+// in registers (exact: every E4M3 value is a bf16 value) into a compute buffer; the per-row scale
+// is folded into the logit and into the probability that multiplies V.
+//
+// When K is split over S > 1 CTAs (so a small batch still covers every SM), each CTA writes its
+// partial (o, m, l) and a second kernel merges them with a log-sum-exp combine.
 #include "dsa_internal.h"
 
 namespace dsa {
 
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kHeads = 16;   // heads per CTA (M of m16n8k16)
-constexpr int kRows = 64;    // gathered rows per block
-constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kHeads = 16;    // heads per CTA (M of m16n8k16)
+constexpr int kRows = 64;     // gathered rows per block
+constexpr int kMaxRows = 4096;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// Byte offset of 16-byte chunk c of row r in a swizzled bf16 tile whose rows hold `chunks`
-// chunks (a multiple of 8): the chunk index is XORed with (r & 7) so that the 8 rows an
-// ldmatrix phase touches fall in distinct banks.
+// 16-byte chunk c of row r of a swizzled tile with `chunks` chunks per row (a multiple of 8).
 __device__ __forceinline__ uint32_t swz(int r, int c, int chunks) {
   return (uint32_t)((r * chunks + (c ^ (r & 7))) * 16);
 }
 
 template <int DQK, int DV, bool FP8, bool SEPV>
-struct Smem {
-  static constexpr int QK_CHUNKS = DQK / 8;
-  static constexpr int V_CHUNKS = DV / 8;
+struct Cfg {
+  static constexpr int GROUPS = FP8 ? 1 : 2;             // warp groups of 4 warps
+  static constexpr int THREADS = 128 * GROUPS;
+  static constexpr int ROW = DQK * 2 + 16;               // padded bf16 row (bytes)
+  static constexpr int VROW = SEPV ? DV * 2 + 16 : 0;    // padded bf16 V row
+  static constexpr int RAWROW = FP8 ? DQK + 16 : 0;      // padded E4M3 row
+  static constexpr int SLOT = FP8 ? kRows * RAWROW : kRows * (ROW + VROW);  // one load slot
+  static constexpr int CBUF = FP8 ? kRows * ROW : 0;     // bf16 compute buffer (FP8)
   static constexpr int P_CHUNKS = kRows / 8;
-  static constexpr int Q_BYTES = kHeads * DQK * 2;
-  static constexpr int KV_BYTES = kRows * DQK * 2;
-  static constexpr int V_BYTES = SEPV ? kRows * DV * 2 : 0;
-  static constexpr int P_BYTES = kHeads * kRows * 2;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = OFF_Q + Q_BYTES;
-  static constexpr int OFF_V = OFF_KV + KV_BYTES;
-  static constexpr int OFF_P = OFF_V + V_BYTES;
-  static constexpr int OFF_IDX = OFF_P + P_BYTES;
-  static constexpr int OFF_SCALE = OFF_IDX + kRows * 4;
-  static constexpr int OFF_RED = OFF_SCALE + kRows * 4;
-  static constexpr int BYTES = OFF_RED + 2 * 4 * kHeads * 4;
+  static constexpr int OFF_SLOT = OFF_Q + kHeads * ROW;
+  static constexpr int OFF_CBUF = OFF_SLOT + 2 * SLOT;
+  static constexpr int OFF_P = OFF_CBUF + CBUF;                      // per group
+  static constexpr int OFF_RED = OFF_P + GROUPS * kHeads * kRows * 2;  // per group: max, sum
+  static constexpr int OFF_BAR = OFF_RED + GROUPS * 2 * 4 * kHeads * 4;
+  static constexpr int OFF_IDX = OFF_BAR + 64;
+  static int bytes(int rows) { return OFF_IDX + rows * 4 * (FP8 ? 2 : 1); }
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -64,47 +69,132 @@ __device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
   return make_uint2(pack_bf16(f0.x, f0.y), pack_bf16(f1.x, f1.y));
 }
 
+// Bulk copy of `bytes` (a multiple of 16) from global to shared memory on the TMA engine.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void group_sync(int g) {
+  asm volatile("bar.sync %0, 128;" ::"r"(g + 1) : "memory");
+}
+
 template <int DQK, int DV, bool FP8, bool SEPV>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(Cfg<DQK, DV, FP8, SEPV>::THREADS, 1)
 sparse_attn_kernel(const SparseAttnParams p) {
-  using S = Smem<DQK, DV, FP8, SEPV>;
+  using C = Cfg<DQK, DV, FP8, SEPV>;
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* q_s = smem + S::OFF_Q;
-  uint8_t* kv_s = smem + S::OFF_KV;
-  uint8_t* v_s = SEPV ? smem + S::OFF_V : kv_s;
-  uint8_t* p_s = smem + S::OFF_P;
-  int* idx_s = reinterpret_cast<int*>(smem + S::OFF_IDX);
-  float* scale_s = reinterpret_cast<float*>(smem + S::OFF_SCALE);
-  float* red_max = reinterpret_cast<float*>(smem + S::OFF_RED);
-  float* red_sum = red_max + 4 * kHeads;
+  pdl_launch_dependents();  // the combine kernel may launch now; it waits for this grid's results
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
-  const int warp = tid >> 5;
+  const int g = tid >> 7;          // warp group
+  const int gw = (tid >> 5) & 3;   // warp within the group
+  const int gt = tid & 127;        // thread within the group
   const int split = blockIdx.x;
   const int t = blockIdx.y;
   const int h0 = blockIdx.z * kHeads;
   const int seq = (t + p.t_off) / p.q_per_seq;
   const int row_begin = split * p.rows_per_split;
   const int row_end = min(p.K, row_begin + p.rows_per_split);
+  const int nrows = max(0, row_end - row_begin);
+  const int nblk = (nrows + kRows - 1) / kRows;
+
+  uint8_t* q_s = smem + C::OFF_Q;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);  // [0,1] slots, [2] q
+  int* idx_s = reinterpret_cast<int*>(smem + C::OFF_IDX);
+  float* scale_s = reinterpret_cast<float*>(smem + C::OFF_IDX + p.rows_per_split * 4);
+  uint8_t* p_s = smem + C::OFF_P + g * kHeads * kRows * 2;
+  float* red_max = reinterpret_cast<float*>(smem + C::OFF_RED) + g * 2 * 4 * kHeads;
+  float* red_sum = red_max + 4 * kHeads;
 
   const uint8_t* kv_base = p.kv + (int64_t)seq * p.kv_seq_stride;
   const uint8_t* v_base = SEPV ? p.kv_v + (int64_t)seq * p.v_seq_stride : nullptr;
   const float* scale_base = FP8 ? p.kv_scale + (int64_t)seq * p.L : nullptr;
 
-  // q rows h0 .. h0+15 (rows past H are zero); q is a caller input, so it is fetched before
-  // waiting for the kernel that produces the index rows
-  {
-    const __nv_bfloat16* qg = p.q + ((int64_t)t * p.H) * DQK;
-    for (int id = tid; id < kHeads * S::QK_CHUNKS; id += kThreads) {
-      const int r = id / S::QK_CHUNKS, c = id % S::QK_CHUNKS;
-      const bool ok = (h0 + r) < p.H;
-      const void* src = ok ? (const void*)(qg + (int64_t)(h0 + r) * DQK + c * 8) : (const void*)p.q;
-      cp_async16(q_s + swz(r, c, S::QK_CHUNKS), src, ok);
-    }
-    cp_async_commit();
+  if (tid == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    mbar_init(&bars[2], 1);
+    fence_mbar_init();
   }
+  __syncthreads();
+  // q rows h0 .. h0+15 (a caller input, so fetched before waiting for the previous kernel);
+  // rows past H are zero
+  if (tid < kHeads) {
+    const int h = h0 + tid;
+    if (h < p.H) {
+      mbar_expect_tx(&bars[2], DQK * 2);
+      bulk_g2s(q_s + tid * C::ROW, p.q + ((int64_t)t * p.H + h) * DQK, DQK * 2, &bars[2]);
+    } else {
+      for (int c = 0; c < DQK / 8; ++c) *reinterpret_cast<uint4*>(q_s + tid * C::ROW + c * 16) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  __syncthreads();
+  if (tid == 0) mbar_arrive(&bars[2]);
   pdl_wait();  // the index rows come from the previous kernel in the stream
+
+  // this CTA's index rows (and FP8 row scales), checked against [-1, L)
+  for (int j = tid; j < nblk * kRows; j += C::THREADS) {
+    int i = -1;
+    if (j < nrows) {
+      i = p.idx[(int64_t)t * p.K + row_begin + j];
+      if (i < -1 || i >= p.L) {
+        record_error(p.err, DSA_DEVERR_INDEX_RANGE);
+        i = -1;
+      }
+    }
+    idx_s[j] = i;
+    if (FP8) scale_s[j] = (i >= 0) ? scale_base[i] : 0.f;
+  }
+  __syncthreads();
+
+  // block b -> slot b & 1, issued by the group that owns the slot; missing rows are zero-filled
+  auto issue = [&](int b) {
+    uint8_t* slot = smem + C::OFF_SLOT + (b & 1) * C::SLOT;
+    uint64_t* bar = &bars[b & 1];
+    fence_proxy_async_smem();  // earlier generic reads / zero-fills of this slot come first
+    for (int r = gt; r < kRows; r += 128) {
+      const int i = idx_s[b * kRows + r];
+      if (FP8) {
+        uint8_t* dst = slot + r * C::RAWROW;
+        if (i >= 0) {
+          mbar_expect_tx(bar, DQK);
+          bulk_g2s(dst, kv_base + (int64_t)i * p.kv_row_stride, DQK, bar);
+        } else {
+          for (int c = 0; c < DQK / 16; ++c) *reinterpret_cast<uint4*>(dst + c * 16) = make_uint4(0, 0, 0, 0);
+        }
+      } else {
+        uint8_t* dst = slot + r * C::ROW;
+        if (i >= 0) {
+          mbar_expect_tx(bar, DQK * 2 + (SEPV ? DV * 2 : 0));
+          bulk_g2s(dst, kv_base + (int64_t)i * p.kv_row_stride, DQK * 2, bar);
+          if (SEPV) bulk_g2s(slot + kRows * C::ROW + r * C::VROW, v_base + (int64_t)i * p.v_row_stride, DV * 2, bar);
+        } else {
+          for (int c = 0; c < DQK / 8; ++c) *reinterpret_cast<uint4*>(dst + c * 16) = make_uint4(0, 0, 0, 0);
+          if (SEPV)
+            for (int c = 0; c < DV / 8; ++c)
+              *reinterpret_cast<uint4*>(slot + kRows * C::ROW + r * C::VROW + c * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+    }
+    group_sync(g);  // every expect_tx of the block precedes the arrival that opens the phase
+    if (gt == 0) mbar_arrive(bar);
+  };
+  if (C::GROUPS == 2) {
+    if (g < nblk) issue(g);
+  } else {
+    if (nblk > 0) issue(0);
+    if (nblk > 1) issue(1);
+  }
+  bool ok = mbar_wait(&bars[2], 0, p.err);  // q is in shared memory
 
   // per-thread softmax state for heads r0 = lane/4 and r1 = lane/4 + 8
   const int r0 = lane >> 2, r1 = r0 + 8;
@@ -115,88 +205,41 @@ sparse_attn_kernel(const SparseAttnParams p) {
 #pragma unroll
   for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
-  for (int blk = row_begin; blk < row_end; blk += kRows) {
-    const int nrows = min(kRows, row_end - blk);
-    if (tid < kRows) {
-      int i = -1;
-      if (tid < nrows) {
-        i = p.idx[(int64_t)t * p.K + blk + tid];
-        if (i < -1 || i >= p.L) {
-          record_error(p.err, DSA_DEVERR_INDEX_RANGE);
-          i = -1;
-        }
-      }
-      idx_s[tid] = i;
-      if (FP8) scale_s[tid] = (i >= 0) ? scale_base[i] : 0.f;
-    }
-    __syncthreads();
-
-    // gather: 16-byte pieces, consecutive threads on consecutive pieces of one row
-    if (!FP8) {
-      for (int id = tid; id < kRows * S::QK_CHUNKS; id += kThreads) {
-        const int r = id / S::QK_CHUNKS, c = id % S::QK_CHUNKS;
-        const int i = idx_s[r];
-        const uint8_t* src = (i >= 0) ? kv_base + (int64_t)i * p.kv_row_stride + c * 16 : p.kv;
-        cp_async16(kv_s + swz(r, c, S::QK_CHUNKS), src, i >= 0);
-      }
-      if (SEPV) {
-        for (int id = tid; id < kRows * S::V_CHUNKS; id += kThreads) {
-          const int r = id / S::V_CHUNKS, c = id % S::V_CHUNKS;
-          const int i = idx_s[r];
-          const uint8_t* src = (i >= 0) ? v_base + (int64_t)i * p.v_row_stride + c * 16 : p.kv;
-          cp_async16(v_s + swz(r, c, S::V_CHUNKS), src, i >= 0);
-        }
-      }
-      cp_async_commit();
-    } else {
-      // E4M3 row = DQK bytes = DQK/16 pieces of 16 codes; each piece becomes two bf16 chunks
+  int use = 0;  // how many blocks this group has consumed (mbarrier phase of its slots)
+  for (int b = (C::GROUPS == 2 ? g : 0); b < nblk; b += C::GROUPS, ++use) {
+    const int slot_i = b & 1;
+    ok = ok && mbar_wait(&bars[slot_i], (uint32_t)((C::GROUPS == 2 ? use : (use >> 1)) & 1), p.err);
+    const int* ib = idx_s + b * kRows;
+    const float* sb = scale_s + b * kRows;
+    uint8_t* slot = smem + C::OFF_SLOT + slot_i * C::SLOT;
+    uint8_t* kv_s = FP8 ? smem + C::OFF_CBUF : slot;
+    uint8_t* v_s = SEPV ? slot + kRows * C::ROW : kv_s;
+    constexpr int VR = SEPV ? C::VROW : C::ROW;
+    if (FP8) {
       constexpr int PIECES = DQK / 16;
-      constexpr int PER_THREAD = (kRows * PIECES + kThreads - 1) / kThreads;
-      constexpr int BATCH = 6;
-#pragma unroll
-      for (int b0 = 0; b0 < PER_THREAD; b0 += BATCH) {
-        uint4 raw[BATCH];
-#pragma unroll
-        for (int j = 0; j < BATCH; ++j) {
-          const int id = tid + (b0 + j) * kThreads;
-          raw[j] = make_uint4(0, 0, 0, 0);
-          if (b0 + j < PER_THREAD && id < kRows * PIECES) {
-            const int r = id / PIECES, c = id % PIECES;
-            const int i = idx_s[r];
-            if (i >= 0)
-              raw[j] = __ldg(reinterpret_cast<const uint4*>(kv_base + (int64_t)i * p.kv_row_stride +
-                                                            c * 16));
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < BATCH; ++j) {
-          const int id = tid + (b0 + j) * kThreads;
-          if (b0 + j < PER_THREAD && id < kRows * PIECES) {
-            const int r = id / PIECES, c = id % PIECES;
-            const uint2 a = e4m3x4_to_bf16x4(raw[j].x), b = e4m3x4_to_bf16x4(raw[j].y);
-            const uint2 cc = e4m3x4_to_bf16x4(raw[j].z), d = e4m3x4_to_bf16x4(raw[j].w);
-            *reinterpret_cast<uint4*>(kv_s + swz(r, 2 * c, S::QK_CHUNKS)) = make_uint4(a.x, a.y, b.x, b.y);
-            *reinterpret_cast<uint4*>(kv_s + swz(r, 2 * c + 1, S::QK_CHUNKS)) = make_uint4(cc.x, cc.y, d.x, d.y);
-          }
-        }
+      for (int id = gt; id < kRows * PIECES; id += 128) {
+        const int r = id / PIECES, c = id % PIECES;
+        const uint4 w = *reinterpret_cast<const uint4*>(slot + r * C::RAWROW + c * 16);
+        const uint2 a = e4m3x4_to_bf16x4(w.x), bb = e4m3x4_to_bf16x4(w.y);
+        const uint2 cc = e4m3x4_to_bf16x4(w.z), d = e4m3x4_to_bf16x4(w.w);
+        *reinterpret_cast<uint4*>(kv_s + r * C::ROW + 32 * c) = make_uint4(a.x, a.y, bb.x, bb.y);
+        *reinterpret_cast<uint4*>(kv_s + r * C::ROW + 32 * c + 16) = make_uint4(cc.x, cc.y, d.x, d.y);
       }
+      group_sync(g);
+      if (ok && b + 2 < nblk) issue(b + 2);  // the raw slot of block b is free again
     }
-    cp_async_wait<0>();
-    __syncthreads();
 
-    // ---- S = q . K^T : warp w owns block rows [16w, 16w+16) as two n-tiles of 8
+    // ---- S = q . K^T : warp gw owns block rows [16gw, 16gw+16) as two n-tiles of 8
     float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     {
       const int mat = lane >> 3, rr = lane & 7;
-      const uint32_t q_base = smem_u32(q_s);
-      const uint32_t kv_base_s = smem_u32(kv_s);
-      const int qa_row = rr + (mat & 1) * 8;
-      const int kb_row = warp * 16 + rr + (mat >> 1) * 8;
+      const uint32_t qa = smem_u32(q_s) + (rr + (mat & 1) * 8) * C::ROW + (mat >> 1) * 16;
+      const uint32_t kb = smem_u32(kv_s) + (gw * 16 + rr + (mat >> 1) * 8) * C::ROW + (mat & 1) * 16;
 #pragma unroll 4
       for (int ks = 0; ks < DQK / 16; ++ks) {
         uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-        ldsm_x4(q_base + swz(qa_row, 2 * ks + (mat >> 1), S::QK_CHUNKS), a0, a1, a2, a3);
-        ldsm_x4(kv_base_s + swz(kb_row, 2 * ks + (mat & 1), S::QK_CHUNKS), b0, b1, b2, b3);
+        ldsm_x4(qa + ks * 32, a0, a1, a2, a3);
+        ldsm_x4(kb + ks * 32, b0, b1, b2, b3);
         mma_bf16_16816(s[0], a0, a1, a2, a3, b0, b1);
         mma_bf16_16816(s[1], a0, a1, a2, a3, b2, b3);
       }
@@ -208,10 +251,10 @@ sparse_attn_kernel(const SparseAttnParams p) {
     for (int j = 0; j < 2; ++j) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int pos = warp * 16 + j * 8 + (lane & 3) * 2 + (e & 1);
+        const int pos = gw * 16 + j * 8 + (lane & 3) * 2 + (e & 1);
         float x = s[j][e] * p.scale_log2;
-        if (FP8) x *= scale_s[pos];
-        if (idx_s[pos] < 0) x = -INFINITY;
+        if (FP8) x *= sb[pos];
+        if (ib[pos] < 0) x = -INFINITY;
         s[j][e] = x;
         mx[e >> 1] = fmaxf(mx[e >> 1], x);
       }
@@ -222,16 +265,16 @@ sparse_attn_kernel(const SparseAttnParams p) {
       mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], 2));
     }
     if ((lane & 3) == 0) {
-      red_max[warp * kHeads + r0] = mx[0];
-      red_max[warp * kHeads + r1] = mx[1];
+      red_max[gw * kHeads + r0] = mx[0];
+      red_max[gw * kHeads + r1] = mx[1];
     }
-    __syncthreads();
+    group_sync(g);
     float m_use[2], alpha[2];
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const int h = hh ? r1 : r0;
-      float mb = fmaxf(fmaxf(red_max[h], red_max[kHeads + h]),
-                       fmaxf(red_max[2 * kHeads + h], red_max[3 * kHeads + h]));
+      const float mb = fmaxf(fmaxf(red_max[h], red_max[kHeads + h]),
+                             fmaxf(red_max[2 * kHeads + h], red_max[3 * kHeads + h]));
       const float m_new = fmaxf(m_run[hh], mb);
       m_use[hh] = (m_new == -INFINITY) ? 0.f : m_new;
       alpha[hh] = exp2f(m_run[hh] - m_use[hh]);
@@ -240,18 +283,18 @@ sparse_attn_kernel(const SparseAttnParams p) {
     float psum[2] = {0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      const int pos0 = warp * 16 + j * 8 + (lane & 3) * 2;
+      const int pos0 = gw * 16 + j * 8 + (lane & 3) * 2;
       float pv[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         pv[e] = exp2f(s[j][e] - m_use[e >> 1]);
         psum[e >> 1] += pv[e];
-        if (FP8) pv[e] *= scale_s[pos0 + (e & 1)];  // V rows carry the same per-row scale
+        if (FP8) pv[e] *= sb[pos0 + (e & 1)];  // V rows carry the same per-row scale
       }
       // P is stored [head][position], swizzled in 16-byte chunks of 8 positions
       const int c = pos0 >> 3, within = (pos0 & 7) * 2;
-      *reinterpret_cast<uint32_t*>(p_s + swz(r0, c, S::P_CHUNKS) + within) = pack_bf16(pv[0], pv[1]);
-      *reinterpret_cast<uint32_t*>(p_s + swz(r1, c, S::P_CHUNKS) + within) = pack_bf16(pv[2], pv[3]);
+      *reinterpret_cast<uint32_t*>(p_s + swz(r0, c, C::P_CHUNKS) + within) = pack_bf16(pv[0], pv[1]);
+      *reinterpret_cast<uint32_t*>(p_s + swz(r1, c, C::P_CHUNKS) + within) = pack_bf16(pv[2], pv[3]);
     }
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
@@ -259,8 +302,8 @@ sparse_attn_kernel(const SparseAttnParams p) {
       psum[hh] += __shfl_xor_sync(0xffffffffu, psum[hh], 2);
     }
     if ((lane & 3) == 0) {
-      red_sum[warp * kHeads + r0] = psum[0];
-      red_sum[warp * kHeads + r1] = psum[1];
+      red_sum[gw * kHeads + r0] = psum[0];
+      red_sum[gw * kHeads + r1] = psum[1];
     }
 #pragma unroll
     for (int i = 0; i < NT; ++i) {
@@ -269,40 +312,70 @@ sparse_attn_kernel(const SparseAttnParams p) {
       acc[i][2] *= alpha[1];
       acc[i][3] *= alpha[1];
     }
-    __syncthreads();
+    group_sync(g);
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const int h = hh ? r1 : r0;
-      const float sb = red_sum[h] + red_sum[kHeads + h] + red_sum[2 * kHeads + h] + red_sum[3 * kHeads + h];
-      l_run[hh] = l_run[hh] * alpha[hh] + sb;
+      const float sum = red_sum[h] + red_sum[kHeads + h] + red_sum[2 * kHeads + h] + red_sum[3 * kHeads + h];
+      l_run[hh] = l_run[hh] * alpha[hh] + sum;
     }
 
-    // ---- O += P . V : warp w owns value columns [w*DV/4, (w+1)*DV/4)
+    // ---- O += P . V : warp gw owns value columns [gw*DV/4, (gw+1)*DV/4)
     {
       const int mat = lane >> 3, rr = lane & 7;
       const uint32_t p_base = smem_u32(p_s);
-      const uint32_t v_base_s = smem_u32(v_s);
-      constexpr int VCH = SEPV ? S::V_CHUNKS : S::QK_CHUNKS;  // chunks per smem row holding V
+      const uint32_t vb = smem_u32(v_s) + (rr + (mat & 1) * 8) * VR + (gw * (DV / 4) + (mat >> 1) * 8) * 2;
 #pragma unroll
       for (int kk = 0; kk < kRows / 16; ++kk) {
         uint32_t a0, a1, a2, a3;
-        ldsm_x4(p_base + swz(rr + (mat & 1) * 8, 2 * kk + (mat >> 1), S::P_CHUNKS), a0, a1, a2, a3);
-        const int vrow = kk * 16 + rr + (mat & 1) * 8;
+        ldsm_x4(p_base + swz(rr + (mat & 1) * 8, 2 * kk + (mat >> 1), C::P_CHUNKS), a0, a1, a2, a3);
 #pragma unroll
         for (int nt = 0; nt < NT; nt += 2) {
-          const int col_chunk = (warp * (DV / 4)) / 8 + nt + (mat >> 1);
           uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(v_base_s + swz(vrow, col_chunk, VCH), b0, b1, b2, b3);
+          ldsm_x4_t(vb + kk * 16 * VR + nt * 16, b0, b1, b2, b3);
           mma_bf16_16816(acc[nt], a0, a1, a2, a3, b0, b1);
           mma_bf16_16816(acc[nt + 1], a0, a1, a2, a3, b2, b3);
         }
       }
     }
-    __syncthreads();  // smem is rewritten by the next block
+    group_sync(g);  // the slot and P are rewritten next
+    if (!FP8 && ok && b + 2 < nblk) issue(b + 2);
+  }
+  // ---- merge the second group into the first (bf16 only)
+  if (C::GROUPS == 2) {
+    __syncthreads();  // all slots are idle: reuse slot 1 as staging
+    float* stage = reinterpret_cast<float*>(smem + C::OFF_SLOT + C::SLOT);
+    float2* ml = reinterpret_cast<float2*>(smem + C::OFF_P);  // P of group 0 is idle as well
+    if (g == 1) {
+      float4* st = reinterpret_cast<float4*>(stage) + (size_t)gt * NT;
+#pragma unroll
+      for (int i = 0; i < NT; ++i) st[i] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      if (gw == 0 && (lane & 3) == 0) {
+        ml[r0] = make_float2(m_run[0], l_run[0]);
+        ml[r1] = make_float2(m_run[1], l_run[1]);
+      }
+    }
+    __syncthreads();
+    if (g == 1) return;
+    const float4* st = reinterpret_cast<const float4*>(stage) + (size_t)gt * NT;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const float2 o = ml[hh ? r1 : r0];
+      const float m_new = fmaxf(m_run[hh], o.x);
+      const float mu = (m_new == -INFINITY) ? 0.f : m_new;
+      const float a0 = exp2f(m_run[hh] - mu), a1 = exp2f(o.x - mu);
+      l_run[hh] = l_run[hh] * a0 + o.y * a1;
+      m_run[hh] = m_new;
+#pragma unroll
+      for (int i = 0; i < NT; ++i) {
+        const float4 v = st[i];
+        acc[i][2 * hh] = acc[i][2 * hh] * a0 + (hh ? v.z : v.x) * a1;
+        acc[i][2 * hh + 1] = acc[i][2 * hh + 1] * a0 + (hh ? v.w : v.y) * a1;
+      }
+    }
   }
 
-  // ---- results for heads h0 + r0, h0 + r1
-  const int col0 = warp * (DV / 4) + (lane & 3) * 2;
+  const int col0 = gw * (DV / 4) + (lane & 3) * 2;
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
     const int h = h0 + (hh ? r1 : r0);
@@ -311,11 +384,9 @@ sparse_attn_kernel(const SparseAttnParams p) {
       const float inv = l_run[hh] > 0.f ? 1.f / l_run[hh] : 0.f;
       __nv_bfloat16* o = p.out + ((int64_t)t * p.H + h) * DV;
 #pragma unroll
-      for (int i = 0; i < NT; ++i) {
-        *reinterpret_cast<uint32_t*>(o + col0 + i * 8) =
-            pack_bf16(acc[i][2 * hh] * inv, acc[i][2 * hh + 1] * inv);
-      }
-      if (p.lse && (lane & 3) == 0 && warp == 0)
+      for (int i = 0; i < NT; ++i)
+        *reinterpret_cast<uint32_t*>(o + col0 + i * 8) = pack_bf16(acc[i][2 * hh] * inv, acc[i][2 * hh + 1] * inv);
+      if (p.lse && (lane & 3) == 0 && gw == 0)
         p.lse[(int64_t)t * p.H + h] = l_run[hh] > 0.f ? (m_run[hh] + log2f(l_run[hh])) * kLn2 : -INFINITY;
     } else {
       const int64_t row = ((int64_t)t * p.H + h) * p.splits + split;
@@ -323,17 +394,17 @@ sparse_attn_kernel(const SparseAttnParams p) {
 #pragma unroll
       for (int i = 0; i < NT; ++i)
         *reinterpret_cast<float2*>(o + col0 + i * 8) = make_float2(acc[i][2 * hh], acc[i][2 * hh + 1]);
-      if ((lane & 3) == 0 && warp == 0)
+      if ((lane & 3) == 0 && gw == 0)
         *reinterpret_cast<float2*>(p.part_ml + row * 2) = make_float2(m_run[hh], l_run[hh]);
     }
   }
-  pdl_launch_dependents();
 }
 
-// Merge split partials: out = sum_j 2^(m_j - M) o_j / sum_j 2^(m_j - M) l_j,
+// Merges split partials: out = sum_j 2^(m_j - M) o_j / sum_j 2^(m_j - M) l_j and
 // lse = (M + log2 sum_j 2^(m_j - M) l_j) * ln 2.  One CTA per (query, head).
 template <int DV>
 __global__ void __launch_bounds__(DV / 4) lse_combine_kernel(const SparseAttnParams p) {
+  pdl_launch_dependents();
   pdl_wait();
   const int t = blockIdx.x, h = blockIdx.y;
   const int64_t row = ((int64_t)t * p.H + h) * p.splits;
@@ -359,17 +430,17 @@ __global__ void __launch_bounds__(DV / 4) lse_combine_kernel(const SparseAttnPar
   *reinterpret_cast<uint2*>(out) = make_uint2(pack_bf16(o.x * inv, o.y * inv), pack_bf16(o.z * inv, o.w * inv));
   if (p.lse && threadIdx.x == 0)
     p.lse[(int64_t)t * p.H + h] = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
-  pdl_launch_dependents();
 }
 
 template <int DQK, int DV, bool FP8, bool SEPV>
 cudaError_t launch_variant(const SparseAttnParams& p, cudaStream_t stream, bool pdl) {
-  using S = Smem<DQK, DV, FP8, SEPV>;
+  using C = Cfg<DQK, DV, FP8, SEPV>;
   auto kern = sparse_attn_kernel<DQK, DV, FP8, SEPV>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
+  const int smem = C::bytes(p.rows_per_split);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.splits, p.T, (p.H + kHeads - 1) / kHeads);
-  e = launch_kernel(kern, grid, dim3(kThreads), S::BYTES, stream, pdl, p);
+  e = launch_kernel(kern, grid, dim3(C::THREADS), smem, stream, pdl, p);
   if (e != cudaSuccess || p.splits == 1) return e;
   return launch_kernel(lse_combine_kernel<DV>, dim3(p.T, p.H), dim3(DV / 4), 0, stream, true, p);
 }
@@ -377,16 +448,21 @@ cudaError_t launch_variant(const SparseAttnParams& p, cudaStream_t stream, bool 
 }  // namespace
 
 int sparse_attn_splits(int T, int H, int K) {
-  // enough CTAs to cover the SMs about twice; each split holds whole 64-row blocks
+  // about one CTA per SM (each CTA holds two 64-row blocks in flight)
   const int blocks = (K + kRows - 1) / kRows;
-  const int head_groups = (H + kHeads - 1) / kHeads;
-  const int ctas_per_split = T * head_groups;
+  const int ctas_per_split = T * ((H + kHeads - 1) / kHeads);
   if (ctas_per_split <= 0) return 1;
-  int want = (2 * 152 + ctas_per_split - 1) / ctas_per_split;
-  if (want < 1) want = 1;
-  if (want > blocks) want = blocks;
-  if (want > 64) want = 64;
-  return want;
+  int s = (152 + ctas_per_split - 1) / ctas_per_split;
+  s = s < 1 ? 1 : (s > 64 ? 64 : s);
+  if (s > blocks) s = blocks;
+  // whole blocks per split, and no empty split
+  const int rows = ((blocks + s - 1) / s) * kRows;
+  return (K + rows - 1) / rows;
+}
+
+static int rows_per_split(int K, int splits) {
+  const int blocks = (K + kRows - 1) / kRows;
+  return ((blocks + splits - 1) / splits) * kRows;
 }
 
 size_t sparse_attn_ws_bytes(int T, int H, int K, int D_v) {
@@ -396,17 +472,16 @@ size_t sparse_attn_ws_bytes(int T, int H, int K, int D_v) {
   return align_up(rows * D_v * sizeof(float), 256) + align_up(rows * 2 * sizeof(float), 256);
 }
 
-cudaError_t launch_sparse_attn(SparseAttnParams p, int D_qk, int D_v, bool fp8, bool sepv,
-                               void* ws, cudaStream_t stream, bool pdl) {
+cudaError_t launch_sparse_attn(SparseAttnParams p, int D_qk, int D_v, bool fp8, bool sepv, void* ws,
+                               cudaStream_t stream, bool pdl) {
   p.splits = sparse_attn_splits(p.T, p.H, p.K);
-  const int blocks = (p.K + kRows - 1) / kRows;
-  p.rows_per_split = ((blocks + p.splits - 1) / p.splits) * kRows;
-  p.splits = (p.K + p.rows_per_split - 1) / p.rows_per_split;
+  p.rows_per_split = rows_per_split(p.K, p.splits);
+  if (p.rows_per_split > kMaxRows) return cudaErrorNotSupported;
   if (p.splits > 1) {
+    if (!ws) return cudaErrorInvalidValue;
     const size_t rows = (size_t)p.T * p.H * p.splits;
     p.part_o = reinterpret_cast<float*>(ws);
-    p.part_ml = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) +
-                                         align_up(rows * D_v * sizeof(float), 256));
+    p.part_ml = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + align_up(rows * D_v * sizeof(float), 256));
   }
   if (D_qk == 576 && D_v == 512 && !sepv) {
     return fp8 ? launch_variant<576, 512, true, false>(p, stream, pdl)
