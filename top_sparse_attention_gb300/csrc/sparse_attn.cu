@@ -347,9 +347,10 @@ sparse_attn_kernel(const SparseAttnParams p) {
     float* stage = reinterpret_cast<float*>(smem + C::OFF_SLOT + C::SLOT);
     float2* ml = reinterpret_cast<float2*>(smem + C::OFF_P);  // P of group 0 is idle as well
     if (g == 1) {
-      float4* st = reinterpret_cast<float4*>(stage) + (size_t)gt * NT;
+      // element i of thread gt at [i][gt]: consecutive lanes hit consecutive 16-byte words
+      float4* st = reinterpret_cast<float4*>(stage) + gt;
 #pragma unroll
-      for (int i = 0; i < NT; ++i) st[i] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      for (int i = 0; i < NT; ++i) st[i * 128] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
       if (gw == 0 && (lane & 3) == 0) {
         ml[r0] = make_float2(m_run[0], l_run[0]);
         ml[r1] = make_float2(m_run[1], l_run[1]);
@@ -357,7 +358,7 @@ sparse_attn_kernel(const SparseAttnParams p) {
     }
     __syncthreads();
     if (g == 1) return;
-    const float4* st = reinterpret_cast<const float4*>(stage) + (size_t)gt * NT;
+    const float4* st = reinterpret_cast<const float4*>(stage) + gt;
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const float2 o = ml[hh ? r1 : r0];
@@ -368,7 +369,7 @@ sparse_attn_kernel(const SparseAttnParams p) {
       m_run[hh] = m_new;
 #pragma unroll
       for (int i = 0; i < NT; ++i) {
-        const float4 v = st[i];
+        const float4 v = st[i * 128];
         acc[i][2 * hh] = acc[i][2 * hh] * a0 + (hh ? v.z : v.x) * a1;
         acc[i][2 * hh + 1] = acc[i][2 * hh + 1] * a0 + (hh ? v.w : v.y) * a1;
       }
