@@ -116,6 +116,27 @@ dsa_status dsa_topk(const float* scores, int64_t ld_scores, int T, int q_per_seq
 size_t dsa_topk_workspace_size(int T, int L, int K);
 
 /* --------------------------------------------------------------------------------------------
+ * dsa_topk_noalloc -- dsa_topk for callers that cannot provide device memory.  The source pages
+ * have no counterpart; this entry exists for callers such as a host framework that owns every
+ * device allocation through its own pool, or a decode loop that must not allocate while it runs
+ * (an allocation can synchronise the device and fragment memory).
+ *
+ * Same arguments, results and errors as dsa_topk, without ws / ws_bytes.  It allocates nothing:
+ * its scratch is a fixed array inside the library, 64 queries x 8448 words (2.2 MB) on every
+ * GPU that loads the library, held until the process exits.  T > 64 returns
+ * DSA_ERR_UNSUPPORTED before any launch.
+ *  - The first call on a device looks up the array's device address (once per device, with that
+ *    device current); make that first call before any stream capture.
+ *  - Each call clears the part of the array it uses (an asynchronous memset on `stream`), then
+ *    launches the Top-K kernel; the array keeps the last call's contents afterwards.
+ *  - All calls share the one array: calls that overlap on the GPU (other streams, other threads)
+ *    race and corrupt each other's results.  Serialise them on one stream.
+ * ------------------------------------------------------------------------------------------ */
+dsa_status dsa_topk_noalloc(const float* scores, int64_t ld_scores, int T, int q_per_seq,
+                            int q_pos0, const int32_t* n_valid, int L, int K, int32_t* idx,
+                            void* stream);
+
+/* --------------------------------------------------------------------------------------------
  * dsa_sparse_attn -- step 3: gather the selected rows of the latent KV cache and compute exact
  * softmax attention over them ("a sparse-attention kernel then reads only the selected KV
  * entries to perform exact computation", Day 0 Support for New LLM Architectures, Step 1;

@@ -19,7 +19,7 @@ DEVERR = {0: "none", 1: "index out of range", 2: "wait timeout"}
 EXPORTS = (
     "dsa_status_string", "dsa_abi_version", "dsa_get_device_error", "dsa_index_score",
     "dsa_topk", "dsa_topk_workspace_size", "dsa_sparse_attn", "dsa_sparse_attn_workspace_size",
-    "dsa_workspace_size", "dsa_decode", "dsa_prefill",
+    "dsa_workspace_size", "dsa_decode", "dsa_prefill", "dsa_topk_noalloc",
 )
 
 
@@ -64,6 +64,7 @@ def _load():
         "dsa_index_score": (I, [P, P, P, P, P, I64, I64, I, I, I, P, I, I, I, I, P, I64, P]),
         "dsa_topk": (I, [P, I64, I, I, I, P, I, I, P, P, SZ, P]),
         "dsa_topk_workspace_size": (SZ, [I, I, I]),
+        "dsa_topk_noalloc": (I, [P, I64, I, I, I, P, I, I, P, P]),
         "dsa_sparse_attn": (I, [P, P, P, P, I64, I64, I64, I64, P, I, I, I, I, I, I, I, F, I, P, P,
                                 P, SZ, P]),
         "dsa_sparse_attn_workspace_size": (SZ, [I, I, I, I]),

@@ -288,6 +288,15 @@ dsa_status run_chain(const dsa_args* a, void* ws, size_t ws_bytes, void* stream,
 
 }  // namespace
 
+dsa_status check_topk_args(const float* scores, int64_t ld_scores, int T, int q_per_seq, int q_pos0,
+                           const int32_t* n_valid, int L, int K, const int32_t* idx) {
+  return check_topk(scores, ld_scores, T, q_per_seq, q_pos0, n_valid, L, K, idx);
+}
+
+dsa_status check_device_arch() { return check_device(); }
+
+int* device_error_word() { return device_error_ptr(); }
+
 CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, cuuint32_t rank, void* addr,
                            const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
                            CUtensorMapSwizzle swizzle) {

@@ -106,6 +106,12 @@ size_t sparse_attn_ws_bytes(int T, int H, int K, int D_v);
 cudaError_t launch_sparse_attn(SparseAttnParams p, int D_qk, int D_v, bool fp8, bool sepv,
                                void* ws, cudaStream_t stream, bool pdl);
 
+// Argument checks and device facts shared with entry points defined outside dsa_api.cu.
+dsa_status check_topk_args(const float* scores, int64_t ld_scores, int T, int q_per_seq, int q_pos0,
+                           const int32_t* n_valid, int L, int K, const int32_t* idx);
+dsa_status check_device_arch();
+int* device_error_word();
+
 // Driver entry point for tensor-map encoding (resolved once through the runtime).
 CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, cuuint32_t rank,
                            void* addr, const cuuint64_t* dims, const cuuint64_t* strides,

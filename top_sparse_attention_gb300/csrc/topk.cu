@@ -21,6 +21,8 @@
 //    many-candidate path, through distributed shared memory); a block-wide scan places each
 //    thread's positions.  Global histograms are zeroed again before the kernel ends.
 // Cluster barriers are hardware barriers: there is no spin loop.
+#include <mutex>
+
 #include "dsa_internal.h"
 
 namespace dsa {
@@ -462,4 +464,69 @@ cudaError_t launch_topk(const TopkParams& p, void* ws, cudaStream_t stream, bool
   return cudaLaunchKernelEx(&cfg, kern, q);
 }
 
+// ---------------------------------------------------------------------------------------------
+// Top-K without a caller workspace.
+//
+// Some callers cannot hand the library device memory: a host framework that owns every device
+// allocation through its own pool and forbids raw cudaMalloc, or a decode loop that must not
+// allocate while it runs (an allocation can synchronise the device and fragment memory).  For
+// them dsa_topk_noalloc keeps the Top-K level histograms in the file-scope array below, sized for
+// kNoAllocMaxQueries queries.  Every GPU that loads the library holds these bytes until the
+// process exits.
+
+constexpr int kNoAllocMaxQueries = 64;
+static __device__ __align__(256) uint32_t g_topk_scratch[kNoAllocMaxQueries * kWorkWords];
+
+namespace {
+
+// The array's device address on the current device.  In host code `g_topk_scratch` names a
+// host-side stand-in, not device memory, so the address is looked up (once per device, with that
+// device current) and passed to the kernel.
+cudaError_t scratch_address(uint32_t** out) {
+  static std::mutex mu;
+  static uint32_t* addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_topk_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = reinterpret_cast<uint32_t*>(ptr);
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
 }  // namespace dsa
+
+extern "C" dsa_status dsa_topk_noalloc(const float* scores, int64_t ld_scores, int T, int q_per_seq,
+                                       int q_pos0, const int32_t* n_valid, int L, int K, int32_t* idx,
+                                       void* stream) {
+  using namespace dsa;
+  dsa_status s = check_topk_args(scores, ld_scores, T, q_per_seq, q_pos0, n_valid, L, K, idx);
+  if (s != DSA_OK || T == 0) return s;
+  if (T > kNoAllocMaxQueries) return DSA_ERR_UNSUPPORTED;
+  if ((s = check_device_arch()) != DSA_OK) return s;
+  uint32_t* scratch = nullptr;
+  if (scratch_address(&scratch) != cudaSuccess) return DSA_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // the histograms must start at zero; the array keeps whatever the previous call left
+  if (cudaMemsetAsync(scratch, 0, (size_t)T * kWorkWords * sizeof(uint32_t), st) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  TopkParams p = {};
+  p.scores = scores;
+  p.ld_scores = ld_scores;
+  p.n_valid = n_valid;
+  p.idx = idx;
+  p.T = T;
+  p.q_per_seq = q_per_seq;
+  p.q_pos0 = q_pos0;
+  p.L = L;
+  p.K = K;
+  p.err = device_error_word();
+  return launch_topk(p, scratch, st, false) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
