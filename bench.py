@@ -218,6 +218,22 @@ def cpu_oracle_rate(wl, cpu_inputs, budget_s):
 # arms
 
 
+def rank_seed_offset(rank, i):
+    """Seed offset of input set i on rank `rank`: every replica draws its own batches."""
+    return rank * 100 + i
+
+
+def max_over_ranks(ms, world, device):
+    """The slowest rank's per-step time: the job is as fast as its slowest replica."""
+    if world <= 1:
+        return ms
+    import torch.distributed as dist
+
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -280,7 +296,7 @@ def run_ours(args, wl):
     n_sets = max(3, min(8, -(-3 * L2_BYTES // max(per_step, 1))))
     if args.sets:
         n_sets = args.sets
-    cpu_sets = [synth.make_inputs(wl, seed_offset=rank * 100 + i) for i in range(n_sets)]
+    cpu_sets = [synth.make_inputs(wl, seed_offset=rank_seed_offset(rank, i)) for i in range(n_sets)]
     dev_sets = [{k: (v.to(dev) if v is not None else None) for k, v in s.items()} for s in cpu_sets]
     calls = [dsa.call_from_tensors(s, K=wl.K, sm_scale=wl.sm_scale, q_per_seq=wl.q_per_seq,
                                    q_pos0=wl.q_pos0) for s in dev_sets]
@@ -327,13 +343,7 @@ def run_ours(args, wl):
             ev1.record(stream)
         torch.cuda.synchronize()
     barrier()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world, dev)
     err = dsa.dsa_get_device_error(stream)
     queries = wl.T * world
     value = queries / (ms * 1e-3)

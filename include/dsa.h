@@ -69,6 +69,14 @@ int dsa_abi_version(void);
  * (this is the one call that blocks the host).  *code receives DSA_DEVERR_*. */
 dsa_status dsa_get_device_error(int* code, void* stream);
 
+/* Failure-path self-test (no counterpart in the method): launches one kernel whose single thread
+ * waits, through the same bounded wait that every kernel of the chain uses, on a barrier that
+ * nothing arrives on.  After the wait limit (about one second) the kernel records
+ * DSA_DEVERR_WAIT_TIMEOUT in the device error word and returns normally, so the context stays
+ * usable; dsa_get_device_error then reports (and clears) the code.  Returns DSA_OK once the kernel
+ * is enqueued on `stream` (NULL = default stream). */
+dsa_status dsa_selftest_wait_timeout(void* stream);
+
 /* --------------------------------------------------------------------------------------------
  * dsa_index_score -- step 1: indexer relevance scores ("relevance scoring, head-weight
  * application", Day 0 Support for New LLM Architectures, Key Optimization 1; MXFP8 index path

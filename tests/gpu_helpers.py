@@ -35,3 +35,29 @@ def score_error_bound(q_idx: np.ndarray, w: np.ndarray, k_idx: np.ndarray) -> np
     d, H = q_idx.shape[1], q_idx.shape[0]
     mag = np.abs(k_idx) @ np.abs(q_idx).T  # [n, H]
     return u * (d + H + 2) * (mag @ np.abs(w)) + 1e-30
+
+
+def check_chain(dsa, wl, cpu, queries=None):
+    dev = to_device(cpu)
+    call = dsa.call_from_tensors(dev, K=wl.K, sm_scale=wl.sm_scale, q_per_seq=wl.q_per_seq, q_pos0=wl.q_pos0)
+    out, lse, idx = call()
+    torch.cuda.synchronize()
+    out = out.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    idx = idx.cpu().numpy()
+    ch, _ = oracle_chain(wl, cpu)
+    kind = wl.kv_dtype
+    report = {"band": 0, "swaps": 0, "worst_attn": 0.0}
+    for t in (range(wl.T) if queries is None else queries):
+        rep = oracle.parity.check_topk(idx[t], ch.scores(t), wl.K)
+        report["band"] += rep["band"]
+        report["swaps"] += rep["swaps"]
+        ref, ref_lse = ch.attention(t, idx[t], wl.D_v)
+        err = float(np.max(np.abs(out[t] - ref)))
+        report["worst_attn"] = max(report["worst_attn"], err)
+        assert err <= ATTN_TOL[kind], f"t={t}: attention max-abs {err}"
+        fin = np.isfinite(ref_lse)
+        assert np.all(np.abs(lse[t][fin] - ref_lse[fin]) <= LSE_TOL)
+    assert report["worst_attn"] <= ATTN_GUARD[kind]
+    print(wl.name, report)
+    return report

@@ -13,7 +13,7 @@ import torch
 
 import oracle
 import synth
-from gpu_helpers import ATTN_GUARD, ATTN_TOL, LSE_TOL, oracle_chain, score_error_bound, to_device
+from gpu_helpers import ATTN_GUARD, ATTN_TOL, LSE_TOL, check_chain, oracle_chain, score_error_bound, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -217,30 +217,7 @@ def test_sparse_attn_out_of_range_index_is_skipped_and_recorded(dsa):
 # fused chain
 
 
-def _check_chain(dsa, wl, cpu, queries=None):
-    dev = to_device(cpu)
-    call = dsa.call_from_tensors(dev, K=wl.K, sm_scale=wl.sm_scale, q_per_seq=wl.q_per_seq, q_pos0=wl.q_pos0)
-    out, lse, idx = call()
-    torch.cuda.synchronize()
-    out = out.float().cpu().numpy()
-    lse = lse.cpu().numpy()
-    idx = idx.cpu().numpy()
-    ch, _ = oracle_chain(wl, cpu)
-    kind = wl.kv_dtype
-    report = {"band": 0, "swaps": 0, "worst_attn": 0.0}
-    for t in (range(wl.T) if queries is None else queries):
-        rep = oracle.parity.check_topk(idx[t], ch.scores(t), wl.K)
-        report["band"] += rep["band"]
-        report["swaps"] += rep["swaps"]
-        ref, ref_lse = ch.attention(t, idx[t], wl.D_v)
-        err = float(np.max(np.abs(out[t] - ref)))
-        report["worst_attn"] = max(report["worst_attn"], err)
-        assert err <= ATTN_TOL[kind], f"t={t}: attention max-abs {err}"
-        fin = np.isfinite(ref_lse)
-        assert np.all(np.abs(lse[t][fin] - ref_lse[fin]) <= LSE_TOL)
-    assert report["worst_attn"] <= ATTN_GUARD[kind]
-    print(wl.name, report)
-    return report
+_check_chain = check_chain
 
 
 @pytest.mark.parametrize("name", ["tiny_decode_l2k", "decode_b8_l32k_bf16", "decode_b8_l32k_mxfp8"])

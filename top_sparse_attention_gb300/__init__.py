@@ -9,7 +9,8 @@ need the library).
 import importlib
 
 _API = ("DsaCall", "dsa_decode", "dsa_get_device_error", "dsa_index_score", "dsa_prefill",
-        "dsa_sparse_attn", "dsa_topk", "dsa_workspace_size", "ld_scores_for")
+        "dsa_selftest_wait_timeout", "dsa_sparse_attn", "dsa_topk", "dsa_workspace_size",
+        "ld_scores_for")
 _NATIVE = ("DsaError", "LIB_PATH", "EXPORTS")
 
 INPUT_KEYS = ("q_idx", "q_idx_sf", "w", "k_idx", "k_idx_sf", "q", "kv", "kv_scale", "kv_v", "n_valid")

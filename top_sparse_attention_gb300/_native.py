@@ -20,6 +20,7 @@ EXPORTS = (
     "dsa_status_string", "dsa_abi_version", "dsa_get_device_error", "dsa_index_score",
     "dsa_topk", "dsa_topk_workspace_size", "dsa_sparse_attn", "dsa_sparse_attn_workspace_size",
     "dsa_workspace_size", "dsa_decode", "dsa_prefill", "dsa_topk_noalloc",
+    "dsa_selftest_wait_timeout",
 )
 
 
@@ -61,6 +62,7 @@ def _load():
         "dsa_status_string": (ctypes.c_char_p, [I]),
         "dsa_abi_version": (I, []),
         "dsa_get_device_error": (I, [ctypes.POINTER(I), P]),
+        "dsa_selftest_wait_timeout": (I, [P]),
         "dsa_index_score": (I, [P, P, P, P, P, I64, I64, I, I, I, P, I, I, I, I, P, I64, P]),
         "dsa_topk": (I, [P, I64, I, I, I, P, I, I, P, P, SZ, P]),
         "dsa_topk_workspace_size": (SZ, [I, I, I]),

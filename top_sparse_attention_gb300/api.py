@@ -178,3 +178,9 @@ def dsa_get_device_error(stream=None) -> int:
     code = ctypes.c_int(0)
     N.check(N.lib.dsa_get_device_error(ctypes.byref(code), _stream(stream)), "dsa_get_device_error")
     return code.value
+
+
+def dsa_selftest_wait_timeout(stream=None) -> None:
+    """Enqueue the failure-path self-test: a kernel whose bounded wait runs out (about one second)
+    and records the wait-timeout device error code; read it with dsa_get_device_error."""
+    N.check(N.lib.dsa_selftest_wait_timeout(_stream(stream)), "dsa_selftest_wait_timeout")

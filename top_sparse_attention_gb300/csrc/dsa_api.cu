@@ -286,6 +286,18 @@ dsa_status run_chain(const dsa_args* a, void* ws, size_t ws_bytes, void* stream,
   return DSA_OK;
 }
 
+// Failure-path self-test: one thread waits, through the same bounded wait every kernel of the
+// chain uses, on an mbarrier that nothing arrives on.  The wait gives up after its limit, records
+// DSA_DEVERR_WAIT_TIMEOUT and the kernel returns normally.
+__global__ void selftest_wait_kernel(int* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_wait(&bar, 0, err);
+  }
+}
+
 }  // namespace
 
 dsa_status check_topk_args(const float* scores, int64_t ld_scores, int T, int q_per_seq, int q_pos0,
@@ -344,6 +356,13 @@ dsa_status dsa_get_device_error(int* code, void* stream) {
   if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return DSA_ERR_CUDA;
   *code = v;
   return DSA_OK;
+}
+
+dsa_status dsa_selftest_wait_timeout(void* stream) {
+  dsa_status s = check_device();
+  if (s != DSA_OK) return s;
+  selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(device_error_ptr());
+  return from_cuda(cudaGetLastError());
 }
 
 dsa_status dsa_index_score(const void* q_idx, const uint8_t* q_idx_sf, const float* w,
