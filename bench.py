@@ -417,22 +417,36 @@ def slice_queries(wl):
 
 def kernel_times(dsa, wl, dev_sets, stream, reps):
     """Average device time of each step's kernel(s), launched alone through the component entry
-    points on the same inputs, rotating over the input sets."""
+    points on the same inputs, rotating over the input sets (so the keys come from DRAM).  Each
+    component's `reps` launches are captured in one CUDA graph and timed with CUDA events on the
+    launching stream around its replay, so the figure is device time without host launch gaps."""
     n = len(dev_sets)
     L = wl.L
-    scores = [torch.empty(wl.T, dsa.ld_scores_for(L), dtype=torch.float32, device=s["q"].device) for s in dev_sets]
-    idx = [torch.empty(wl.T, wl.K, dtype=torch.int32, device=s["q"].device) for s in dev_sets]
+    dev = dev_sets[0]["q"].device
+    scores = [torch.empty(wl.T, dsa.ld_scores_for(L), dtype=torch.float32, device=dev) for s in dev_sets]
+    idx = [torch.empty(wl.T, wl.K, dtype=torch.int32, device=dev) for s in dev_sets]
+    from top_sparse_attention_gb300 import _native
+
+    topk_ws = torch.zeros(max(16, _native.lib.dsa_topk_workspace_size(wl.T, L, wl.K)), dtype=torch.uint8, device=dev)
+    attn_ws_bytes = _native.lib.dsa_sparse_attn_workspace_size(wl.T, wl.H, wl.K, wl.D_v)
+    attn_ws = torch.zeros(max(16, attn_ws_bytes), dtype=torch.uint8, device=dev) if attn_ws_bytes else None
     out = {}
 
     def timed(fn):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             for i in range(3):
                 fn(i % n)
-            torch.cuda.synchronize()
-            e0.record(stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
             for i in range(reps):
                 fn(i % n)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            g.replay()
             e1.record(stream)
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) * 1e3 / reps
@@ -444,14 +458,16 @@ def kernel_times(dsa, wl, dev_sets, stream, reps):
                             stream=stream)
 
     def topk(i):
-        dsa.dsa_topk(scores[i], wl.K, L=L, q_per_seq=wl.q_per_seq, q_pos0=wl.q_pos0, idx=idx[i], stream=stream)
+        dsa.dsa_topk(scores[i], wl.K, L=L, q_per_seq=wl.q_per_seq, q_pos0=wl.q_pos0, idx=idx[i], ws=topk_ws,
+                     stream=stream)
 
     outs = [torch.empty(wl.T, wl.H, wl.D_v, dtype=torch.bfloat16, device=s["q"].device) for s in dev_sets]
     lses = [torch.empty(wl.T, wl.H, dtype=torch.float32, device=s["q"].device) for s in dev_sets]
     def attn(i):
         s = dev_sets[i]
         dsa.dsa_sparse_attn(s["q"], s["kv"], idx[i], sm_scale=wl.sm_scale, kv_v=s["kv_v"], kv_scale=s["kv_scale"],
-                            D_v=wl.D_v, q_per_seq=wl.q_per_seq, out=outs[i], lse=lses[i], stream=stream)
+                            D_v=wl.D_v, q_per_seq=wl.q_per_seq, out=outs[i], lse=lses[i], ws=attn_ws,
+                            stream=stream)
 
     out["index_score_us"] = timed(score)
     out["topk_us"] = timed(topk)

@@ -114,7 +114,8 @@ dsa_status dsa_index_score(const void* q_idx, const uint8_t* q_idx_sf, const flo
  * ascending position order, followed by -1 in the remaining slots.  Scores are compared as
  * fp32 with -0 equal to +0; NaN scores are not supported.
  *   ws / ws_bytes  device workspace of at least dsa_topk_workspace_size(T, L, K) bytes,
- *                  zero-filled once before its first use (every completed call leaves it zero);
+ *                  zero-filled once before its first use (every completed call leaves it ready
+ *                  for the next: the areas that must start at zero are zeroed again);
  *                  calls sharing a workspace must not run concurrently
  * Supported: 1 <= K <= 4096.
  * ------------------------------------------------------------------------------------------ */
@@ -130,8 +131,8 @@ size_t dsa_topk_workspace_size(int T, int L, int K);
  * (an allocation can synchronise the device and fragment memory).
  *
  * Same arguments, results and errors as dsa_topk, without ws / ws_bytes.  It allocates nothing:
- * its scratch is a fixed array inside the library, 64 queries x 8448 words (2.2 MB) on every
- * GPU that loads the library, held until the process exits.  T > 64 returns
+ * its scratch is a fixed array inside the library, 16 queries x 38912 words (2.4 MB) on every
+ * GPU that loads the library, held until the process exits.  T > 16 returns
  * DSA_ERR_UNSUPPORTED before any launch.
  *  - The first call on a device looks up the array's device address (once per device, with that
  *    device current); make that first call before any stream capture.

@@ -65,13 +65,17 @@ def dsa_index_score(q_idx, w, k_idx, *, q_idx_sf=None, k_idx_sf=None, q_per_seq=
     return scores
 
 
-def dsa_topk(scores, K, *, L, q_per_seq=1, q_pos0=-1, n_valid=None, idx=None, stream=None) -> torch.Tensor:
-    """Top-K positions [T, K] int32 (ascending, -1 padded)."""
+def dsa_topk(scores, K, *, L, q_per_seq=1, q_pos0=-1, n_valid=None, idx=None, ws=None, stream=None) -> torch.Tensor:
+    """Top-K positions [T, K] int32 (ascending, -1 padded).  `ws`, if given, is a zero-filled
+    uint8 tensor of at least dsa_topk_workspace_size bytes that later calls may reuse."""
     T = scores.shape[0]
     if idx is None:
         idx = torch.empty(T, K, dtype=torch.int32, device=scores.device)
     ws_bytes = N.lib.dsa_topk_workspace_size(T, L, K)
-    ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=scores.device) if ws_bytes else None
+    if ws is None:
+        ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=scores.device) if ws_bytes else None
+    else:
+        ws_bytes = ws.numel()
     st = N.lib.dsa_topk(_p(scores), scores.stride(0), T, q_per_seq, q_pos0, _p(n_valid), L, K, _p(idx),
                         _p(ws), ws_bytes, _stream(stream))
     N.check(st, "dsa_topk")

@@ -3,24 +3,28 @@
 // Day-0 Readiness...", section 2.1).
 //
 // Radix select on order-preserving 32-bit keys of the fp32 scores, never sorting.  One
-// thread-block cluster of C CTAs (C = 1..16) handles one query; CTA r owns a contiguous slice of
-// the query's positions and keeps its keys in shared memory when they fit.
-//  * Level 0: a histogram of the top 12 key bits.  In the fused chain it arrives ready-made from
-//    the index-score kernel's epilogue; otherwise every CTA adds its non-zero bins into a global
-//    per-query histogram (L2 atomics) before a cluster barrier.  Every CTA then reads it and
-//    finds, with a block-wide suffix scan, the bin b0 holding the K-th largest key (all CTAs get
-//    the same answer, so nothing is broadcast).
-//  * Few candidates (the keys of bin b0; the usual case): each CTA lists its candidates in
-//    position order, one cluster barrier later every CTA copies all lists through distributed
-//    shared memory and resolves the exact threshold key T on its own (two 10-bit digit passes
-//    over the candidates), again identically in every CTA.
-//  * Many candidates: two more digit levels (12 and 8 bits) run like level 0, with global
-//    histograms and a cluster barrier each.
-//  * Output in ascending position order: keys above T, then the first ties by position (exact
-//    ties go to the lower position).  Per-CTA counts come from the candidate lists (or, on the
-//    many-candidate path, through distributed shared memory); a block-wide scan places each
-//    thread's positions.  Global histograms are zeroed again before the kernel ends.
-// Cluster barriers are hardware barriers: there is no spin loop.
+// thread-block cluster of C CTAs (C = 1..16, about 2048 positions per CTA) handles one query; CTA
+// r owns a contiguous slice of the query's positions and keeps its keys in shared memory when the
+// slice fits.  Threads read keys four at a time (16-byte loads, chunk-major, thread order within a
+// chunk equals position order).  Bulk data crosses CTAs through a per-query area of the workspace
+// (L2); single counts go through distributed shared memory; the cluster's hardware barrier orders
+// both (no spin loop).
+//  * Level 0, the top 12 key bits.  In the fused chain the histogram arrives ready-made from the
+//    index-score epilogue; otherwise each CTA counts its keys in shared memory and adds the
+//    non-zero bins into the workspace histogram before a barrier.  Every CTA reads it and finds,
+//    with a block-wide suffix scan, the same bin b0 holding the K-th largest key.
+//  * Pass A: each CTA lists its candidates (keys in bin b0, with positions), counts its keys
+//    above b0 and copies the list to its own region of the workspace.  One barrier; the counts
+//    then come from the other CTAs' shared memory.
+//  * Few candidates (at most 4096 in the query and 1024 in any CTA, the usual case): every CTA
+//    reads every list and resolves the last 20 bits of the threshold key T with two 10-bit
+//    levels on its own; the lists also give the keys above T and equal to T before its slice.
+//    Many candidates: the two levels and the per-CTA counts go through the cluster, one barrier
+//    each.
+//  * Output, ascending positions: the slot of a kept key is (keys > T before it) + min(keys == T
+//    before it, ties to take), so exact ties go to the lower positions; each CTA writes its keys
+//    straight to the index row.
+// The workspace histograms are zeroed again before the kernel ends.
 #include <mutex>
 
 #include "dsa_internal.h"
@@ -30,410 +34,551 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kCachedKeys = 16384;  // largest cached slice
-constexpr int kCand = 4096;         // candidates resolved through distributed shared memory
-constexpr int kWorkWords = 2 * kHistBins + 256;  // per query: level-0, level-1, level-2 bins
+constexpr int kChunk = 4 * kThreads;  // keys per block-wide step
+constexpr int kCachedKeys = 16384;    // largest slice kept in shared memory
+constexpr int kCand = 4096;           // candidates gathered into every CTA (registers)
+constexpr int kGather = kCand / kThreads;
+constexpr int kRegion = 1024;         // workspace list entries per CTA
+constexpr int kMaxK = 4096;
+constexpr int kLevelBins = 1024;      // levels 1 and 2: 10-bit digits
+constexpr uint32_t kNoBin = 0xFFFFFFFFu;
 
-// Shared memory (in 32-bit words): histogram | scratch (96) | counts (4) | own candidate keys,
-// positions (min(slice, kCand) each) | all candidate keys, positions (kCand each) | keys
+// Per-query workspace, in 32-bit words: level-0 histogram (when the chain does not supply one) |
+// level-1 histogram | level-2 histogram | C lists of kRegion (key, position) entries.
+constexpr int kWsGh0 = 0;
+constexpr int kWsGh1 = kWsGh0 + kHistBins;
+constexpr int kWsGh2 = kWsGh1 + kLevelBins;
+constexpr int kWsList = kWsGh2 + kLevelBins;
+__host__ __device__ inline int64_t ws_words(int C) { return kWsList + 2 * (int64_t)C * kRegion; }
+
+// Shared-memory layout in 32-bit words.  The host sizes it from the longest row of the launch.
 struct TopkSmem {
-  int own, keys, words;
-  __host__ __device__ TopkSmem(int slice, bool cached) {
-    own = slice < kCand ? slice : kCand;
-    keys = cached ? slice + slice / 32 : 0;
-    words = kHistBins + 96 + 4 + 2 * own + 2 * kCand + keys;
+  int h0, h1, h2, sc, pub, own, keys, own_cap, words;
+  bool cached;
+  __host__ __device__ explicit TopkSmem(int slice_max) {
+    cached = slice_max <= kCachedKeys;
+    own_cap = slice_max < kCand ? slice_max : kCand;
+    h0 = 0;                        // level-0 counts of this CTA (kHistBins)
+    h1 = h0 + kHistBins;           // level-1 counts
+    h2 = h1 + kLevelBins;          // level-2 counts
+    sc = h2 + kLevelBins;          // 128 words of scan scratch and broadcasts
+    pub = sc + 128;                // 8 words read by the other CTAs of the cluster
+    own = pub + 8;                 // this CTA's candidates (key, position), own_cap entries
+    keys = own + 2 * own_cap;      // cached keys (16-byte aligned: every offset is a multiple of 4)
+    words = keys + (cached ? slice_max : 0);
   }
 };
 
-__device__ __forceinline__ int pad(int i) { return i + (i >> 5); }
+__host__ __device__ inline int slice_of(int n, int C) { return (((n + C - 1) / C) + 31) & ~31; }
 
-// Block-wide inclusive prefix sum in thread order.
-__device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, uint32_t* sc) {
+// Adds 1 to hist[d] for every lane with d != kNoBin; a warp whose lanes all carry the same digit
+// adds 32 with one atomic, so equal keys do not serialise on one shared-memory address.  Every
+// lane of the warp must call it.
+__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t d) {
+  const uint32_t d0 = __shfl_sync(0xffffffffu, d, 0);
+  if (__all_sync(0xffffffffu, d == d0)) {
+    if ((threadIdx.x & 31) == 0 && d0 != kNoBin) atomicAdd(&hist[d0], 32u);
+  } else if (d != kNoBin) {
+    atomicAdd(&hist[d], 1u);
+  }
+}
+
+// Block-wide exclusive prefix sum of 64-bit values in thread order; *total receives the block
+// sum.  Callers pack several counts into disjoint bit fields.  sc: 2 * kWarps + 2 words.
+__device__ __forceinline__ uint64_t block_excl_scan(uint64_t v, uint32_t* sc, uint64_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint64_t x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
+    const uint64_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
   }
-  if (lane == 31) sc[warp] = v;
+  uint64_t* s64 = reinterpret_cast<uint64_t*>(sc);
+  if (lane == 31) s64[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    uint32_t s = lane < kWarps ? sc[lane] : 0u;
+    const uint64_t w = lane < kWarps ? s64[lane] : 0ull;
+    uint64_t s = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t n = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += n;
+      const uint64_t y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
     }
-    if (lane < kWarps) sc[lane] = s;
+    if (lane < kWarps) s64[lane] = s - w;
+    if (lane == 31) s64[kWarps] = s;
   }
   __syncthreads();
-  const uint32_t r = v + (warp > 0 ? sc[warp - 1] : 0u);
+  const uint64_t r = x - v + s64[warp];
+  *total = s64[kWarps];
   __syncthreads();
   return r;
 }
 
-// Block-wide inclusive suffix sum (thread i receives the sum over threads >= i).
-__device__ __forceinline__ uint32_t block_incl_suffix(uint32_t v, uint32_t* sc) {
+// Thread i holds the counts c[0..PER) of bins i*PER .. i*PER+PER-1 (ascending digits).  Finds the
+// digit d with count(> d) < kr <= count(>= d); returns d and sets *above = count(> d).
+template <int PER>
+__device__ __forceinline__ uint32_t find_digit(const uint32_t (&c)[PER], uint32_t kr, uint32_t* sc,
+                                               uint32_t* above) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t n = __shfl_down_sync(0xffffffffu, v, o);
-    if (lane + o < 32) v += n;
-  }
-  if (lane == 0) sc[warp] = v;
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t s = lane < kWarps ? sc[lane] : 0u;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t n = __shfl_down_sync(0xffffffffu, s, o);
-      if (lane + o < 32) s += n;
-    }
-    if (lane < kWarps) sc[lane] = s;
-  }
-  __syncthreads();
-  const uint32_t r = v + (warp < kWarps - 1 ? sc[warp + 1] : 0u);
-  __syncthreads();
-  return r;
-}
-
-// In the global histogram g of `bins` bins, the bin d holding the kr-th largest element:
-// count(bins > d) < kr <= count(bins >= d).  Returns d; `above` = count(bins > d),
-// `in_bin` = g[d].
-__device__ __forceinline__ uint32_t find_digit(const uint32_t* g, int bins, uint32_t kr, uint32_t* sc,
-                                               uint32_t& above, uint32_t& in_bin) {
-  const int per = bins >= kThreads ? bins / kThreads : 1;
-  const int b0 = threadIdx.x * per;
-  uint32_t c[8];
   uint32_t mine = 0;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    c[k] = (k < per && b0 + k < bins) ? __ldcg(g + b0 + k) : 0u;
-    mine += c[k];
-  }
-  uint32_t a = block_incl_suffix(mine, sc) - mine;  // count in bins >= b0 + per
+  for (int k = 0; k < PER; ++k) mine += c[k];
+  uint32_t x = mine;  // inclusive suffix sum over the warp
 #pragma unroll
-  for (int k = 7; k >= 0; --k) {
-    if (k < per && b0 + k < bins) {
-      if (a < kr && a + c[k] >= kr) {
-        sc[64] = (uint32_t)(b0 + k);
-        sc[65] = a;
-        sc[66] = c[k];
-      }
-      a += c[k];
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_down_sync(0xffffffffu, x, o);
+    if (lane + o < 32) x += y;
+  }
+  if (lane == 0) sc[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t w = lane < kWarps ? sc[lane] : 0u;
+    uint32_t s = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_down_sync(0xffffffffu, s, o);
+      if (lane + o < 32) s += y;
     }
+    if (lane < kWarps) sc[lane] = s - w;  // count in higher warps
   }
   __syncthreads();
-  const uint32_t d = sc[64];
-  above = sc[65];
-  in_bin = sc[66];
+  uint32_t a = x - mine + sc[warp];  // count in higher threads' bins
+#pragma unroll
+  for (int k = PER - 1; k >= 0; --k) {
+    if (a < kr && a + c[k] >= kr) {  // exactly one bin of the block satisfies this
+      sc[32] = (uint32_t)(threadIdx.x * PER + k);
+      sc[33] = a;
+    }
+    a += c[k];
+  }
+  __syncthreads();
+  const uint32_t d = sc[32];
+  *above = sc[33];
   __syncthreads();
   return d;
 }
 
+// Global histogram read as PER consecutive bins per thread.
+template <int PER>
+__device__ __forceinline__ void load_bins(const uint32_t* g, uint32_t (&c)[PER]) {
+  static_assert(PER == 2 || PER == 8, "bins per thread");
+  if constexpr (PER == 8) {
+    const uint4 a = __ldcg(reinterpret_cast<const uint4*>(g) + 2 * threadIdx.x);
+    const uint4 b = __ldcg(reinterpret_cast<const uint4*>(g) + 2 * threadIdx.x + 1);
+    c[0] = a.x, c[1] = a.y, c[2] = a.z, c[3] = a.w, c[4] = b.x, c[5] = b.y, c[6] = b.z, c[7] = b.w;
+  } else {
+    const uint2 a = __ldcg(reinterpret_cast<const uint2*>(g) + threadIdx.x);
+    c[0] = a.x, c[1] = a.y;
+  }
+}
+
+// Adds a shared-memory histogram's non-zero bins into a global one.
+__device__ __forceinline__ void flush_bins(const uint32_t* h, uint32_t* g, int bins) {
+  for (int b = threadIdx.x; b < bins; b += kThreads) {
+    const uint32_t v = h[b];
+    if (v) atomicAdd(&g[b], v);
+  }
+}
+
+// Warp-aggregated append of (key, position) to a shared-memory list; every lane must call it.
+__device__ __forceinline__ void list_append(uint2* list, uint32_t* count, int cap, bool take, uint32_t key,
+                                            uint32_t pos) {
+  const uint32_t ballot = __ballot_sync(0xffffffffu, take);
+  if (ballot == 0u) return;
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(ballot) - 1;
+  uint32_t base = 0;
+  if (lane == leader) base = atomicAdd(count, (uint32_t)__popc(ballot));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  const uint32_t at = base + __popc(ballot & ((1u << lane) - 1u));
+  if (take && at < (uint32_t)cap) list[at] = make_uint2(key, pos);
+}
+
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkParams p) {
-  extern __shared__ uint32_t sm[];
+  extern __shared__ __align__(16) uint32_t sm[];
   pdl_launch_dependents();
   const int t = blockIdx.y;
   const int tid = threadIdx.x;
-  const int lane = tid & 31;
   const int C = (int)cluster_size();
   const int r = (int)cluster_rank();
   pdl_wait();
   const int n = visible_len(t + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid);
   const float* scr = p.scores + (int64_t)t * p.ld_scores;
   int32_t* out = p.idx + (int64_t)t * p.K;
-  uint32_t* work = p.work + (int64_t)t * kWorkWords;
-  uint32_t* g0 = p.hist ? p.hist + (int64_t)t * kHistBins : work;  // level-0 histogram
-  uint32_t* g1 = work + kHistBins;
-  uint32_t* g2 = work + 2 * kHistBins;
+  uint32_t* ws = p.work + (int64_t)t * ws_words(C);
+  uint32_t* gh0 = p.hist ? p.hist + (int64_t)t * kHistBins : ws + kWsGh0;
+  uint32_t* gh1 = ws + kWsGh1;
+  uint32_t* gh2 = ws + kWsGh2;
+  uint2* glist = reinterpret_cast<uint2*>(ws + kWsList);
 
   if (n <= p.K) {  // the whole cluster leaves here together (n is the same for all its CTAs)
     if (r == 0 && p.hist)
-      for (int b = tid; b < kHistBins; b += kThreads) g0[b] = 0;  // leave it zeroed
+      for (int b = tid; b < kHistBins; b += kThreads) gh0[b] = 0;  // leave it zeroed
     for (int i = r * kThreads + tid; i < p.K; i += C * kThreads) out[i] = i < n ? i : -1;
     return;
   }
-  const int slice = (((n + C - 1) / C) + 31) & ~31;
-  const int lo = min(n, r * slice), hi = min(n, lo + slice), cnt = hi - lo;
-  // the shared-memory layout follows the longest row of the launch (the host sizes it the same
-  // way), so every CTA of every cluster uses the same offsets
-  const int slice_max = (((p.L + C - 1) / C) + 31) & ~31;
-  const bool cached = slice_max <= kCachedKeys;
-  const TopkSmem L(slice_max, cached);
-  uint32_t* hist = sm;              // this CTA's histogram
-  uint32_t* sc = hist + kHistBins;  // scan scratch and broadcast words
-  uint32_t* counts = sc + 96;       // [0] keys above the threshold / candidates, [1] ties
-  uint32_t* own_key = counts + 4;
-  uint32_t* own_pos = own_key + L.own;
-  uint32_t* all_key = own_pos + L.own;
-  uint32_t* all_pos = all_key + kCand;
-  uint32_t* keys = all_pos + kCand;
-  if (cached) {
-#pragma unroll 4
-    for (int i = tid; i < cnt; i += kThreads) keys[pad(i)] = float_key(scr[lo + i]);
-  }
-  auto key_at = [&](int i) -> uint32_t { return cached ? keys[pad(i)] : float_key(scr[lo + i]); };
+  const TopkSmem S(slice_of(p.L, C));
+  const int slice = slice_of(n, C);
+  const int lo = min(n, r * slice), cnt = min(n, lo + slice) - lo;
+  uint32_t* h0 = sm + S.h0;
+  uint32_t* h1 = sm + S.h1;
+  uint32_t* h2 = sm + S.h2;
+  uint32_t* sc = sm + S.sc;
+  uint32_t* pub = sm + S.pub;
+  uint2* own = reinterpret_cast<uint2*>(sm + S.own);
+  uint32_t* keys = sm + S.keys;
+  const float* src = scr + lo;
+  const bool vec = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
 
-  // adds this CTA's keys that match `prefix` (pbits high bits) into `hist`, digit = the next
-  // `width` bits, then flushes the non-zero bins into the global histogram g
-  auto count_level = [&](uint32_t prefix, int pbits, int width, uint32_t* g) {
-    const int bins = 1 << width;
-    const int shift = 32 - pbits - width;
-    for (int b = tid; b < bins; b += kThreads) hist[b] = 0;
-    __syncthreads();
-    for (int i0 = 0; i0 < cnt; i0 += kThreads) {
-      const int i = i0 + tid;
-      uint32_t d = 0xFFFFFFFFu;
-      if (i < cnt) {
-        const uint32_t key = key_at(i);
-        if (pbits == 0 || (key >> (32 - pbits)) == prefix) d = (key >> shift) & (uint32_t)(bins - 1);
-      }
-      const uint32_t peers = __match_any_sync(0xffffffffu, d);
-      if (d != 0xFFFFFFFFu && lane == __ffs(peers) - 1) atomicAdd(&hist[d], __popc(peers));
+  // keys at local positions i .. i+3 (i a multiple of 4); positions >= cnt read as 0 and every
+  // caller excludes them with its own bound check
+  auto load_global = [&](int i, uint32_t (&k)[4]) {
+    if (vec && i + 3 < cnt) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(src + i));
+      k[0] = float_key(v.x), k[1] = float_key(v.y), k[2] = float_key(v.z), k[3] = float_key(v.w);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) k[j] = i + j < cnt ? float_key(__ldcg(src + i + j)) : 0u;
     }
-    __syncthreads();
-    for (int b = tid; b < bins; b += kThreads)
-      if (hist[b]) atomicAdd(&g[b], hist[b]);
-    __threadfence();  // the global counts are visible before the cluster barrier completes
+  };
+  auto load4 = [&](int i, uint32_t (&k)[4]) {
+    if (i >= cnt) {
+      k[0] = k[1] = k[2] = k[3] = 0u;
+    } else if (S.cached) {
+      const uint4 v = *reinterpret_cast<const uint4*>(keys + i);
+      k[0] = v.x, k[1] = v.y, k[2] = v.z, k[3] = v.w;
+    } else {
+      load_global(i, k);
+    }
   };
 
-  uint32_t prefix = 0;  // chosen high digits so far
-  int pbits = 0;        // how many high bits are fixed
-  uint32_t kr = (uint32_t)p.K;
-  uint32_t above, in_bin;
-  // level 0: top 12 bits (complete on entry when it comes from the index-score kernel)
+  // ---- loads: the level-0 counts (when ready-made) and this slice's keys, all in flight at once
+  uint32_t c8[8];
+  if (p.hist) load_bins<8>(gh0, c8);
+  if (S.cached) {
+    constexpr int kFill = kCachedKeys / kChunk;
+    uint32_t k[kFill][4];
+#pragma unroll
+    for (int f = 0; f < kFill; ++f)
+      if (f * kChunk < cnt) load_global(f * kChunk + 4 * tid, k[f]);
+#pragma unroll
+    for (int f = 0; f < kFill; ++f) {
+      const int i = f * kChunk + 4 * tid;
+      if (i < cnt) *reinterpret_cast<uint4*>(keys + i) = make_uint4(k[f][0], k[f][1], k[f][2], k[f][3]);
+    }
+  }
+  h1[2 * tid] = h1[2 * tid + 1] = 0;
+  h2[2 * tid] = h2[2 * tid + 1] = 0;
+  if (tid == 0) sc[120] = sc[121] = 0;  // this CTA's candidates, keys above b0
+
+  // ---- level 0: top 12 bits
   if (!p.hist) {
-    count_level(0, 0, 12, g0);
-    cluster_sync();
+    reinterpret_cast<uint4*>(h0)[2 * tid] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4*>(h0)[2 * tid + 1] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    for (int base = 0; base < cnt; base += kChunk) {
+      const int i = base + 4 * tid;
+      uint32_t k[4];
+      load4(i, k);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) hist_add(h0, i + j < cnt ? k[j] >> 20 : kNoBin);
+    }
+    __syncthreads();
+    flush_bins(h0, gh0, kHistBins);
+    cluster_sync();  // every CTA's counts are in gh0 (the barrier's release orders the atomics)
+    load_bins<8>(gh0, c8);
   } else {
-    __syncthreads();
+    __syncthreads();  // cached keys and cleared histograms visible
   }
-  uint32_t d = find_digit(g0, kHistBins, kr, sc, above, in_bin);
+  uint32_t above;
+  uint32_t kr = (uint32_t)p.K;
+  const uint32_t b0 = find_digit<8>(c8, kr, sc, &above);
   kr -= above;
-  prefix = d;
-  pbits = 12;
-  const int E = (cnt + kThreads - 1) / kThreads;  // per-thread contiguous ranges, in order
-  const int a = min(cnt, tid * E), z = min(cnt, a + E);
 
-  if (in_bin <= (uint32_t)kCand && in_bin != kr) {
-    // ---- few candidates: list them, exchange the lists, resolve T in every CTA
-    uint32_t n_gt = 0, n_c = 0;
-    for (int i = a; i < z; ++i) {
-      const uint32_t b = key_at(i) >> 20;
-      n_gt += b > d;
-      n_c += b == d;
-    }
-    const uint32_t c_incl = block_incl_scan(n_c, sc);
-    const uint32_t gt_incl = block_incl_scan(n_gt, sc);
-    uint32_t at = c_incl - n_c;
-    for (int i = a; i < z; ++i) {
-      const uint32_t key = key_at(i);
-      if ((key >> 20) == d) {
-        own_key[at] = key;
-        own_pos[at] = (uint32_t)(lo + i);
-        ++at;
-      }
-    }
-    if (tid == kThreads - 1) {
-      counts[0] = c_incl;   // candidates of this CTA
-      counts[1] = gt_incl;  // keys in higher bins
-    }
-    cluster_sync();  // lists and counts complete
-    // warp 0: lane q reads CTA q's counts; exclusive prefixes give each list's place
-    if (tid < 32) {
-      const uint32_t cq = tid < C ? dsmem_ld_u32(dsmem_addr(&counts[0], (uint32_t)tid)) : 0u;
-      const uint32_t gq = tid < C ? dsmem_ld_u32(dsmem_addr(&counts[1], (uint32_t)tid)) : 0u;
-      uint32_t ci = cq, gi = gq;
+  // ---- pass A: this CTA's candidates (bin b0) and its count of keys above b0
+  {
+    uint32_t n_above = 0;
+    for (int base = 0; base < cnt; base += kChunk) {
+      const int i = base + 4 * tid;
+      uint32_t k[4];
+      load4(i, k);
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t a = __shfl_up_sync(0xffffffffu, ci, o), b = __shfl_up_sync(0xffffffffu, gi, o);
-        if (tid >= o) {
-          ci += a;
-          gi += b;
-        }
-      }
-      sc[32 + tid] = ci - cq;  // candidates before CTA tid
-      if (tid == r) sc[80] = gi - gq;  // keys in higher bins before this CTA
-      if (tid == 31) sc[81] = ci;      // all candidates
-    }
-    __syncthreads();
-    const uint32_t total = sc[81], my_start = sc[32 + r], gt_before = sc[80];
-    // copy every CTA's list (rank order = position order): thread tid fetches entries
-    // tid, tid + 512, ... of the concatenated lists, all remote loads first, then the stores
-    {
-      constexpr int PER = kCand / kThreads;
-      uint32_t kk[PER], pp[PER];
-#pragma unroll
-      for (int e = 0; e < PER; ++e) {
-        const uint32_t j = (uint32_t)(tid + e * kThreads);
-        kk[e] = pp[e] = 0;
-        if (j < total) {
-          int q = 0;
-          while (q + 1 < C && sc[32 + q + 1] <= j) ++q;  // the CTA whose list holds entry j
-          const uint32_t local = j - sc[32 + q];
-          kk[e] = dsmem_ld_u32(dsmem_addr(own_key, (uint32_t)q) + 4 * local);
-          pp[e] = dsmem_ld_u32(dsmem_addr(own_pos, (uint32_t)q) + 4 * local);
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < PER; ++e) {
-        const uint32_t j = (uint32_t)(tid + e * kThreads);
-        if (j < total) {
-          all_key[j] = kk[e];
-          all_pos[j] = pp[e];
-        }
+      for (int j = 0; j < 4; ++j) {
+        const bool ok = i + j < cnt;
+        const uint32_t d = k[j] >> 20;
+        n_above += ok && d > b0;
+        list_append(own, &sc[120], S.own_cap, ok && d == b0, k[j], (uint32_t)(lo + i + j));
       }
     }
-    __syncthreads();
-    // two 10-bit passes over the candidates' low 20 bits
-    uint32_t pre = d;
-    int pb = 12;
-    for (int pass = 0; pass < 2; ++pass) {
-      for (int b = tid; b < 1024; b += kThreads) hist[b] = 0;
-      __syncthreads();
-      const int shift = 32 - pb - 10;
-      // few candidates spread over 1024 bins: plain shared-memory atomics rarely collide
-      for (int j = tid; j < (int)total; j += kThreads) {
-        const uint32_t key = all_key[j];
-        if ((key >> (32 - pb)) == pre) atomicAdd(&hist[(key >> shift) & 1023u], 1u);
-      }
-      __syncthreads();
-      uint32_t ab, ib;
-      uint32_t* ls = sc;  // find_digit reads a global histogram; here the bins are in shared memory
-      const int per = 2;  // 1024 bins / 512 threads
-      uint32_t c0 = hist[2 * tid], c1 = hist[2 * tid + 1];
-      uint32_t above1 = block_incl_suffix(c0 + c1, ls) - c0 - c1;
-      if (above1 < kr && above1 + c1 >= kr) { ls[64] = 2 * tid + 1; ls[65] = above1; }
-      const uint32_t above0 = above1 + c1;
-      if (above0 < kr && above0 + c0 >= kr) { ls[64] = 2 * tid; ls[65] = above0; }
-      __syncthreads();
-      const uint32_t dd = ls[64];
-      ab = ls[65];
-      (void)per;
-      (void)ib;
-      __syncthreads();
-      kr -= ab;
-      pre = (pre << 10) | dd;
-      pb += 10;
-    }
-    const uint32_t T = pre;  // full threshold key; take every key > T and the first kr keys == T
-    // selected candidates and ties before this CTA's part of the list
-    uint32_t sel_b = 0, tie_b = 0;
-    for (uint32_t j = tid; j < my_start; j += kThreads) {
-      sel_b += all_key[j] > T;
-      tie_b += all_key[j] == T;
-    }
-    sel_b = block_incl_scan(sel_b, sc);  // the last thread holds the block total
-    tie_b = block_incl_scan(tie_b, sc);
-    if (tid == kThreads - 1) {
-      sc[84] = sel_b;
-      sc[85] = tie_b;
-    }
-    __syncthreads();
-    const uint32_t ties_before_cta = sc[85];
-    const uint32_t tie_take_before = min(ties_before_cta, kr);
-    const uint32_t out_before_cta = gt_before + sc[84] + tie_take_before;
-    uint32_t n_sel = 0, n_tie = 0;
-    for (int i = a; i < z; ++i) {
-      const uint32_t key = key_at(i);
-      n_sel += key > T;
-      n_tie += key == T;
-    }
-    const uint32_t tie_incl = block_incl_scan(n_tie, sc);
-    const uint32_t tb = ties_before_cta + tie_incl - n_tie;  // ties before this thread's range
-    const uint32_t tie_take = tb >= kr ? 0u : min(n_tie, kr - tb);
-    const uint32_t take = n_sel + tie_take;
-    uint32_t pos = out_before_cta + block_incl_scan(take, sc) - take;
-    uint32_t tie_left = tie_take;
-    for (int i = a; i < z; ++i) {
-      const uint32_t key = key_at(i);
-      bool keep = key > T;
-      if (key == T && tie_left > 0) {
-        keep = true;
-        --tie_left;
-      }
-      if (keep && pos < (uint32_t)p.K) out[pos++] = lo + i;
-    }
-    cluster_sync();  // every CTA has read the lists
-    if (r == 0)
-      for (int b = tid; b < kHistBins; b += kThreads) g0[b] = 0;
-    return;
-  }
-
-  // ---- many candidates: levels 1 and 2 (next 12, then last 8 bits) over all keys
-  const int widths[2] = {12, 8};
-  uint32_t* gl[2] = {g1, g2};
-  for (int lv = 0; lv < 2 && in_bin != kr; ++lv) {
-    count_level(prefix, pbits, widths[lv], gl[lv]);
-    cluster_sync();
-    d = find_digit(gl[lv], 1 << widths[lv], kr, sc, above, in_bin);
-    kr -= above;
-    prefix = (prefix << widths[lv]) | d;
-    pbits += widths[lv];
-  }
-  // selected: top bits > prefix, plus the first kr keys (by position) whose top bits == prefix
-  const int sh = 32 - pbits;
-  uint32_t n_gt = 0, n_eq = 0;
-  for (int i = a; i < z; ++i) {
-    const uint32_t k = key_at(i) >> sh;
-    n_gt += k > prefix;
-    n_eq += k == prefix;
-  }
-  const uint32_t eq_incl = block_incl_scan(n_eq, sc);
-  const uint32_t gt_incl = block_incl_scan(n_gt, sc);
-  if (tid == kThreads - 1) {
-    counts[0] = gt_incl;
-    counts[1] = eq_incl;
-  }
-  cluster_sync();  // per-CTA counts visible to the cluster
-  if (tid == 0) {
-    uint32_t eq_before = 0, out_before = 0;
-    for (int q = 0; q < r; ++q) {
-      const uint32_t gt_q = dsmem_ld_u32(dsmem_addr(&counts[0], (uint32_t)q));
-      const uint32_t eq_q = dsmem_ld_u32(dsmem_addr(&counts[1], (uint32_t)q));
-      const uint32_t take_q = eq_before >= kr ? 0u : min(eq_q, kr - eq_before);
-      out_before += gt_q + take_q;
-      eq_before += eq_q;
-    }
-    sc[80] = eq_before;
-    sc[81] = out_before;
+    n_above = __reduce_add_sync(0xffffffffu, n_above);
+    if ((tid & 31) == 0 && n_above) atomicAdd(&sc[121], n_above);
   }
   __syncthreads();
-  const uint32_t eq_before = sc[80] + eq_incl - n_eq;
-  const uint32_t eq_take = eq_before >= kr ? 0u : min(n_eq, kr - eq_before);
-  const uint32_t take = n_gt + eq_take;
-  uint32_t pos = sc[81] + block_incl_scan(take, sc) - take;
-  uint32_t eq_left = eq_take;
-  for (int i = a; i < z; ++i) {
-    const uint32_t k = key_at(i) >> sh;
-    bool keep = k > prefix;
-    if (k == prefix && eq_left > 0) {
-      keep = true;
-      --eq_left;
-    }
-    if (keep && pos < (uint32_t)p.K) out[pos++] = lo + i;
+  const uint32_t own_cand = sc[120];
+  if (tid == 0) {
+    pub[0] = own_cand;
+    pub[1] = sc[121];
   }
-  cluster_sync();  // every CTA has read the counts and the global histograms
-  if (r == 0) {
-    for (int b = tid; b < kHistBins; b += kThreads) {
-      g0[b] = 0;
-      g1[b] = 0;
-    }
-    for (int b = tid; b < 256; b += kThreads) g2[b] = 0;
+  {
+    const uint32_t m = min(own_cand, (uint32_t)kRegion);
+    uint2* region = glist + (int64_t)r * kRegion;
+    for (uint32_t j = tid; j < m; j += kThreads) region[j] = own[j];
   }
+  cluster_sync();  // lists and counts of every CTA are published
+
+  // ---- every CTA's counts (distributed shared memory): list offsets, keys above b0 before
+  if (tid < 32) {
+    const uint2 v = tid < C ? dsmem_ld_u2(dsmem_addr(pub, (uint32_t)tid)) : make_uint2(0u, 0u);
+    uint32_t x = v.x, mx = v.x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (tid >= o) x += y;
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    const uint32_t ab = __reduce_add_sync(0xffffffffu, tid < r ? v.y : 0u);
+    if (tid <= 16) sc[64 + tid] = x - v.x;  // entries before CTA tid (entry C = total)
+    if (tid == 0) {
+      sc[96] = mx;
+      sc[97] = ab;
+    }
+  }
+  __syncthreads();
+  const uint32_t total = sc[64 + 16];
+  const bool few = total <= (uint32_t)kCand && sc[96] <= (uint32_t)kRegion;
+  uint32_t gt_before = sc[97], eq_before = 0;
+  uint32_t T;
+  uint64_t bf = 0;  // (list keys > T << 48) | (list keys == T << 32) before this slice, per thread
+
+  if (few) {
+    cluster_arrive();  // this CTA's reads of the others' shared memory are done
+    // ---- few candidates: every CTA's list, levels 1 and 2 resolved here
+    uint2 e[kGather];
+#pragma unroll
+    for (int g = 0; g < kGather; ++g) {
+      const uint32_t j = (uint32_t)(tid + g * kThreads);
+      e[g] = make_uint2(0u, 0u);
+      if (j < total) {
+        int q = 0;  // the CTA whose list holds entry j: largest q with offset(q) <= j
+#pragma unroll
+        for (int step = 8; step > 0; step >>= 1)
+          if (q + step < C && sc[64 + q + step] <= j) q += step;
+        e[g] = __ldcg(glist + (int64_t)q * kRegion + (j - sc[64 + q]));
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < kGather; ++g) {
+      const uint32_t j = (uint32_t)(tid + g * kThreads);
+      hist_add(h1, j < total ? (e[g].x >> 10) & (kLevelBins - 1) : kNoBin);
+    }
+    __syncthreads();
+    uint32_t c2[2] = {h1[2 * tid], h1[2 * tid + 1]};
+    const uint32_t d1 = find_digit<2>(c2, kr, sc, &above);
+    kr -= above;
+    const uint32_t p22 = (b0 << 10) | d1;
+#pragma unroll
+    for (int g = 0; g < kGather; ++g) {
+      const uint32_t j = (uint32_t)(tid + g * kThreads);
+      const bool m = j < total && (e[g].x >> 10) == p22;
+      hist_add(h2, m ? e[g].x & (kLevelBins - 1) : kNoBin);
+    }
+    __syncthreads();
+    c2[0] = h2[2 * tid];
+    c2[1] = h2[2 * tid + 1];
+    const uint32_t d2 = find_digit<2>(c2, kr, sc, &above);
+    kr -= above;
+    T = (p22 << 10) | d2;
+    uint32_t g_ = 0, q_ = 0;
+#pragma unroll
+    for (int g = 0; g < kGather; ++g) {
+      const uint32_t j = (uint32_t)(tid + g * kThreads);
+      const bool m = j < total && e[g].y < (uint32_t)lo;
+      g_ += m && e[g].x > T;
+      q_ += m && e[g].x == T;
+    }
+    bf = ((uint64_t)g_ << 48) | ((uint64_t)q_ << 32);
+  } else {
+    // ---- many candidates: levels 1 and 2 and the per-CTA counts go through the cluster
+    const bool listed = own_cand <= (uint32_t)S.own_cap;
+    uint32_t prefix = b0;
+    int pbits = 12;
+#pragma unroll 1
+    for (int lv = 0; lv < 2; ++lv) {
+      uint32_t* h = lv == 0 ? h1 : h2;
+      uint32_t* gh = lv == 0 ? gh1 : gh2;
+      const int shift = 32 - pbits - 10;
+      if (listed) {
+        for (uint32_t j0 = 0; j0 < own_cand; j0 += kThreads) {
+          const uint32_t j = j0 + tid;
+          const bool m = j < own_cand && (own[j].x >> (32 - pbits)) == prefix;
+          hist_add(h, m ? (own[j].x >> shift) & (kLevelBins - 1) : kNoBin);
+        }
+      } else {
+        for (int base = 0; base < cnt; base += kChunk) {
+          const int i = base + 4 * tid;
+          uint32_t k[4];
+          load4(i, k);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const bool m = i + j < cnt && (k[j] >> (32 - pbits)) == prefix;
+            hist_add(h, m ? (k[j] >> shift) & (kLevelBins - 1) : kNoBin);
+          }
+        }
+      }
+      __syncthreads();
+      flush_bins(h, gh, kLevelBins);
+      cluster_sync();  // every CTA's level counts are in gh
+      uint32_t c2[2];
+      load_bins<2>(gh, c2);
+      const uint32_t d = find_digit<2>(c2, kr, sc, &above);
+      kr -= above;
+      prefix = (prefix << 10) | d;
+      pbits += 10;
+    }
+    T = prefix;
+    uint32_t g_ = 0, q_ = 0;  // this CTA's candidates above T, keys equal to T
+    if (listed) {
+      for (uint32_t j = tid; j < own_cand; j += kThreads) {
+        const uint32_t key = own[j].x;
+        g_ += key > T;
+        q_ += key == T;
+      }
+    } else {
+      for (int base = 0; base < cnt; base += kChunk) {
+        const int i = base + 4 * tid;
+        uint32_t k[4];
+        load4(i, k);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          g_ += i + j < cnt && (k[j] >> 20) == b0 && k[j] > T;
+          q_ += i + j < cnt && k[j] == T;
+        }
+      }
+    }
+    uint64_t tot;
+    block_excl_scan(((uint64_t)g_ << 32) | q_, sc, &tot);
+    if (tid == 0) {
+      pub[2] = pub[1] + (uint32_t)(tot >> 32);  // keys above T
+      pub[3] = (uint32_t)tot;                   // keys equal to T
+    }
+    cluster_sync();  // per-CTA counts visible
+    if (tid < 32) {
+      const uint2 v = tid < r ? dsmem_ld_u2(dsmem_addr(pub + 2, (uint32_t)tid)) : make_uint2(0u, 0u);
+      const uint32_t x = __reduce_add_sync(0xffffffffu, v.x), y = __reduce_add_sync(0xffffffffu, v.y);
+      if (tid == 0) {
+        sc[98] = x;
+        sc[99] = y;
+      }
+    }
+    __syncthreads();
+    cluster_arrive();  // this CTA's reads of the others' shared memory are done
+    gt_before = sc[98];
+    eq_before = sc[99];
+  }
+
+  // ---- output, ascending positions: slot = (keys > T before) + min(keys == T before, kr).
+  // One 64-bit scan per chunk: low half = (ties << 16 | keys above T) prefix in the chunk, high
+  // half = the list counts before this slice (first chunk only; summed over the block).
+  uint32_t gt_in = 0, eq_in = 0;  // keys above T / ties of this slice before the chunk
+  for (int base = 0; base < cnt; base += kChunk) {
+    const int i = base + 4 * tid;
+    uint32_t k[4];
+    load4(i, k);
+    uint32_t ng = 0, ne = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      ng += i + j < cnt && k[j] > T;
+      ne += i + j < cnt && k[j] == T;
+    }
+    uint64_t tot;
+    const uint64_t ex = block_excl_scan((uint64_t)(ng | (ne << 16)) | (base == 0 ? bf : 0ull), sc, &tot);
+    if (base == 0) {
+      gt_before += (uint32_t)(tot >> 48);
+      eq_before += (uint32_t)(tot >> 32) & 0xFFFFu;
+    }
+    uint32_t gb = gt_before + gt_in + ((uint32_t)ex & 0xFFFFu);
+    uint32_t eb = eq_before + eq_in + (((uint32_t)ex >> 16) & 0xFFFFu);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const bool ok = i + j < cnt;
+      const bool is_gt = ok && k[j] > T, is_eq = ok && k[j] == T;
+      if (is_gt || (is_eq && eb < kr)) {
+        const uint32_t slot = gb + min(eb, kr);
+        if (slot < (uint32_t)p.K) out[slot] = lo + i + j;
+      }
+      gb += is_gt;
+      eb += is_eq;
+    }
+    gt_in += (uint32_t)tot & 0xFFFFu;
+    eq_in += ((uint32_t)tot >> 16) & 0xFFFFu;
+  }
+  cluster_wait();  // every CTA is past its reads of the workspace histograms and of this CTA
+  // leave the workspace histograms zeroed, split over the cluster's CTAs
+  for (int i = r * kThreads + tid; i < kHistBins / 4; i += C * kThreads)
+    reinterpret_cast<uint4*>(gh0)[i] = make_uint4(0u, 0u, 0u, 0u);
+  if (!few)
+    for (int i = r * kThreads + tid; i < 2 * kLevelBins / 4; i += C * kThreads)
+      reinterpret_cast<uint4*>(gh1)[i] = make_uint4(0u, 0u, 0u, 0u);  // gh1 and gh2 are adjacent
 }
 
-// About 2048 keys per CTA, at most 16 CTAs per cluster.
-int cluster_ctas(int n_max) {
+// About 2048 keys per CTA, at most 16 CTAs per cluster; at most 8 when more clusters are needed
+// than 16-CTA clusters can run at once.
+int cluster_ctas(int n_max, int T, size_t smem16) {
   int c = 1;
   while (c < 16 && (int64_t)c * 2048 < n_max) c <<= 1;
+  if (c == 16) {
+    static std::mutex mu;
+    static size_t cached_smem = 0;
+    static int cached_active = 0;
+    int active = 0;
+    {
+      std::lock_guard<std::mutex> lock(mu);
+      if (cached_smem == smem16) active = cached_active;
+    }
+    if (active == 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(16, 1);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = smem16;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 16;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&active, topk_cluster_kernel, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        active = 1;
+      }
+      std::lock_guard<std::mutex> lock(mu);
+      cached_smem = smem16;
+      cached_active = active;
+    }
+    if (T > active) c = 8;
+  }
   return c;
 }
 
 }  // namespace
 
-size_t topk_ws_bytes(int T, int, int) { return align_up((size_t)T * kWorkWords * sizeof(uint32_t), 256); }
+// Largest cluster a row of n_max positions can use (the launch may use fewer).
+int cluster_ctas_max(int n_max) {
+  int c = 1;
+  while (c < 16 && (int64_t)c * 2048 < n_max) c <<= 1;
+  return c;
+}
+
+size_t topk_ws_bytes(int T, int L, int) {
+  return align_up((size_t)T * ws_words(cluster_ctas_max(L)) * sizeof(uint32_t), 256);
+}
 
 cudaError_t launch_topk(const TopkParams& p, void* ws, cudaStream_t stream, bool pdl) {
   if (p.T <= 0) return cudaSuccess;
@@ -441,11 +586,15 @@ cudaError_t launch_topk(const TopkParams& p, void* ws, cudaStream_t stream, bool
   TopkParams q = p;
   q.work = reinterpret_cast<uint32_t*>(ws);
   auto kern = topk_cluster_kernel;
-  const int C = cluster_ctas(p.L);
-  const int slice = (((p.L + C - 1) / C) + 31) & ~31;  // the largest slice of any query
-  const size_t smem = (size_t)TopkSmem(slice, slice <= kCachedKeys).words * 4;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  if (p.K > kMaxK) return cudaErrorNotSupported;
+  const size_t smem16 = (size_t)TopkSmem(slice_of(p.L, 16)).words * 4;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem16);
+  if (e != cudaSuccess) return e;
+  const int C = cluster_ctas(p.L, p.T, smem16);
+  const size_t smem = (size_t)TopkSmem(slice_of(p.L, C)).words * 4;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, p.T);
@@ -470,12 +619,13 @@ cudaError_t launch_topk(const TopkParams& p, void* ws, cudaStream_t stream, bool
 // Some callers cannot hand the library device memory: a host framework that owns every device
 // allocation through its own pool and forbids raw cudaMalloc, or a decode loop that must not
 // allocate while it runs (an allocation can synchronise the device and fragment memory).  For
-// them dsa_topk_noalloc keeps the Top-K level histograms in the file-scope array below, sized for
-// kNoAllocMaxQueries queries.  Every GPU that loads the library holds these bytes until the
-// process exits.
+// them dsa_topk_noalloc keeps the Top-K exchange areas (histograms, counts, candidate lists) in
+// the file-scope array below, sized for kNoAllocMaxQueries queries.  Every GPU that loads the
+// library holds these bytes until the process exits.
 
-constexpr int kNoAllocMaxQueries = 64;
-static __device__ __align__(256) uint32_t g_topk_scratch[kNoAllocMaxQueries * kWorkWords];
+constexpr int kNoAllocMaxQueries = 16;
+constexpr int64_t kNoAllocWords = kNoAllocMaxQueries * (kWsList + 2 * 16 * kRegion);
+static __device__ __align__(256) uint32_t g_topk_scratch[kNoAllocWords];
 
 namespace {
 
@@ -515,7 +665,7 @@ extern "C" dsa_status dsa_topk_noalloc(const float* scores, int64_t ld_scores, i
   if (scratch_address(&scratch) != cudaSuccess) return DSA_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // the histograms must start at zero; the array keeps whatever the previous call left
-  if (cudaMemsetAsync(scratch, 0, (size_t)T * kWorkWords * sizeof(uint32_t), st) != cudaSuccess)
+  if (cudaMemsetAsync(scratch, 0, topk_ws_bytes(T, L, K), st) != cudaSuccess)
     return DSA_ERR_CUDA;
   TopkParams p = {};
   p.scores = scores;
