@@ -173,6 +173,15 @@ cudaError_t run_topk(const dsa_args& a, int t_off, int T, const float* scores, i
   p.t_off = t_off;
   p.err = device_error_ptr();
   p.hist = hist;
+  // the chain prefetches the selected cache rows for the attention step
+  p.kv = reinterpret_cast<const uint8_t*>(a.kv);
+  p.kv_row_stride = a.kv_row_stride;
+  p.kv_seq_stride = a.kv_seq_stride;
+  p.kv_bytes = a.D_qk * (a.kv_dtype == DSA_BF16 ? 2 : 1);
+  p.kv_v = reinterpret_cast<const uint8_t*>(a.kv_v);
+  p.v_row_stride = a.v_row_stride;
+  p.v_seq_stride = a.v_seq_stride;
+  p.v_bytes = a.D_v * 2;
   return launch_topk(p, ws, st, pdl);
 }
 

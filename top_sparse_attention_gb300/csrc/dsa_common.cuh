@@ -336,6 +336,11 @@ __device__ __forceinline__ float4 dsmem_ld_f4(uint32_t addr) {
   return v;
 }
 
+// Asynchronous prefetch of `bytes` (a multiple of 16, 16-byte aligned address) into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ------------------------------------------------------------------------------------------
 // Programmatic dependent launch (no-ops when the launch did not opt in)
 

@@ -73,7 +73,15 @@ struct TopkParams {
   int* err;                // device error word
   uint32_t* hist;          // [T][4096] top-12-bit histograms from the index-score kernel, or
                            // null (then built here); zeroed after use
-  uint32_t* work;          // per-query level histograms (set by launch_topk from its workspace)
+  uint32_t* work;          // per-query exchange areas (set by launch_topk from its workspace)
+  // Optional L2 prefetch of the selected rows of the attention cache (null kv: none), issued as
+  // each selected position is written.
+  const uint8_t* kv;
+  int64_t kv_row_stride, kv_seq_stride;
+  int kv_bytes;            // bytes of a row to prefetch (a multiple of 16)
+  const uint8_t* kv_v;     // separate V rows, or null
+  int64_t v_row_stride, v_seq_stride;
+  int v_bytes;
 };
 
 cudaError_t launch_topk(const TopkParams& p, void* ws, cudaStream_t stream, bool pdl);

@@ -3,7 +3,7 @@
 // Day-0 Readiness...", section 2.1).
 //
 // Radix select on order-preserving 32-bit keys of the fp32 scores, never sorting.  One
-// thread-block cluster of C CTAs (C = 1..16, about 2048 positions per CTA) handles one query; CTA
+// thread-block cluster of C CTAs (C = 1..16, about 4096 positions per CTA) handles one query; CTA
 // r owns a contiguous slice of the query's positions and keeps its keys in shared memory when the
 // slice fits.  Threads read keys four at a time (16-byte loads, chunk-major, thread order within a
 // chunk equals position order).  Bulk data crosses CTAs through a per-query area of the workspace
@@ -16,15 +16,18 @@
 //  * Pass A: each CTA lists its candidates (keys in bin b0, with positions), counts its keys
 //    above b0 and copies the list to its own region of the workspace.  One barrier; the counts
 //    then come from the other CTAs' shared memory.
-//  * Few candidates (at most 4096 in the query and 1024 in any CTA, the usual case): every CTA
-//    reads every list and resolves the last 20 bits of the threshold key T with two 10-bit
-//    levels on its own; the lists also give the keys above T and equal to T before its slice.
+//  * Few candidates (at most 1024 in any CTA, the usual case): every CTA reads every list (thread
+//    i holds entry i of each) and resolves the last 20 bits of the threshold key T with two
+//    10-bit levels on its own; the lists also give the keys above T and equal to T before its
+//    slice.
 //    Many candidates: the two levels and the per-CTA counts go through the cluster, one barrier
 //    each.
 //  * Output, ascending positions: the slot of a kept key is (keys > T before it) + min(keys == T
 //    before it, ties to take), so exact ties go to the lower positions; each CTA writes its keys
 //    straight to the index row.
-// The workspace histograms are zeroed again before the kernel ends.
+// The workspace histograms are zeroed again before the kernel ends.  In the fused chain the kernel
+// also starts the attention step's cache reads: every selected row is prefetched into L2 as its
+// position is written, so the reads overlap the kernel boundary.
 #include <mutex>
 
 #include "dsa_internal.h"
@@ -32,16 +35,24 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kChunk = 4 * kThreads;  // keys per block-wide step
 constexpr int kCachedKeys = 16384;    // largest slice kept in shared memory
-constexpr int kCand = 4096;           // candidates gathered into every CTA (registers)
-constexpr int kGather = kCand / kThreads;
-constexpr int kRegion = 1024;         // workspace list entries per CTA
+constexpr int kCand = 4096;           // own candidate list capacity (shared memory)
+constexpr int kRegion = kThreads;     // workspace list entries per CTA (one per thread)
 constexpr int kMaxK = 4096;
 constexpr int kLevelBins = 1024;      // levels 1 and 2: 10-bit digits
 constexpr uint32_t kNoBin = 0xFFFFFFFFu;
+constexpr int kBins0 = kHistBins / kThreads;   // level-0 bins per thread
+constexpr int kBins1 = kLevelBins / kThreads;  // level-1/2 bins per thread
+static_assert(kBins1 >= 1 && kWarps <= 32, "block shape");
+// scratch words in sc: [0, 2 * kWarps + 2) scans; named slots from kScOff
+constexpr int kScOff = 128;   // [kScOff + q] list entries before CTA q, q = 0..16
+constexpr int kScMax = 160;   // longest list
+constexpr int kScAbove = 161; // keys above b0 in the CTAs before this one
+constexpr int kScGt = 162, kScEq = 163;  // many-candidate path: counts before this CTA
+constexpr int kScCand = 200, kScAboveOwn = 201;  // this CTA's candidate and above-b0 counters
 
 // Per-query workspace, in 32-bit words: level-0 histogram (when the chain does not supply one) |
 // level-1 histogram | level-2 histogram | C lists of kRegion (key, position) entries.
@@ -61,8 +72,8 @@ struct TopkSmem {
     h0 = 0;                        // level-0 counts of this CTA (kHistBins)
     h1 = h0 + kHistBins;           // level-1 counts
     h2 = h1 + kLevelBins;          // level-2 counts
-    sc = h2 + kLevelBins;          // 128 words of scan scratch and broadcasts
-    pub = sc + 128;                // 8 words read by the other CTAs of the cluster
+    sc = h2 + kLevelBins;          // 256 words of scan scratch and broadcasts
+    pub = sc + 256;                // 8 words read by the other CTAs of the cluster
     own = pub + 8;                 // this CTA's candidates (key, position), own_cap entries
     keys = own + 2 * own_cap;      // cached keys (16-byte aligned: every offset is a multiple of 4)
     words = keys + (cached ? slice_max : 0);
@@ -146,14 +157,14 @@ __device__ __forceinline__ uint32_t find_digit(const uint32_t (&c)[PER], uint32_
 #pragma unroll
   for (int k = PER - 1; k >= 0; --k) {
     if (a < kr && a + c[k] >= kr) {  // exactly one bin of the block satisfies this
-      sc[32] = (uint32_t)(threadIdx.x * PER + k);
-      sc[33] = a;
+      sc[kWarps] = (uint32_t)(threadIdx.x * PER + k);
+      sc[kWarps + 1] = a;
     }
     a += c[k];
   }
   __syncthreads();
-  const uint32_t d = sc[32];
-  *above = sc[33];
+  const uint32_t d = sc[kWarps];
+  *above = sc[kWarps + 1];
   __syncthreads();
   return d;
 }
@@ -161,14 +172,18 @@ __device__ __forceinline__ uint32_t find_digit(const uint32_t (&c)[PER], uint32_
 // Global histogram read as PER consecutive bins per thread.
 template <int PER>
 __device__ __forceinline__ void load_bins(const uint32_t* g, uint32_t (&c)[PER]) {
-  static_assert(PER == 2 || PER == 8, "bins per thread");
-  if constexpr (PER == 8) {
-    const uint4 a = __ldcg(reinterpret_cast<const uint4*>(g) + 2 * threadIdx.x);
-    const uint4 b = __ldcg(reinterpret_cast<const uint4*>(g) + 2 * threadIdx.x + 1);
-    c[0] = a.x, c[1] = a.y, c[2] = a.z, c[3] = a.w, c[4] = b.x, c[5] = b.y, c[6] = b.z, c[7] = b.w;
-  } else {
+  if constexpr (PER % 4 == 0) {
+#pragma unroll
+    for (int v = 0; v < PER / 4; ++v) {
+      const uint4 a = __ldcg(reinterpret_cast<const uint4*>(g) + (PER / 4) * threadIdx.x + v);
+      c[4 * v] = a.x, c[4 * v + 1] = a.y, c[4 * v + 2] = a.z, c[4 * v + 3] = a.w;
+    }
+  } else if constexpr (PER == 2) {
     const uint2 a = __ldcg(reinterpret_cast<const uint2*>(g) + threadIdx.x);
     c[0] = a.x, c[1] = a.y;
+  } else {
+    static_assert(PER == 1, "bins per thread");
+    c[0] = __ldcg(g + threadIdx.x);
   }
 }
 
@@ -178,20 +193,6 @@ __device__ __forceinline__ void flush_bins(const uint32_t* h, uint32_t* g, int b
     const uint32_t v = h[b];
     if (v) atomicAdd(&g[b], v);
   }
-}
-
-// Warp-aggregated append of (key, position) to a shared-memory list; every lane must call it.
-__device__ __forceinline__ void list_append(uint2* list, uint32_t* count, int cap, bool take, uint32_t key,
-                                            uint32_t pos) {
-  const uint32_t ballot = __ballot_sync(0xffffffffu, take);
-  if (ballot == 0u) return;
-  const int lane = threadIdx.x & 31;
-  const int leader = __ffs(ballot) - 1;
-  uint32_t base = 0;
-  if (lane == leader) base = atomicAdd(count, (uint32_t)__popc(ballot));
-  base = __shfl_sync(0xffffffffu, base, leader);
-  const uint32_t at = base + __popc(ballot & ((1u << lane) - 1u));
-  if (take && at < (uint32_t)cap) list[at] = make_uint2(key, pos);
 }
 
 __device__ __forceinline__ void cluster_arrive() {
@@ -218,10 +219,22 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkParams
   uint32_t* gh2 = ws + kWsGh2;
   uint2* glist = reinterpret_cast<uint2*>(ws + kWsList);
 
+  // L2 prefetch of a selected row of the attention cache (chain only)
+  const int64_t seq = (t + p.t_off) / p.q_per_seq;
+  const uint8_t* pf_kv = p.kv ? p.kv + seq * p.kv_seq_stride : nullptr;
+  const uint8_t* pf_v = p.kv_v ? p.kv_v + seq * p.v_seq_stride : nullptr;
+  auto prefetch_row = [&](uint32_t pos) {
+    prefetch_l2(pf_kv + (int64_t)pos * p.kv_row_stride, (uint32_t)p.kv_bytes);
+    if (pf_v) prefetch_l2(pf_v + (int64_t)pos * p.v_row_stride, (uint32_t)p.v_bytes);
+  };
+
   if (n <= p.K) {  // the whole cluster leaves here together (n is the same for all its CTAs)
     if (r == 0 && p.hist)
       for (int b = tid; b < kHistBins; b += kThreads) gh0[b] = 0;  // leave it zeroed
-    for (int i = r * kThreads + tid; i < p.K; i += C * kThreads) out[i] = i < n ? i : -1;
+    for (int i = r * kThreads + tid; i < p.K; i += C * kThreads) {
+      out[i] = i < n ? i : -1;
+      if (pf_kv && i < n) prefetch_row((uint32_t)i);
+    }
     return;
   }
   const TopkSmem S(slice_of(p.L, C));
@@ -260,8 +273,8 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkParams
   };
 
   // ---- loads: the level-0 counts (when ready-made) and this slice's keys, all in flight at once
-  uint32_t c8[8];
-  if (p.hist) load_bins<8>(gh0, c8);
+  uint32_t c0[kBins0];
+  if (p.hist) load_bins<kBins0>(gh0, c0);
   if (S.cached) {
     constexpr int kFill = kCachedKeys / kChunk;
     uint32_t k[kFill][4];
@@ -274,14 +287,13 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkParams
       if (i < cnt) *reinterpret_cast<uint4*>(keys + i) = make_uint4(k[f][0], k[f][1], k[f][2], k[f][3]);
     }
   }
-  h1[2 * tid] = h1[2 * tid + 1] = 0;
-  h2[2 * tid] = h2[2 * tid + 1] = 0;
-  if (tid == 0) sc[120] = sc[121] = 0;  // this CTA's candidates, keys above b0
+#pragma unroll
+  for (int k = 0; k < kBins1; ++k) h1[kBins1 * tid + k] = h2[kBins1 * tid + k] = 0;
+  if (tid == 0) sc[kScCand] = sc[kScAboveOwn] = 0;
 
   // ---- level 0: top 12 bits
   if (!p.hist) {
-    reinterpret_cast<uint4*>(h0)[2 * tid] = make_uint4(0u, 0u, 0u, 0u);
-    reinterpret_cast<uint4*>(h0)[2 * tid + 1] = make_uint4(0u, 0u, 0u, 0u);
+    for (int b = tid; b < kHistBins / 4; b += kThreads) reinterpret_cast<uint4*>(h0)[b] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
     for (int base = 0; base < cnt; base += kChunk) {
       const int i = base + 4 * tid;
@@ -293,38 +305,57 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkParams
     __syncthreads();
     flush_bins(h0, gh0, kHistBins);
     cluster_sync();  // every CTA's counts are in gh0 (the barrier's release orders the atomics)
-    load_bins<8>(gh0, c8);
+    load_bins<kBins0>(gh0, c0);
   } else {
     __syncthreads();  // cached keys and cleared histograms visible
   }
   uint32_t above;
   uint32_t kr = (uint32_t)p.K;
-  const uint32_t b0 = find_digit<8>(c8, kr, sc, &above);
+  const uint32_t b0 = find_digit<kBins0>(c0, kr, sc, &above);
   kr -= above;
 
   // ---- pass A: this CTA's candidates (bin b0) and its count of keys above b0
   {
     uint32_t n_above = 0;
+    const int lane = tid & 31;
     for (int base = 0; base < cnt; base += kChunk) {
       const int i = base + 4 * tid;
       uint32_t k[4];
       load4(i, k);
+      uint32_t cm = 0;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const bool ok = i + j < cnt;
         const uint32_t d = k[j] >> 20;
         n_above += ok && d > b0;
-        list_append(own, &sc[120], S.own_cap, ok && d == b0, k[j], (uint32_t)(lo + i + j));
+        cm |= (uint32_t)(ok && d == b0) << j;
       }
+      // one shared-memory atomic per warp places the warp's candidates
+      const uint32_t nc = __popc(cm);
+      uint32_t x = nc;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      uint32_t at = 0;
+      if (lane == 31 && x) at = atomicAdd(&sc[kScCand], x);
+      at = __shfl_sync(0xffffffffu, at, 31) + x - nc;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if ((cm >> j) & 1u) {
+          if (at < (uint32_t)S.own_cap) own[at] = make_uint2(k[j], (uint32_t)(lo + i + j));
+          ++at;
+        }
     }
     n_above = __reduce_add_sync(0xffffffffu, n_above);
-    if ((tid & 31) == 0 && n_above) atomicAdd(&sc[121], n_above);
+    if ((tid & 31) == 0 && n_above) atomicAdd(&sc[kScAboveOwn], n_above);
   }
   __syncthreads();
-  const uint32_t own_cand = sc[120];
+  const uint32_t own_cand = sc[kScCand];
   if (tid == 0) {
     pub[0] = own_cand;
-    pub[1] = sc[121];
+    pub[1] = sc[kScAboveOwn];
   }
   {
     const uint32_t m = min(own_cand, (uint32_t)kRegion);
@@ -336,6 +367,7 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkParams
   // ---- every CTA's counts (distributed shared memory): list offsets, keys above b0 before
   if (tid < 32) {
     const uint2 v = tid < C ? dsmem_ld_u2(dsmem_addr(pub, (uint32_t)tid)) : make_uint2(0u, 0u);
+    (void)__reduce_or_sync(0xffffffffu, v.x);  // every lane's count has arrived before the scan
     uint32_t x = v.x, mx = v.x;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -344,64 +376,56 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkParams
       mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     }
     const uint32_t ab = __reduce_add_sync(0xffffffffu, tid < r ? v.y : 0u);
-    if (tid <= 16) sc[64 + tid] = x - v.x;  // entries before CTA tid (entry C = total)
+    if (tid <= 16) sc[kScOff + tid] = x - v.x;  // entries before CTA tid (entry C = total)
     if (tid == 0) {
-      sc[96] = mx;
-      sc[97] = ab;
+      sc[kScMax] = mx;
+      sc[kScAbove] = ab;
     }
   }
   __syncthreads();
-  const uint32_t total = sc[64 + 16];
-  const bool few = total <= (uint32_t)kCand && sc[96] <= (uint32_t)kRegion;
-  uint32_t gt_before = sc[97], eq_before = 0;
+  const bool few = sc[kScMax] <= (uint32_t)kRegion;
+  uint32_t gt_before = sc[kScAbove], eq_before = 0;
   uint32_t T;
   uint64_t bf = 0;  // (list keys > T << 48) | (list keys == T << 32) before this slice, per thread
 
   if (few) {
     cluster_arrive();  // this CTA's reads of the others' shared memory are done
     // ---- few candidates: every CTA's list, levels 1 and 2 resolved here
-    uint2 e[kGather];
+    // entry tid of every CTA's list (a list holds at most kRegion = kThreads entries):
+    // coalesced loads, no search for the owner
+    uint2 e[16];
+    bool ev[16];
 #pragma unroll
-    for (int g = 0; g < kGather; ++g) {
-      const uint32_t j = (uint32_t)(tid + g * kThreads);
-      e[g] = make_uint2(0u, 0u);
-      if (j < total) {
-        int q = 0;  // the CTA whose list holds entry j: largest q with offset(q) <= j
-#pragma unroll
-        for (int step = 8; step > 0; step >>= 1)
-          if (q + step < C && sc[64 + q + step] <= j) q += step;
-        e[g] = __ldcg(glist + (int64_t)q * kRegion + (j - sc[64 + q]));
-      }
+    for (int q = 0; q < 16; ++q) {
+      ev[q] = q < C && (uint32_t)tid < sc[kScOff + q + 1] - sc[kScOff + q];
+      e[q] = ev[q] ? __ldcg(glist + (int64_t)q * kRegion + tid) : make_uint2(0u, 0u);
     }
+    // few candidates spread over 1024 bins: plain shared-memory atomics rarely collide
 #pragma unroll
-    for (int g = 0; g < kGather; ++g) {
-      const uint32_t j = (uint32_t)(tid + g * kThreads);
-      hist_add(h1, j < total ? (e[g].x >> 10) & (kLevelBins - 1) : kNoBin);
-    }
+    for (int q = 0; q < 16; ++q)
+      if (ev[q]) atomicAdd(&h1[(e[q].x >> 10) & (kLevelBins - 1)], 1u);
     __syncthreads();
-    uint32_t c2[2] = {h1[2 * tid], h1[2 * tid + 1]};
-    const uint32_t d1 = find_digit<2>(c2, kr, sc, &above);
+    uint32_t c1[kBins1];
+#pragma unroll
+    for (int k = 0; k < kBins1; ++k) c1[k] = h1[kBins1 * tid + k];
+    const uint32_t d1 = find_digit<kBins1>(c1, kr, sc, &above);
     kr -= above;
     const uint32_t p22 = (b0 << 10) | d1;
 #pragma unroll
-    for (int g = 0; g < kGather; ++g) {
-      const uint32_t j = (uint32_t)(tid + g * kThreads);
-      const bool m = j < total && (e[g].x >> 10) == p22;
-      hist_add(h2, m ? e[g].x & (kLevelBins - 1) : kNoBin);
-    }
+    for (int q = 0; q < 16; ++q)
+      if (ev[q] && (e[q].x >> 10) == p22) atomicAdd(&h2[e[q].x & (kLevelBins - 1)], 1u);
     __syncthreads();
-    c2[0] = h2[2 * tid];
-    c2[1] = h2[2 * tid + 1];
-    const uint32_t d2 = find_digit<2>(c2, kr, sc, &above);
+#pragma unroll
+    for (int k = 0; k < kBins1; ++k) c1[k] = h2[kBins1 * tid + k];
+    const uint32_t d2 = find_digit<kBins1>(c1, kr, sc, &above);
     kr -= above;
     T = (p22 << 10) | d2;
     uint32_t g_ = 0, q_ = 0;
 #pragma unroll
-    for (int g = 0; g < kGather; ++g) {
-      const uint32_t j = (uint32_t)(tid + g * kThreads);
-      const bool m = j < total && e[g].y < (uint32_t)lo;
-      g_ += m && e[g].x > T;
-      q_ += m && e[g].x == T;
+    for (int q = 0; q < 16; ++q) {
+      const bool m = ev[q] && q < r;  // lists of the CTAs before this one
+      g_ += m && e[q].x > T;
+      q_ += m && e[q].x == T;
     }
     bf = ((uint64_t)g_ << 48) | ((uint64_t)q_ << 32);
   } else {
@@ -435,9 +459,9 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkParams
       __syncthreads();
       flush_bins(h, gh, kLevelBins);
       cluster_sync();  // every CTA's level counts are in gh
-      uint32_t c2[2];
-      load_bins<2>(gh, c2);
-      const uint32_t d = find_digit<2>(c2, kr, sc, &above);
+      uint32_t c1[kBins1];
+      load_bins<kBins1>(gh, c1);
+      const uint32_t d = find_digit<kBins1>(c1, kr, sc, &above);
       kr -= above;
       prefix = (prefix << 10) | d;
       pbits += 10;
@@ -473,14 +497,14 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkParams
       const uint2 v = tid < r ? dsmem_ld_u2(dsmem_addr(pub + 2, (uint32_t)tid)) : make_uint2(0u, 0u);
       const uint32_t x = __reduce_add_sync(0xffffffffu, v.x), y = __reduce_add_sync(0xffffffffu, v.y);
       if (tid == 0) {
-        sc[98] = x;
-        sc[99] = y;
+        sc[kScGt] = x;
+        sc[kScEq] = y;
       }
     }
     __syncthreads();
     cluster_arrive();  // this CTA's reads of the others' shared memory are done
-    gt_before = sc[98];
-    eq_before = sc[99];
+    gt_before = sc[kScGt];
+    eq_before = sc[kScEq];
   }
 
   // ---- output, ascending positions: slot = (keys > T before) + min(keys == T before, kr).
@@ -512,6 +536,7 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkParams
       if (is_gt || (is_eq && eb < kr)) {
         const uint32_t slot = gb + min(eb, kr);
         if (slot < (uint32_t)p.K) out[slot] = lo + i + j;
+        if (pf_kv) prefetch_row((uint32_t)(lo + i + j));
       }
       gb += is_gt;
       eb += is_eq;
@@ -528,11 +553,11 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkParams
       reinterpret_cast<uint4*>(gh1)[i] = make_uint4(0u, 0u, 0u, 0u);  // gh1 and gh2 are adjacent
 }
 
-// About 2048 keys per CTA, at most 16 CTAs per cluster; at most 8 when more clusters are needed
+// About kChunk keys per CTA, at most 16 CTAs per cluster; at most 8 when more clusters are needed
 // than 16-CTA clusters can run at once.
 int cluster_ctas(int n_max, int T, size_t smem16) {
   int c = 1;
-  while (c < 16 && (int64_t)c * 2048 < n_max) c <<= 1;
+  while (c < 16 && (int64_t)c * kChunk < n_max) c <<= 1;
   if (c == 16) {
     static std::mutex mu;
     static size_t cached_smem = 0;
@@ -572,7 +597,7 @@ int cluster_ctas(int n_max, int T, size_t smem16) {
 // Largest cluster a row of n_max positions can use (the launch may use fewer).
 int cluster_ctas_max(int n_max) {
   int c = 1;
-  while (c < 16 && (int64_t)c * 2048 < n_max) c <<= 1;
+  while (c < 16 && (int64_t)c * kChunk < n_max) c <<= 1;
   return c;
 }
 
