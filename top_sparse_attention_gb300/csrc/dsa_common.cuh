@@ -180,6 +180,19 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
 // TMEM -> registers: 32 lanes x W consecutive 32-bit columns (W = 16 or 32); thread i of the
 // warp receives lane (base + i).  The load and its completion wait are one asm statement so the
 // compiler cannot use the destination registers before the data has arrived.
+__device__ __forceinline__ void tmem_ld_sync(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_ld_sync(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
   asm volatile(

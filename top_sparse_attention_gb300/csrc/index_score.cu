@@ -10,8 +10,9 @@
 // lane = one position and all of its head columns, so ReLU, the head weights and (for MXFP8) the
 // per-group E8M0 scales are applied in registers with no cross-thread reduction.
 //
-// Warp roles (192 threads): warp 0 = producer (TMA for A and B), warp 1 = TMEM
-// owner and MMA issuer, warps 2-5 = epilogue.  A ring of shared-memory stages decouples loads
+// Warp roles: warp 0 = producer (TMA for A and B), warp 1 = TMEM owner and MMA issuer, warps
+// 2-5 = epilogue (bf16); MXFP8 with N >= 32 uses 8 epilogue warps in two groups that split the
+// head columns of every tile, group 1 handing its partial scores to group 0 through shared memory.  A ring of shared-memory stages decouples loads
 // from MMAs; two TMEM accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
 // The grid is persistent: CTA c processes a contiguous range of (query group, tile) units.
 //
@@ -32,7 +33,6 @@ namespace dsa {
 namespace {
 
 constexpr int kTileM = 128;
-constexpr int kThreads = 192;
 constexpr int kSmemBudget = 225 * 1024;
 
 constexpr int pow2_at_least(int x) {
@@ -56,7 +56,13 @@ struct Cfg {
   static constexpr int ACC_COLS = GROUPS * N;
   static constexpr int TMEM_COLS = pow2_at_least(2 * ACC_COLS);
   static constexpr int HIST_BYTES = G == 1 ? kHistBins * 4 : 0;  // fused score histogram
-  static constexpr int AUX_BYTES = 1024 + 4096 + G * NPAD * 4 + G * NPAD * GROUPS * 4 + HIST_BYTES;
+  // MXFP8 epilogues do four times the work per tile: two warp groups split the head columns
+  static constexpr int EPI = MX && N >= 32 ? 8 : 4;  // epilogue warps
+  static constexpr int SPLITS = EPI / 4;      // column splits (each warp group covers all rows)
+  static constexpr int THREADS = 64 + 32 * EPI;
+  static constexpr int COLS = N / SPLITS;     // accumulator columns per epilogue warp
+  static constexpr int PART_BYTES = 2 * (SPLITS - 1) * kTileM * 4;  // partial scores of groups 1..
+  static constexpr int AUX_BYTES = 1024 + 4096 + G * NPAD * 4 + G * NPAD * GROUPS * 4 + HIST_BYTES + PART_BYTES;
   static constexpr int STAGES_FIT = (kSmemBudget - B_BUFS * B_BYTES - AUX_BYTES) / A_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int OFF_B = STAGES * A_BYTES;
@@ -64,14 +70,21 @@ struct Cfg {
   static constexpr int OFF_W = OFF_BAR + 1024;
   static constexpr int OFF_QS = OFF_W + G * NPAD * 4;
   static constexpr int OFF_HIST = OFF_QS + G * NPAD * GROUPS * 4;
-  static constexpr int SMEM = OFF_HIST + HIST_BYTES + 1024;  // + alignment slack
+  static constexpr int OFF_PART = OFF_HIST + HIST_BYTES;
+  static constexpr int SMEM = OFF_PART + PART_BYTES + 1024;  // + alignment slack
   static_assert(N % 16 == 0 && N >= 16 && N <= 256, "MMA N out of range");
   static_assert(2 * ACC_COLS <= 512, "accumulators exceed tensor memory");
   static_assert(STAGES >= 2, "not enough shared memory for the pipeline");
   static_assert(ROW_BYTES % 128 == 0, "rows must fill whole swizzle atoms");
+  static_assert(SPLITS == 1 || G == 1, "split columns only for one query per group");
+  static_assert(COLS >= 8, "at least one 8-column TMEM load per warp");
 };
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// named barriers of the epilogue warps (ids 1 and 2; 0 is __syncthreads)
+template <int THREADS>
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory"); }
+template <int THREADS>
+__device__ __forceinline__ void part_bar() { asm volatile("bar.sync 2, %0;" ::"n"(THREADS) : "memory"); }
 
 // E8M0 byte -> 2^(e - 127) as an fp32 bit pattern (e = 0 is the subnormal 2^-127).
 __device__ __forceinline__ float e8m0_value(uint32_t e) {
@@ -99,7 +112,7 @@ __device__ __forceinline__ bool unit_of(const IndexScoreParams& p, int u, Unit& 
 }
 
 template <bool MX, int D, int G, int NPAD>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<MX, D, G, NPAD>::THREADS, 1)
 index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                    const uint8_t* __restrict__ q_idx, const int q_by_tma, const IndexScoreParams p) {
   using C = Cfg<MX, D, G, NPAD>;
@@ -136,7 +149,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
       mbar_init(&bfull[i], 1);
       mbar_init(&bempty[i], 1);
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 4);  // one arrival per epilogue warp
+      mbar_init(&tempty[i], C::EPI);  // one arrival per epilogue warp
     }
     fence_mbar_init();
     prefetch_tmap(&tm_k);
@@ -258,14 +271,17 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     }
   } else {
     // ------------------------------------------------------------------ epilogue
-    const int q4 = warp & 3;  // the TMEM lane quarter this warp may access
+    constexpr int ET = 32 * C::EPI;  // epilogue threads
+    const int q4 = warp & 3;         // the TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;  // which column split of the accumulator this warp reads
     const int row = q4 * 32 + lane;
     const int et = threadIdx.x - 64;
+    float* part_s = reinterpret_cast<float*>(smem + C::OFF_PART);  // [2][SPLITS - 1][kTileM]
     int ai = 0, cur_t0 = -1;
     bool ok = true;
     // flushes the shared histogram of query t into the global one (non-zero bins only)
     auto flush_hist = [&](int t) {
-      for (int b = et; b < kHistBins; b += 128) {
+      for (int b = et; b < kHistBins; b += ET) {
         const uint32_t v = hist_s[b];
         if (v) {
           atomicAdd(&p.hist[(int64_t)t * kHistBins + b], v);
@@ -274,20 +290,46 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
       }
     };
     if (build_hist)
-      for (int b = et; b < kHistBins; b += 128) hist_s[b] = 0;
+      for (int b = et; b < kHistBins; b += ET) hist_s[b] = 0;
+    // MXFP8: this row's key scales are loaded one unit ahead, so the global load overlaps the
+    // previous unit's epilogue instead of stalling the current one
+    auto load_ks = [&](const Unit& y) -> uint32_t {
+      uint32_t raw = 0;
+      const int pos = y.tile * kTileM + row;
+      if (pos < y.n_max) {
+        const int sq = (y.t0 + p.t_off) / p.q_per_seq;
+        const uint8_t* src = p.k_sf + (int64_t)sq * p.k_sf_seq_stride + (int64_t)pos * C::GROUPS;
+        if (C::GROUPS == 4) raw = __ldg(reinterpret_cast<const uint32_t*>(src));
+        else
+          for (int g = 0; g < C::GROUPS; ++g) raw |= (uint32_t)__ldg(src + g) << (8 * g);
+      }
+      return raw;
+    };
+    // the next visible unit after u (u_end when none)
+    auto next_unit = [&](int u, Unit& y) -> int {
+      for (++u; u < u_end; ++u)
+        if (unit_of<G>(p, u, y)) return u;
+      return u_end;
+    };
+    uint32_t raw_next = 0;
+    if (MX) {
+      Unit y;
+      const int u0 = next_unit(u_begin - 1, y);
+      if (u0 < u_end) raw_next = load_ks(y);
+    }
     // after a timed-out wait the epilogue warps keep walking the units (so that every named
-    // barrier below is reached by all 128 threads) but skip the waits and the tile work
+    // barrier below is reached by every epilogue thread) but skip the waits and the tile work
     for (int u = u_begin; u < u_end; ++u) {
       Unit x;
       if (!unit_of<G>(p, u, x)) continue;
       if (x.t0 != cur_t0) {
-        epi_bar();
+        epi_bar<ET>();
         if (build_hist && cur_t0 >= 0) {
           flush_hist(cur_t0);
-          epi_bar();
+          epi_bar<ET>();
         }
         cur_t0 = x.t0;
-        for (int i = et; i < G * NPAD; i += 128) {
+        for (int i = et; i < G * NPAD; i += ET) {
           const int j = i / NPAD, h = i % NPAD;
           const bool valid = h < p.H_idx && x.t0 + j < p.T;
           w_s[i] = valid ? p.w[(int64_t)(x.t0 + j) * p.H_idx + h] : 0.f;
@@ -298,70 +340,76 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                   valid ? e8m0_value(p.q_sf[((int64_t)(x.t0 + j) * p.H_idx + h) * C::GROUPS + g]) : 0.f;
           }
         }
-        epi_bar();
+        epi_bar<ET>();
       }
-      if (!ok) continue;
-      const int pos = x.tile * kTileM + row;
-      const int seq = (x.t0 + p.t_off) / p.q_per_seq;
       float ks[C::GROUPS];
       if (MX) {
-        uint32_t raw = 0;
-        if (pos < x.n_max) {
-          const uint8_t* src = p.k_sf + (int64_t)seq * p.k_sf_seq_stride + (int64_t)pos * C::GROUPS;
-          if (C::GROUPS == 4) raw = *reinterpret_cast<const uint32_t*>(src);
-          else
-            for (int g = 0; g < C::GROUPS; ++g) raw |= (uint32_t)src[g] << (8 * g);
-        }
+        const uint32_t raw = raw_next;  // this unit's scales
+        Unit y;
+        const int un = next_unit(u, y);
+        if (un < u_end) raw_next = load_ks(y);
 #pragma unroll
         for (int g = 0; g < C::GROUPS; ++g) ks[g] = e8m0_value((raw >> (8 * g)) & 0xFFu);
       }
+      const int pos = x.tile * kTileM + row;
       const int ab = ai & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&tfull[ab], (ai >> 1) & 1, p.err));
-      if (!ok) continue;
-      tc_fence_after();
-      const uint32_t tb = tmem + ((uint32_t)(q4 * 32) << 16) + ab * C::ACC_COLS;
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&tfull[ab], (ai >> 1) & 1, p.err));
       float score[G];
 #pragma unroll
       for (int j = 0; j < G; ++j) score[j] = 0.f;
-      constexpr int CW = C::N < 32 ? C::N : 32;  // columns per TMEM load
+      if (ok) {
+        tc_fence_after();
+        const uint32_t tb = tmem + ((uint32_t)(q4 * 32) << 16) + ab * C::ACC_COLS;
+        constexpr int CW = C::COLS < 32 ? C::COLS : 32;  // columns per TMEM load
 #pragma unroll
-      for (int c = 0; c < C::N / CW; ++c) {
-        const int j = (c * CW) / NPAD;  // query of the group these columns belong to
-        float v[CW];
-        if (!MX) {
-          tmem_ld_sync(tb + c * CW, v);
-        } else {
+        for (int c = 0; c < C::COLS / CW; ++c) {
+          const int col = half * C::COLS + c * CW;  // first accumulator column of this load
+          const int j = col / NPAD;                 // query of the group these columns belong to
+          float v[CW];
+          if (!MX) {
+            tmem_ld_sync(tb + col, v);
+          } else {
 #pragma unroll
-          for (int i = 0; i < CW; ++i) v[i] = 0.f;
+            for (int i = 0; i < CW; ++i) v[i] = 0.f;
 #pragma unroll
-          for (int g = 0; g < C::GROUPS; ++g) {
-            float d[CW];
-            tmem_ld_sync(tb + g * C::N + c * CW, d);
+            for (int g = 0; g < C::GROUPS; ++g) {
+              float d[CW];
+              tmem_ld_sync(tb + g * C::N + col, d);
 #pragma unroll
-            for (int i = 0; i < CW; ++i) v[i] = fmaf(ks[g] * qs_s[(c * CW + i) * C::GROUPS + g], d[i], v[i]);
+              for (int i = 0; i < CW; ++i) v[i] = fmaf(ks[g] * qs_s[(col + i) * C::GROUPS + g], d[i], v[i]);
+            }
           }
+#pragma unroll
+          for (int i = 0; i < CW; ++i) score[j] = fmaf(w_s[col + i], fmaxf(v[i], 0.f), score[j]);
         }
-#pragma unroll
-        for (int i = 0; i < CW; ++i) score[j] = fmaf(w_s[c * CW + i], fmaxf(v[i], 0.f), score[j]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[ab]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[ab]);
+      if constexpr (C::SPLITS > 1) {
+        // every epilogue thread meets this barrier once per unit, whatever happened to its waits
+        float* part = part_s + ab * (C::SPLITS - 1) * kTileM;
+        if (half > 0) part[(half - 1) * kTileM + row] = score[0];
+        part_bar<ET>();
+        if (half == 0)
 #pragma unroll
-      for (int j = 0; j < G; ++j) {
-        const int t = x.t0 + j;
-        const bool vis = t < p.T && pos < visible_len(t + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid);
-        if (vis) p.scores[(int64_t)t * p.ld_scores + pos] = score[j];
-        if (build_hist) {
-          const uint32_t bin = vis ? (float_key(score[j]) >> 20) : 0xFFFFFFFFu;
-          const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-          if (vis && lane == __ffs(peers) - 1) atomicAdd(&hist_s[bin], __popc(peers));
+          for (int k = 0; k < C::SPLITS - 1; ++k) score[0] += part[k * kTileM + row];
+      }
+      if (ok && half == 0) {
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          const int t = x.t0 + j;
+          const bool vis = t < p.T && pos < visible_len(t + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid);
+          if (vis) p.scores[(int64_t)t * p.ld_scores + pos] = score[j];
+          // shared-memory atomics: lanes on the same bin serialise in the atomic unit, which costs
+          // far less than grouping them first with a warp match
+          if (build_hist && vis) atomicAdd(&hist_s[float_key(score[j]) >> 20], 1u);
         }
       }
       ++ai;
     }
     if (build_hist && cur_t0 >= 0) {
-      epi_bar();
+      epi_bar<ET>();
       flush_hist(cur_t0);
     }
   }
@@ -409,7 +457,7 @@ cudaError_t launch_cfg(const void* q_idx, const void* k_idx, int64_t k_seq_strid
   if (units >= (1ll << 31)) return cudaErrorNotSupported;
   const int grid = (int)(units < sms ? units : sms);
   if (grid <= 0) return cudaSuccess;
-  return launch_kernel(kern, dim3(grid), dim3(kThreads), C::SMEM, stream, pdl, tm, tq,
+  return launch_kernel(kern, dim3(grid), dim3(C::THREADS), C::SMEM, stream, pdl, tm, tq,
                        reinterpret_cast<const uint8_t*>(q_idx), q_by_tma, p);
 }
 
