@@ -347,7 +347,14 @@ def run_ours(args, wl):
     err = dsa.dsa_get_device_error(stream)
     queries = wl.T * world
     value = queries / (ms * 1e-3)
-    launches_per_step = 3 * (-(-wl.T // slice_queries(wl)))  # index score, Top-K, attention
+    # per slice: index score, Top-K, attention, and the combine kernel when K is split (the
+    # attention needs a partials workspace exactly then)
+    from top_sparse_attention_gb300 import _native
+
+    tc = slice_queries(wl)
+    n_slices = -(-wl.T // tc)
+    split = _native.lib.dsa_sparse_attn_workspace_size(tc, wl.H, wl.K, wl.D_v) > 0
+    launches_per_step = (3 + int(split)) * n_slices
 
     # ---- per-kernel durations (component entry points, same kernels and launch shapes), events
     # on the launching stream over `reps` launches each
