@@ -13,7 +13,7 @@
 // Warp roles: warp 0 = producer (TMA for A and B), warp 1 = TMEM owner and MMA issuer, warps
 // 2-5 = epilogue (bf16); MXFP8 with N >= 32 uses 8 epilogue warps in two groups that split the
 // head columns of every tile, group 1 handing its partial scores to group 0 through shared memory.  A ring of shared-memory stages decouples loads
-// from MMAs; two TMEM accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
+// from MMAs; up to four TMEM accumulators let the epilogue trail the MMAs by several tiles.
 // The grid is persistent: CTA c processes a contiguous range of (query group, tile) units.
 //
 // For the Top-K step, the epilogue also builds a histogram of the top 12 bits of each score's
@@ -54,7 +54,10 @@ struct Cfg {
   static constexpr int B_BUFS = (2 * B_BYTES <= 64 * 1024) ? 2 : 1;
   static constexpr int GROUPS = MX ? D / 32 : 1;  // accumulators per tile
   static constexpr int ACC_COLS = GROUPS * N;
-  static constexpr int TMEM_COLS = pow2_at_least(2 * ACC_COLS);
+  // accumulators in flight between the MMA warp and the epilogue: as many as fit in 512 columns,
+  // up to 4 (two were not enough to hide MMA completion + epilogue latency per tile)
+  static constexpr int ACC_BUFS = 512 / ACC_COLS >= 4 ? 4 : 2;
+  static constexpr int TMEM_COLS = pow2_at_least(ACC_BUFS * ACC_COLS);
   static constexpr int HIST_BYTES = G == 1 ? kHistBins * 4 : 0;  // fused score histogram
   // MXFP8 epilogues do four times the work per tile: two warp groups split the head columns
   static constexpr int EPI = MX && N >= 32 ? 8 : 4;  // epilogue warps
@@ -73,7 +76,7 @@ struct Cfg {
   static constexpr int OFF_PART = OFF_HIST + HIST_BYTES;
   static constexpr int SMEM = OFF_PART + PART_BYTES + 1024;  // + alignment slack
   static_assert(N % 16 == 0 && N >= 16 && N <= 256, "MMA N out of range");
-  static_assert(2 * ACC_COLS <= 512, "accumulators exceed tensor memory");
+  static_assert(ACC_BUFS * ACC_COLS <= 512, "accumulators exceed tensor memory");
   static_assert(STAGES >= 2, "not enough shared memory for the pipeline");
   static_assert(ROW_BYTES % 128 == 0, "rows must fill whole swizzle atoms");
   static_assert(SPLITS == 1 || G == 1, "split columns only for one query per group");
@@ -126,8 +129,8 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
   uint64_t* bfull = empty + C::STAGES;
   uint64_t* bempty = bfull + 2;
   uint64_t* tfull = bempty + 2;
-  uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* tempty = tfull + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 4);
   float* w_s = reinterpret_cast<float*>(smem + C::OFF_W);    // [G][NPAD]
   float* qs_s = reinterpret_cast<float*>(smem + C::OFF_QS);  // [G][NPAD][GROUPS]
   uint32_t* hist_s = reinterpret_cast<uint32_t*>(smem + C::OFF_HIST);  // G == 1 only
@@ -148,6 +151,8 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bfull[i], 1);
       mbar_init(&bempty[i], 1);
+    }
+    for (int i = 0; i < C::ACC_BUFS; ++i) {
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], C::EPI);  // one arrival per epilogue warp
     }
@@ -244,8 +249,9 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
       }
       const int s = it % C::STAGES;
       ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (it / C::STAGES) & 1, p.err));
-      const int ab = ai & 1;
-      if (ok && ai >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&tempty[ab], ((ai - 2) >> 1) & 1, p.err));
+      const int ab = ai % C::ACC_BUFS;
+      if (ok && ai >= C::ACC_BUFS)
+        ok = __all_sync(0xffffffffu, mbar_wait(&tempty[ab], ((ai - C::ACC_BUFS) / C::ACC_BUFS) & 1, p.err));
       if (!ok) break;
       tc_fence_after();
       if (lane == 0) {
@@ -352,8 +358,8 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         for (int g = 0; g < C::GROUPS; ++g) ks[g] = e8m0_value((raw >> (8 * g)) & 0xFFu);
       }
       const int pos = x.tile * kTileM + row;
-      const int ab = ai & 1;
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&tfull[ab], (ai >> 1) & 1, p.err));
+      const int ab = ai % C::ACC_BUFS;
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&tfull[ab], (ai / C::ACC_BUFS) & 1, p.err));
       float score[G];
 #pragma unroll
       for (int j = 0; j < G; ++j) score[j] = 0.f;
@@ -388,7 +394,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
       }
       if constexpr (C::SPLITS > 1) {
         // every epilogue thread meets this barrier once per unit, whatever happened to its waits
-        float* part = part_s + ab * (C::SPLITS - 1) * kTileM;
+        float* part = part_s + (ai & 1) * (C::SPLITS - 1) * kTileM;  // alternates per unit
         if (half > 0) part[(half - 1) * kTileM + row] = score[0];
         part_bar<ET>();
         if (half == 0)
