@@ -392,18 +392,24 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkParams
     cluster_arrive();  // this CTA's reads of the others' shared memory are done
     // ---- few candidates: every CTA's list, levels 1 and 2 resolved here
     // entry tid of every CTA's list (a list holds at most kRegion = kThreads entries):
-    // coalesced loads, no search for the owner
+    // coalesced loads, no search for the owner.  Threads past the longest list hold nothing.
+    const bool holds = (uint32_t)tid < sc[kScMax];
+    uint32_t vm = 0;  // bit q: this thread holds entry tid of CTA q's list
     uint2 e[16];
-    bool ev[16];
 #pragma unroll
     for (int q = 0; q < 16; ++q) {
-      ev[q] = q < C && (uint32_t)tid < sc[kScOff + q + 1] - sc[kScOff + q];
-      e[q] = ev[q] ? __ldcg(glist + (int64_t)q * kRegion + tid) : make_uint2(0u, 0u);
+      if (q >= C || !holds) break;
+      if ((uint32_t)tid < sc[kScOff + q + 1] - sc[kScOff + q]) {
+        vm |= 1u << q;
+        e[q] = __ldcg(glist + (int64_t)q * kRegion + tid);
+      }
     }
     // few candidates spread over 1024 bins: plain shared-memory atomics rarely collide
 #pragma unroll
-    for (int q = 0; q < 16; ++q)
-      if (ev[q]) atomicAdd(&h1[(e[q].x >> 10) & (kLevelBins - 1)], 1u);
+    for (int q = 0; q < 16; ++q) {
+      if (!(vm >> q)) break;
+      if ((vm >> q) & 1u) atomicAdd(&h1[(e[q].x >> 10) & (kLevelBins - 1)], 1u);
+    }
     __syncthreads();
     uint32_t c1[kBins1];
 #pragma unroll
@@ -412,8 +418,10 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkParams
     kr -= above;
     const uint32_t p22 = (b0 << 10) | d1;
 #pragma unroll
-    for (int q = 0; q < 16; ++q)
-      if (ev[q] && (e[q].x >> 10) == p22) atomicAdd(&h2[e[q].x & (kLevelBins - 1)], 1u);
+    for (int q = 0; q < 16; ++q) {
+      if (!(vm >> q)) break;
+      if (((vm >> q) & 1u) && (e[q].x >> 10) == p22) atomicAdd(&h2[e[q].x & (kLevelBins - 1)], 1u);
+    }
     __syncthreads();
 #pragma unroll
     for (int k = 0; k < kBins1; ++k) c1[k] = h2[kBins1 * tid + k];
@@ -421,9 +429,11 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkParams
     kr -= above;
     T = (p22 << 10) | d2;
     uint32_t g_ = 0, q_ = 0;
+    const uint32_t before_mask = vm & ((1u << r) - 1u);  // lists of the CTAs before this one
 #pragma unroll
     for (int q = 0; q < 16; ++q) {
-      const bool m = ev[q] && q < r;  // lists of the CTAs before this one
+      if (!(before_mask >> q)) break;
+      const bool m = (before_mask >> q) & 1u;
       g_ += m && e[q].x > T;
       q_ += m && e[q].x == T;
     }
