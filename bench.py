@@ -296,6 +296,8 @@ def run_ours(args, wl):
     n_sets = max(3, min(8, -(-3 * L2_BYTES // max(per_step, 1))))
     if args.sets:
         n_sets = args.sets
+    inflight = max(1, args.inflight)
+    n_sets = -(-n_sets // inflight) * inflight  # set j always runs on stream j % inflight
     cpu_sets = [synth.make_inputs(wl, seed_offset=rank_seed_offset(rank, i)) for i in range(n_sets)]
     dev_sets = [{k: (v.to(dev) if v is not None else None) for k, v in s.items()} for s in cpu_sets]
     calls = [dsa.call_from_tensors(s, K=wl.K, sm_scale=wl.sm_scale, q_per_seq=wl.q_per_seq,
@@ -332,18 +334,43 @@ def run_ours(args, wl):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
+    # with inflight > 1, consecutive steps (independent batches) go to different streams so that
+    # one batch's selection and attention overlap the next batch's scoring
+    streams = [stream] + [torch.cuda.Stream(device=dev) for _ in range(inflight - 1)]
     with ClockSampler(dev.index) as clocks:
+        ev0.record(stream)
+        for st in streams[1:]:
+            st.wait_event(ev0)
+        for i in range(args.steps):
+            st = streams[i % inflight]
+            with torch.cuda.stream(st):
+                if graphs is not None:
+                    graphs[i % n_sets].replay()
+                else:
+                    calls[i % n_sets](st)
+        for st in streams[1:]:
+            stream.wait_stream(st)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world, dev)
+    # the same steps one batch at a time (one stream), reported beside the headline
+    serial = None
+    if inflight > 1:
+        n_serial = min(args.steps, 5000)
+        torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             ev0.record(stream)
-            for i in range(args.steps):
+            for i in range(n_serial):
                 if graphs is not None:
                     graphs[i % n_sets].replay()
                 else:
                     calls[i % n_sets](stream)
             ev1.record(stream)
         torch.cuda.synchronize()
-    barrier()
-    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world, dev)
+        ms_serial = max_over_ranks(ev0.elapsed_time(ev1) / n_serial, world, dev)
+        serial = {"value": wl.T * world / (ms_serial * 1e-3), "unit": "queries/s",
+                  "ms_per_step": ms_serial, "steps": n_serial, "batches_in_flight": 1}
     err = dsa.dsa_get_device_error(stream)
     queries = wl.T * world
     value = queries / (ms * 1e-3)
@@ -375,7 +402,8 @@ def run_ours(args, wl):
                     "algorithmic_flops": flops, "traffic": profiled_traffic(wl.name)}
 
     # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
-    e2e = end_to_end(dsa, wl, cpu_sets, dev_sets, stream, steps=max(10, min(args.steps, 1000)))
+    e2e = end_to_end(dsa, wl, cpu_sets, dev_sets, stream, steps=max(10, min(args.steps, 5000)),
+                     inflight=inflight)
 
     line = None
     if rank == 0:
@@ -394,11 +422,13 @@ def run_ours(args, wl):
             "config": {"workload": wl.name, "batch": wl.T, "L": wl.L, "K": wl.K, "H_idx": wl.H_idx,
                        "d_idx": wl.d_idx, "idx_dtype": wl.idx_dtype, "H": wl.H, "D_qk": wl.D_qk,
                        "D_v": wl.D_v, "kv_dtype": wl.kv_dtype, "cuda_graph": graphs is not None,
+                       "batches_in_flight": inflight,
                        "l2": f"rotating {n_sets} input sets, {n_sets * per_step / 1e6:.0f} MB compulsory bytes > 129 MB L2"},
             "hbm_gbs": chain_gbs, "hbm_frac_of_8tbs": chain_gbs / NOMINAL_HBM_GBS,
             "hbm_frac_of_measured": chain_gbs / peak,
             "roofline": roofline,
             "kernels_us": kern,
+            "serial": serial,
             "cpu_baseline": cpu_base,
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
@@ -482,14 +512,16 @@ def kernel_times(dsa, wl, dev_sets, stream, reps):
     return out
 
 
-def end_to_end(dsa, wl, cpu_sets, dev_sets, stream, steps):
+def end_to_end(dsa, wl, cpu_sets, dev_sets, stream, steps, inflight=1):
     """queries/s through the C ABI with each step's query-side inputs (q, q_idx (+scales), w)
     copied from pinned host memory and its outputs (out, lse) read back, inside the timed region.
     The caches are device-resident state, as in decode, rotating over the same input sets as the
     device timing (their bytes exceed L2).  Inputs sit in one pinned host buffer and one device
-    buffer, outputs likewise, so a step is one host-to-device copy, the fused call (a CUDA graph
-    of dsa_decode per input set) and one device-to-host copy; the copies run on their own streams
-    so that adjacent steps' copies overlap the call, as a serving loop would run them."""
+    buffer, outputs likewise, so a step is one host-to-device copy, the fused call (dsa_decode)
+    and one device-to-host copy.  The copies run on their own streams so that neighbouring steps'
+    copies overlap the calls, as a serving loop would run them; with inflight > 1 consecutive
+    steps' calls run on different streams, as in the device timing.  One CUDA graph replays a
+    period of one step per input set, so the host launches once per period."""
     keys_in = [k for k in ("q", "q_idx", "q_idx_sf", "w") if cpu_sets[0][k] is not None]
 
     def packed(tensors, device, pinned):
@@ -524,63 +556,65 @@ def end_to_end(dsa, wl, cpu_sets, dev_sets, stream, steps):
             for _ in range(2):
                 call(stream)
         torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            call(stream)
-        sets.append((hin, din, hout, dout, g, call))  # the call owns the workspace the graph uses
+        sets.append((hin, din, hout, dout, None, call))  # the call owns its workspace
     h2d, d2h = sets[0][0].numel(), sets[0][2].numel()
     n = len(sets)
     # three streams: copies in, the fused call, copies out; events keep each set's buffers from
     # being overwritten before their readers are done, so step i+1's input copy and step i-1's
     # output copy overlap step i's call
+    # One CUDA graph holds a period of n steps (one per input set): each step's input copy on a
+    # copy stream, its call on compute stream j % inflight, its output copy on a third stream,
+    # ordered by events, so copies and calls of neighbouring steps overlap without host gaps.
     s_in, s_out = torch.cuda.Stream(device=dev0), torch.cuda.Stream(device=dev0)
+    comp = [torch.cuda.Stream(device=dev0) for _ in range(inflight)]
     ev_in = [torch.cuda.Event() for _ in range(n)]
     ev_done = [torch.cuda.Event() for _ in range(n)]
-    ev_out = [torch.cuda.Event() for _ in range(n)]
-    started = [False] * n
-
-    def step(i):
-        j = i % n
-        hin, din, hout, dout, g, _ = sets[j]
-        if started[j]:
-            s_in.wait_event(ev_done[j])   # the previous call on this set has read its inputs
-            stream.wait_event(ev_out[j])  # and its outputs have been copied out
-        with torch.cuda.stream(s_in):
-            din.copy_(hin, non_blocking=True)
-            ev_in[j].record(s_in)
-        stream.wait_event(ev_in[j])
-        with torch.cuda.stream(stream):
-            g.replay()
-            ev_done[j].record(stream)
-        s_out.wait_event(ev_done[j])
-        with torch.cuda.stream(s_out):
-            hout.copy_(dout, non_blocking=True)
-            ev_out[j].record(s_out)
-        started[j] = True
-
-    for i in range(3):
-        step(i)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s_in)
-    stream.wait_event(e0)
-    for i in range(steps):
-        step(i)
-    s_in.wait_stream(stream)
-    s_in.wait_stream(s_out)
-    e1.record(s_in)
-    torch.cuda.synchronize()
+    period = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(period, stream=stream):
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        for st in [s_in, s_out] + comp:
+            st.wait_event(fork)
+        for j in range(n):
+            hin, din, hout, dout, _, call = sets[j]
+            sc = comp[j % inflight]
+            with torch.cuda.stream(s_in):
+                din.copy_(hin, non_blocking=True)
+                ev_in[j].record(s_in)
+            sc.wait_event(ev_in[j])
+            call(sc)
+            ev_done[j].record(sc)
+            s_out.wait_event(ev_done[j])
+            with torch.cuda.stream(s_out):
+                hout.copy_(dout, non_blocking=True)
+        for st in [s_in, s_out] + comp:
+            stream.wait_stream(st)
+    periods = max(1, -(-steps // n))
+    steps = periods * n
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            period.replay()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(periods):
+            period.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     ms = max(e0.elapsed_time(e1), wall * 1e3) / steps
     return {"value": wl.T / (ms * 1e-3), "unit": "queries/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms,
-            "copies_per_step": {"h2d": 1, "d2h": 1}, "pipelined": "copies of adjacent steps overlap the call"}
+            "copies_per_step": {"h2d": 1, "d2h": 1}, "batches_in_flight": inflight,
+            "pipelined": "copies of adjacent steps overlap the calls"}
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--inflight", type=int, default=3,
+                    help="independent batches in flight (consecutive steps on different streams)")
     ap.add_argument("--steps", type=int, default=20000)  # ~1 s of decode steps: clock samples
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
