@@ -176,6 +176,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
+    const uint64_t evict_first = l2_evict_first_policy();  // key tiles are read once
     int it = 0, qn = -1, cur_t0 = -1;
     bool ok = true;
     for (int u = u_begin; u < u_end && ok; ++u) {
@@ -226,8 +227,8 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         const int seq = (x.t0 + p.t_off) / p.q_per_seq;
 #pragma unroll
         for (int b = 0; b < C::BOXES; ++b)
-          tma_load_3d(a_s + s * C::A_BYTES + b * (kTileM * 128), &tm_k, &full[s], b * C::BOX_COLS,
-                      x.tile * kTileM, seq);
+          tma_load_3d_hint(a_s + s * C::A_BYTES + b * (kTileM * 128), &tm_k, &full[s], b * C::BOX_COLS,
+                           x.tile * kTileM, seq, evict_first);
       }
       __syncwarp();
       ++it;
