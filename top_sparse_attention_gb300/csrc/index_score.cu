@@ -11,8 +11,10 @@
 // per-group E8M0 scales are applied in registers with no cross-thread reduction.
 //
 // Warp roles: warp 0 = producer (TMA for A and B), warp 1 = TMEM owner and MMA issuer, warps
-// 2-5 = epilogue (bf16); MXFP8 with N >= 32 uses 8 epilogue warps in two groups that split the
-// head columns of every tile, group 1 handing its partial scores to group 0 through shared memory.  A ring of shared-memory stages decouples loads
+// 2-5 = epilogue.  Heavy epilogues (MXFP8 with N >= 32, four queries per tile) use 8 epilogue
+// warps in two groups that split the accumulator columns: by query (each group scores its own
+// queries) or, for one query, by head (group 1 hands its partial scores to group 0 through
+// shared memory).  A ring of shared-memory stages decouples loads
 // from MMAs; up to four TMEM accumulators let the epilogue trail the MMAs by several tiles.
 // The grid is persistent: CTA c processes a contiguous range of (query group, tile) units.
 //
@@ -60,11 +62,16 @@ struct Cfg {
   static constexpr int TMEM_COLS = pow2_at_least(ACC_BUFS * ACC_COLS);
   static constexpr int HIST_BYTES = G == 1 ? kHistBins * 4 : 0;  // fused score histogram
   // MXFP8 epilogues do four times the work per tile: two warp groups split the head columns
-  static constexpr int EPI = MX && N >= 32 ? 8 : 4;  // epilogue warps
+  // epilogue warps: eight (two groups splitting the accumulator columns) where a tile's epilogue
+  // is heavy: MXFP8 (four scale groups) and four queries per tile (N = 256)
+  static constexpr int EPI = (MX && N >= 32) || G == 4 ? 8 : 4;
   static constexpr int SPLITS = EPI / 4;      // column splits (each warp group covers all rows)
   static constexpr int THREADS = 64 + 32 * EPI;
   static constexpr int COLS = N / SPLITS;     // accumulator columns per epilogue warp
-  static constexpr int PART_BYTES = 2 * (SPLITS - 1) * kTileM * 4;  // partial scores of groups 1..
+  // the split falls between queries (each group scores its own queries) or between heads of one
+  // query (groups 1.. hand partial scores to group 0)
+  static constexpr bool QSPLIT = COLS % NPAD == 0;
+  static constexpr int PART_BYTES = QSPLIT ? 0 : 2 * (SPLITS - 1) * kTileM * 4;
   static constexpr int AUX_BYTES = 1024 + 4096 + G * NPAD * 4 + G * NPAD * GROUPS * 4 + HIST_BYTES + PART_BYTES;
   static constexpr int STAGES_FIT = (kSmemBudget - B_BUFS * B_BYTES - AUX_BYTES) / A_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
@@ -79,7 +86,7 @@ struct Cfg {
   static_assert(ACC_BUFS * ACC_COLS <= 512, "accumulators exceed tensor memory");
   static_assert(STAGES >= 2, "not enough shared memory for the pipeline");
   static_assert(ROW_BYTES % 128 == 0, "rows must fill whole swizzle atoms");
-  static_assert(SPLITS == 1 || G == 1, "split columns only for one query per group");
+  static_assert(QSPLIT || G == 1, "a head split needs one query per group");
   static_assert(COLS >= 8, "at least one 8-column TMEM load per warp");
 };
 
@@ -361,9 +368,12 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
       const int pos = x.tile * kTileM + row;
       const int ab = ai % C::ACC_BUFS;
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&tfull[ab], (ai / C::ACC_BUFS) & 1, p.err));
-      float score[G];
+      // the queries this warp scores: its own group's with a query split, all G otherwise
+      constexpr int QW = C::QSPLIT ? C::COLS / NPAD : G;
+      const int j0 = C::QSPLIT ? half * QW : 0;
+      float score[QW];
 #pragma unroll
-      for (int j = 0; j < G; ++j) score[j] = 0.f;
+      for (int j = 0; j < QW; ++j) score[j] = 0.f;
       if (ok) {
         tc_fence_after();
         const uint32_t tb = tmem + ((uint32_t)(q4 * 32) << 16) + ab * C::ACC_COLS;
@@ -371,7 +381,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 #pragma unroll
         for (int c = 0; c < C::COLS / CW; ++c) {
           const int col = half * C::COLS + c * CW;  // first accumulator column of this load
-          const int j = col / NPAD;                 // query of the group these columns belong to
+          const int j = (c * CW) / NPAD;            // this warp's query the columns belong to
           float v[CW];
           if (!MX) {
             tmem_ld_sync(tb + col, v);
@@ -393,7 +403,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[ab]);
       }
-      if constexpr (C::SPLITS > 1) {
+      if constexpr (!C::QSPLIT) {
         // every epilogue thread meets this barrier once per unit, whatever happened to its waits
         float* part = part_s + (ai & 1) * (C::SPLITS - 1) * kTileM;  // alternates per unit
         if (half > 0) part[(half - 1) * kTileM + row] = score[0];
@@ -402,10 +412,11 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 #pragma unroll
           for (int k = 0; k < C::SPLITS - 1; ++k) score[0] += part[k * kTileM + row];
       }
-      if (ok && half == 0) {
+      // stores: each group its own queries with a query split, group 0 all of them otherwise
+      if (ok && (C::QSPLIT || half == 0)) {
 #pragma unroll
-        for (int j = 0; j < G; ++j) {
-          const int t = x.t0 + j;
+        for (int j = 0; j < QW; ++j) {
+          const int t = x.t0 + j0 + j;
           const bool vis = t < p.T && pos < visible_len(t + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid);
           if (vis) p.scores[(int64_t)t * p.ld_scores + pos] = score[j];
           // shared-memory atomics: lanes on the same bin serialise in the atomic unit, which costs
