@@ -64,7 +64,7 @@ struct Cfg {
   // MXFP8 epilogues do four times the work per tile: two warp groups split the head columns
   // epilogue warps: eight (two groups splitting the accumulator columns) where a tile's epilogue
   // is heavy: MXFP8 (four scale groups) and four queries per tile (N = 256)
-  static constexpr int EPI = (MX && N >= 32) || G == 4 ? 8 : 4;
+  static constexpr int EPI = G == 4 ? 16 : ((MX && N >= 32) ? 8 : 4);
   static constexpr int SPLITS = EPI / 4;      // column splits (each warp group covers all rows)
   static constexpr int THREADS = 64 + 32 * EPI;
   static constexpr int COLS = N / SPLITS;     // accumulator columns per epilogue warp
