@@ -374,14 +374,9 @@ def run_ours(args, wl):
     err = dsa.dsa_get_device_error(stream)
     queries = wl.T * world
     value = queries / (ms * 1e-3)
-    # per slice: index score, Top-K, attention, and the combine kernel when K is split (the
-    # attention needs a partials workspace exactly then)
-    from top_sparse_attention_gb300 import _native
-
-    tc = slice_queries(wl)
-    n_slices = -(-wl.T // tc)
-    split = _native.lib.dsa_sparse_attn_workspace_size(tc, wl.H, wl.K, wl.D_v) > 0
-    launches_per_step = (3 + int(split)) * n_slices
+    # kernels per step as the library plans them (index score, Top-K kernels, attention and the
+    # combine kernel when K is split over CTAs, per slice of queries)
+    launches_per_step = calls[0].launches
 
     # ---- per-kernel durations (component entry points, same kernels and launch shapes), events
     # on the launching stream over `reps` launches each
@@ -441,15 +436,6 @@ def run_ours(args, wl):
 
         dist.destroy_process_group()
     return 0
-
-
-def slice_queries(wl):
-    """Queries per launch of the chain (prefill runs in slices whose fp32 scores fit 256 MB)."""
-    if wl.q_pos0 < 0:
-        return wl.T
-    ld = max(4, (wl.L + 3) // 4 * 4)
-    tc = max(4, (256 * 2 ** 20 // (ld * 4)) // 4 * 4)
-    return min(tc, wl.T)
 
 
 def kernel_times(dsa, wl, dev_sets, stream, reps):

@@ -58,6 +58,8 @@ typedef enum dsa_dtype {
 #define DSA_DEVERR_NONE 0
 #define DSA_DEVERR_INDEX_RANGE 1  /* an index outside [-1, L) reached the attention gather */
 #define DSA_DEVERR_WAIT_TIMEOUT 2 /* a bounded pipeline wait gave up */
+#define DSA_DEVERR_TOPK_COUNTS 3  /* a row-split Top-K slot fell outside [0, K): the row's
+                                     histogram disagreed with its scores; the write was skipped */
 
 /* Human-readable name of a status code.  Never NULL. */
 const char* dsa_status_string(int status);
@@ -220,6 +222,13 @@ typedef struct dsa_args {
  * first use (e.g. cudaMemsetAsync); every completed call leaves it ready for the next one.  Two
  * calls that share a workspace must not run concurrently. */
 dsa_status dsa_workspace_size(const dsa_args* a, int prefill, size_t* bytes);
+
+/* Number of kernels that one dsa_decode (prefill = 0) or dsa_prefill (prefill = 1) call with `a`
+ * launches on its stream, written to *launches: per slice of queries the index score (when
+ * L > 0), one Top-K kernel (or three for rows split over independent CTAs, four when the index
+ * score did not supply the score histogram), the attention kernel and, when K is split over
+ * CTAs, the combine kernel.  Validates `a` like dsa_workspace_size; launches nothing. */
+dsa_status dsa_launch_count(const dsa_args* a, int prefill, int* launches);
 
 dsa_status dsa_decode(const dsa_args* a, void* ws, size_t ws_bytes, void* stream);
 dsa_status dsa_prefill(const dsa_args* a, void* ws, size_t ws_bytes, void* stream);

@@ -126,6 +126,18 @@ def test_fused_validation(native):
     n = ctypes.c_size_t(0)
     assert native.lib.dsa_workspace_size(ctypes.byref(a), 0, ctypes.byref(n)) == 0
     assert n.value >= 2 * 64 * 4
+    # launches per call: index score, Top-K, attention (+ combine when K is split over CTAs)
+    c = ctypes.c_int(-1)
+    assert native.lib.dsa_launch_count(ctypes.byref(a), 0, ctypes.byref(c)) == 0
+    assert c.value in (3, 4)
+    assert native.lib.dsa_launch_count(ctypes.byref(a), 0, None) == 1
+    # a row long enough for the row-split Top-K (three kernels after the fused histogram)
+    a.L, a.K = 300000, 2048
+    a.k_seq_stride = 300000 * 128
+    a.kv_seq_stride = 128 * 300000
+    assert native.lib.dsa_launch_count(ctypes.byref(a), 0, ctypes.byref(c)) == 0
+    assert c.value in (5, 6)
+    a.L, a.K, a.k_seq_stride, a.kv_seq_stride = 64, 8, 64 * 128, 128 * 64
     # decode entry with a causal q_pos0, prefill entry without one, and a block table
     assert native.lib.dsa_workspace_size(ctypes.byref(a), 1, ctypes.byref(n)) == 1
     a.block_table = F

@@ -129,6 +129,53 @@ def test_topk_long_rows_uncached_path(dsa):
     _topk_case(dsa, s, 4096, 70001)
 
 
+# rows longer than 16 x 16384 positions take the row-split path (chunks on independent CTAs)
+
+
+def test_topk_row_split_random_ragged(dsa):
+    rng = np.random.default_rng(21)
+    s = (rng.standard_normal((3, 300001)) * 30 + 140).astype(np.float32)
+    _topk_case(dsa, s, 2048, 300001, n_valid=[300001, 262145, 150000])
+
+
+def test_topk_row_split_heavy_ties(dsa):
+    rng = np.random.default_rng(22)
+    s = (np.round(rng.standard_normal((2, 400000)) * 2) / 2).astype(np.float32)  # ~20 distinct values
+    s[1] = -np.abs(s[1])
+    _topk_case(dsa, s, 4096, 400000)
+
+
+def test_topk_row_split_all_equal(dsa):
+    s = np.full((1, 270000), -2.25, dtype=np.float32)
+    _topk_case(dsa, s, 2048, 270000)
+    _topk_case(dsa, s, 1, 270000)
+
+
+def test_topk_row_split_rows_at_and_below_k(dsa):
+    rng = np.random.default_rng(23)
+    s = rng.standard_normal((4, 280000)).astype(np.float32)
+    _topk_case(dsa, s, 1000, 280000, n_valid=[0, 999, 1000, 1001])
+
+
+def test_topk_row_split_workspace_reuse(dsa):
+    # the histograms in the workspace must be zero again after each call
+    rng = np.random.default_rng(24)
+    T, L, K = 2, 300000, 2048
+    from top_sparse_attention_gb300 import _native
+
+    ws_bytes = _native.lib.dsa_topk_workspace_size(T, L, K)
+    ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+    for rep in range(3):
+        s = (rng.standard_normal((T, L)) * (1 + rep)).astype(np.float32)
+        ld = dsa.ld_scores_for(L)
+        buf = np.zeros((T, ld), dtype=np.float32)
+        buf[:, :L] = s
+        idx = dsa.dsa_topk(torch.from_numpy(buf).cuda(), K, L=L, ws=ws).cpu().numpy()
+        for t in range(T):
+            want = np.sort(oracle.topk_positions(s[t].astype(np.float64), K))
+            assert np.array_equal(want, idx[t]), f"rep={rep} t={t}"
+
+
 def test_topk_causal_rows(dsa):
     rng = np.random.default_rng(15)
     s = rng.standard_normal((6, 2600)).astype(np.float32)

@@ -19,7 +19,7 @@ DEVERR = {0: "none", 1: "index out of range", 2: "wait timeout"}
 EXPORTS = (
     "dsa_status_string", "dsa_abi_version", "dsa_get_device_error", "dsa_index_score",
     "dsa_topk", "dsa_topk_workspace_size", "dsa_sparse_attn", "dsa_sparse_attn_workspace_size",
-    "dsa_workspace_size", "dsa_decode", "dsa_prefill", "dsa_topk_noalloc",
+    "dsa_workspace_size", "dsa_launch_count", "dsa_decode", "dsa_prefill", "dsa_topk_noalloc",
     "dsa_selftest_wait_timeout",
 )
 
@@ -71,6 +71,7 @@ def _load():
                                 P, SZ, P]),
         "dsa_sparse_attn_workspace_size": (SZ, [I, I, I, I]),
         "dsa_workspace_size": (I, [ctypes.POINTER(DsaArgs), I, ctypes.POINTER(SZ)]),
+        "dsa_launch_count": (I, [ctypes.POINTER(DsaArgs), I, ctypes.POINTER(ctypes.c_int)]),
         "dsa_decode": (I, [ctypes.POINTER(DsaArgs), P, SZ, P]),
         "dsa_prefill": (I, [ctypes.POINTER(DsaArgs), P, SZ, P]),
     }

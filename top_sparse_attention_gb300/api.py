@@ -13,7 +13,7 @@ import torch
 from . import _native as N
 
 __all__ = ["dsa_index_score", "dsa_topk", "dsa_sparse_attn", "DsaCall", "dsa_decode", "dsa_prefill",
-           "dsa_workspace_size", "dsa_get_device_error", "ld_scores_for"]
+           "dsa_workspace_size", "dsa_launch_count", "dsa_get_device_error", "ld_scores_for"]
 
 
 def _p(t: Optional[torch.Tensor]):
@@ -152,6 +152,7 @@ class DsaCall:
             raise ValueError(f"workspace has {ws.numel()} bytes, needs {need}")
         self.ws = ws
         self._fn = N.lib.dsa_prefill if self.prefill else N.lib.dsa_decode
+        self.launches = dsa_launch_count(a, self.prefill)  # kernels per call
 
     def __call__(self, stream=None):
         st = self._fn(ctypes.byref(self.args), _p(self.ws), self.ws.numel(), _stream(stream))
@@ -163,6 +164,14 @@ def dsa_workspace_size(args: N.DsaArgs, prefill: bool) -> int:
     n = ctypes.c_size_t(0)
     N.check(N.lib.dsa_workspace_size(ctypes.byref(args), int(bool(prefill)), ctypes.byref(n)),
             "dsa_workspace_size")
+    return n.value
+
+
+def dsa_launch_count(args: N.DsaArgs, prefill: bool) -> int:
+    """Kernels one dsa_decode / dsa_prefill call with `args` launches."""
+    n = ctypes.c_int(0)
+    N.check(N.lib.dsa_launch_count(ctypes.byref(args), int(bool(prefill)), ctypes.byref(n)),
+            "dsa_launch_count")
     return n.value
 
 

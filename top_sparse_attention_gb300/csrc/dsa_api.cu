@@ -470,6 +470,23 @@ dsa_status dsa_workspace_size(const dsa_args* a, int prefill, size_t* bytes) {
   return DSA_OK;
 }
 
+dsa_status dsa_launch_count(const dsa_args* a, int prefill, int* launches) {
+  if (!launches) return DSA_ERR_INVALID_ARG;
+  const dsa_status s = check_args(a, prefill);
+  if (s != DSA_OK) return s;
+  const int tc = slice_queries(*a, prefill);
+  int n = 0;
+  for (int t0 = 0; t0 < a->T; t0 += tc) {
+    const int tn = (a->T - t0) < tc ? (a->T - t0) : tc;
+    const bool filled =
+        a->L > 0 && index_score_builds_hist(tn, a->H_idx, a->q_per_seq, a->idx_dtype == DSA_MXFP8_E4M3);
+    n += (a->L > 0 ? 1 : 0) + topk_launches(tn, a->L, filled) +
+         (sparse_attn_splits(tn, a->H, a->K) > 1 ? 2 : 1);
+  }
+  *launches = n;
+  return DSA_OK;
+}
+
 dsa_status dsa_decode(const dsa_args* a, void* ws, size_t ws_bytes, void* stream) {
   return run_chain(a, ws, ws_bytes, stream, 0);
 }

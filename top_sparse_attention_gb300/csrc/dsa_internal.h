@@ -56,6 +56,10 @@ constexpr int kHistBins = 4096;
 
 // Launches the index-score kernel.  *hist_filled reports whether p.hist was filled (only the
 // one-query-per-tile variants build it).
+// Whether the index-score launch for these queries builds the 12-bit score histogram (the
+// one-query-per-tile variants do; four-query prefill groups do not).
+bool index_score_builds_hist(int T, int H_idx, int q_per_seq, bool mx);
+
 cudaError_t launch_index_score(const void* q_idx, const void* k_idx, int64_t k_seq_stride,
                                int n_seq, int d_idx, bool mx, IndexScoreParams p,
                                cudaStream_t stream, bool pdl, bool* hist_filled);
@@ -74,6 +78,7 @@ struct TopkParams {
   uint32_t* hist;          // [T][4096] top-12-bit histograms from the index-score kernel, or
                            // null (then built here); zeroed after use
   uint32_t* work;          // per-query exchange areas (set by launch_topk from its workspace)
+  int wide_chunk, wide_nch;  // row-split path: positions per CTA and CTAs per row (launch_topk)
   // Optional L2 prefetch of the selected rows of the attention cache (null kv: none), issued as
   // each selected position is written.
   const uint8_t* kv;
@@ -84,7 +89,12 @@ struct TopkParams {
   int v_bytes;
 };
 
-cudaError_t launch_topk(const TopkParams& p, void* ws, cudaStream_t stream, bool pdl);
+// allow_wide: long rows may be split over independent CTAs (workspace from topk_ws_bytes);
+// otherwise one cluster per query (workspace from topk_cluster_ws_bytes).
+cudaError_t launch_topk(const TopkParams& p, void* ws, cudaStream_t stream, bool pdl,
+                        bool allow_wide = true);
+size_t topk_cluster_ws_bytes(int T, int L);
+int topk_launches(int T, int L, bool hist_supplied);
 size_t topk_ws_bytes(int T, int L, int K);
 
 // ---------------------------------------------------------------------------------------------

@@ -481,12 +481,20 @@ cudaError_t launch_cfg(const void* q_idx, const void* k_idx, int64_t k_seq_strid
 
 }  // namespace
 
+// queries that share one cache are scored four at a time (N = 4 x 64) when they can be
+static bool grouped_launch(int T, int H_idx, int q_per_seq, bool mx) {
+  return !mx && H_idx > 32 && q_per_seq % 4 == 0 && T >= 4;
+}
+
+bool index_score_builds_hist(int T, int H_idx, int q_per_seq, bool mx) {
+  return !grouped_launch(T, H_idx, q_per_seq, mx);
+}
+
 cudaError_t launch_index_score(const void* q_idx, const void* k_idx, int64_t k_seq_stride, int n_seq,
                                int d_idx, bool mx, IndexScoreParams p, cudaStream_t stream, bool pdl,
                                bool* hist_filled) {
   const int npad = p.H_idx <= 16 ? 16 : (p.H_idx <= 32 ? 32 : 64);
-  // queries that share one cache are scored four at a time (N = 4 x 64) when they can be
-  const bool grouped = !mx && npad == 64 && p.q_per_seq % 4 == 0 && p.T >= 4;
+  const bool grouped = grouped_launch(p.T, p.H_idx, p.q_per_seq, mx);
   if (grouped) p.hist = nullptr;  // the fused histogram is built by the one-query variants only
   if (hist_filled) *hist_filled = p.hist != nullptr;
   if (mx) {

@@ -563,6 +563,312 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkParams
       reinterpret_cast<uint4*>(gh1)[i] = make_uint4(0u, 0u, 0u, 0u);  // gh1 and gh2 are adjacent
 }
 
+// ---------------------------------------------------------------------------------------------
+// Row-split Top-K for long rows.
+//
+// A cluster holds at most 16 CTAs, so one query over a million positions would keep 16 SMs busy
+// and re-read most of its keys from L2 on every pass.  Here a row is cut into chunks, one CTA
+// each, and the CTAs of a row exchange counts through the workspace between kernels, so no CTA
+// ever waits on another:
+//  * scan (one CTA per chunk): every CTA finds the level-0 bin b0 from the row's 12-bit histogram,
+//    counts its keys above b0, appends its candidates (keys in b0, with positions) to its own
+//    list and adds their next 10 bits into the row's level-1 histogram;
+//  * resolve (one CTA per row): the level-1 digit, a level-2 histogram of the matching candidates
+//    (one warp per chunk list), the threshold key T and the ties to take, then each chunk's
+//    candidates above and equal to T and their exclusive prefixes over the chunks; the row's
+//    histograms are zeroed again;
+//  * emit (one CTA per chunk): the chunk's keys are read once more and every kept position goes
+//    to slot (keys > T before it) + min(keys == T before it, ties to take), as in the cluster path.
+// Without a histogram from the index-score kernel a first kernel builds it from the chunks.
+
+// Per-query workspace of the row-split path, in 32-bit words: level-0 histogram (when none is
+// supplied) | level-1 histogram | 8 row words | 4 words per chunk | one (key, position) list of
+// `chunk` entries per chunk.
+constexpr int kWsWGh0 = 0;
+constexpr int kWsWGh1 = kWsWGh0 + kHistBins;
+constexpr int kWsWRow = kWsWGh1 + kLevelBins;  // [0] T, [1] ties to take
+constexpr int kWsWChunk = kWsWRow + 8;         // per chunk: above b0, candidates, > T before, == T before
+constexpr int kWideMaxChunks = kThreads;       // the resolve kernel scans one chunk per thread
+__host__ __device__ inline int64_t wide_words(int nch, int chunk) {
+  return kWsWChunk + 4 * (int64_t)nch + 2 * (int64_t)nch * chunk;
+}
+
+struct WideRow {
+  uint32_t* gh0;
+  uint32_t* gh1;
+  uint32_t* row;
+  uint32_t* chunk;
+  uint2* lists;
+};
+
+__device__ __forceinline__ WideRow wide_row(const TopkParams& p, int t) {
+  uint32_t* ws = p.work + (int64_t)t * wide_words(p.wide_nch, p.wide_chunk);
+  WideRow w;
+  w.gh0 = p.hist ? p.hist + (int64_t)t * kHistBins : ws + kWsWGh0;
+  w.gh1 = ws + kWsWGh1;
+  w.row = ws + kWsWRow;
+  w.chunk = ws + kWsWChunk;
+  w.lists = reinterpret_cast<uint2*>(ws + kWsWChunk + 4 * (int64_t)p.wide_nch);
+  return w;
+}
+
+// Keys of one chunk: positions [lo, lo + cnt) of row t.
+struct ChunkKeys {
+  const float* src;
+  int lo, cnt;
+  bool vec;
+  __device__ ChunkKeys(const TopkParams& p, int t, int c, int n) {
+    lo = min(n, c * p.wide_chunk);
+    cnt = min(n, lo + p.wide_chunk) - lo;
+    src = p.scores + (int64_t)t * p.ld_scores + lo;
+    vec = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
+  }
+  // keys at local positions i .. i+3; positions >= cnt read as 0 (callers bound-check)
+  __device__ __forceinline__ void load(int i, uint32_t (&k)[4]) const {
+    if (vec && i + 3 < cnt) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(src + i));
+      k[0] = float_key(v.x), k[1] = float_key(v.y), k[2] = float_key(v.z), k[3] = float_key(v.w);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) k[j] = i + j < cnt ? float_key(__ldcg(src + i + j)) : 0u;
+    }
+  }
+};
+
+__global__ void __launch_bounds__(kThreads) topk_wide_hist_kernel(const TopkParams p) {
+  __shared__ uint32_t h0[kHistBins];
+  pdl_launch_dependents();
+  const int c = blockIdx.x, t = blockIdx.y, tid = threadIdx.x;
+  for (int b = tid; b < kHistBins; b += kThreads) h0[b] = 0;
+  pdl_wait();
+  const int n = visible_len(t + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid);
+  if (n <= p.K) return;  // every position is kept; nothing to count
+  const ChunkKeys ck(p, t, c, n);
+  __syncthreads();
+  for (int base = 0; base < ck.cnt; base += kChunk) {
+    const int i = base + 4 * tid;
+    uint32_t k[4];
+    ck.load(i, k);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) hist_add(h0, i + j < ck.cnt ? k[j] >> 20 : kNoBin);
+  }
+  __syncthreads();
+  flush_bins(h0, wide_row(p, t).gh0, kHistBins);
+}
+
+__global__ void __launch_bounds__(kThreads) topk_wide_scan_kernel(const TopkParams p) {
+  __shared__ uint32_t h1[kLevelBins];
+  __shared__ uint32_t sc[256];
+  pdl_launch_dependents();
+  const int c = blockIdx.x, t = blockIdx.y, tid = threadIdx.x, lane = tid & 31;
+#pragma unroll
+  for (int k = 0; k < kBins1; ++k) h1[kBins1 * tid + k] = 0;
+  if (tid == 0) sc[kScCand] = sc[kScAboveOwn] = 0;
+  pdl_wait();
+  const int n = visible_len(t + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid);
+  if (n <= p.K) return;
+  const WideRow w = wide_row(p, t);
+  const ChunkKeys ck(p, t, c, n);
+  uint32_t c0[kBins0];
+  load_bins<kBins0>(w.gh0, c0);
+  uint32_t above;
+  const uint32_t b0 = find_digit<kBins0>(c0, (uint32_t)p.K, sc, &above);  // also orders the zeroing
+  uint2* list = w.lists + (int64_t)c * p.wide_chunk;
+  uint32_t n_above = 0;
+  for (int base = 0; base < ck.cnt; base += kChunk) {
+    const int i = base + 4 * tid;
+    uint32_t k[4];
+    ck.load(i, k);
+    uint32_t cm = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const bool ok = i + j < ck.cnt;
+      const uint32_t d = k[j] >> 20;
+      n_above += ok && d > b0;
+      cm |= (uint32_t)(ok && d == b0) << j;
+    }
+    // candidates go to this chunk's list (one shared-memory atomic per warp places them)
+    const uint32_t nc = __popc(cm);
+    uint32_t incl = nc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
+    if (tot) {
+      uint32_t wbase = 0;
+      if (lane == 31) wbase = atomicAdd(&sc[kScCand], tot);
+      uint32_t o = __shfl_sync(0xffffffffu, wbase, 31) + incl - nc;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if ((cm >> j) & 1u) {
+          list[o++] = make_uint2(k[j], (uint32_t)(ck.lo + i + j));
+          atomicAdd(&h1[(k[j] >> 10) & (kLevelBins - 1)], 1u);
+        }
+    }
+  }
+  n_above = __reduce_add_sync(0xffffffffu, n_above);
+  if (lane == 0 && n_above) atomicAdd(&sc[kScAboveOwn], n_above);
+  __syncthreads();
+  flush_bins(h1, w.gh1, kLevelBins);
+  if (tid == 0) {
+    w.chunk[4 * c] = sc[kScAboveOwn];
+    w.chunk[4 * c + 1] = sc[kScCand];
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) topk_wide_resolve_kernel(const TopkParams p) {
+  __shared__ uint32_t h2[kLevelBins];
+  __shared__ uint32_t sc[256];
+  __shared__ uint32_t gt_c[kWideMaxChunks];
+  __shared__ uint32_t eq_c[kWideMaxChunks];
+  pdl_launch_dependents();
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+  for (int k = 0; k < kBins1; ++k) h2[kBins1 * tid + k] = 0;
+  pdl_wait();
+  const int n = visible_len(t + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid);
+  const WideRow w = wide_row(p, t);
+  if (n <= p.K) {  // the ready-made histogram is left zeroed; the emit kernel keeps everything
+    if (p.hist)
+      for (int b = tid; b < kHistBins / 4; b += kThreads)
+        reinterpret_cast<uint4*>(w.gh0)[b] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  uint32_t above, kr = (uint32_t)p.K;
+  uint32_t c0[kBins0];
+  load_bins<kBins0>(w.gh0, c0);
+  const uint32_t b0 = find_digit<kBins0>(c0, kr, sc, &above);
+  kr -= above;
+  uint32_t c1[kBins1];
+  load_bins<kBins1>(w.gh1, c1);
+  const uint32_t d1 = find_digit<kBins1>(c1, kr, sc, &above);
+  kr -= above;
+  const uint32_t p22 = (b0 << 10) | d1;  // the first 22 bits of T
+  // every thread has read both histograms (find_digit ends with a barrier): leave them zeroed
+  for (int b = tid; b < kHistBins / 4; b += kThreads)
+    reinterpret_cast<uint4*>(w.gh0)[b] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+  for (int k = 0; k < kBins1; ++k) w.gh1[kBins1 * tid + k] = 0;
+
+  // level 2 over the candidates that share p22, one warp per chunk list
+  const int nch = p.wide_nch;
+  for (int c = warp; c < nch; c += kWarps) {
+    const uint32_t m = __ldcg(w.chunk + 4 * c + 1);
+    const uint2* list = w.lists + (int64_t)c * p.wide_chunk;
+    for (uint32_t j = lane; j < m; j += 32) {
+      const uint32_t key = __ldcg(list + j).x;
+      if ((key >> 10) == p22) atomicAdd(&h2[key & (kLevelBins - 1)], 1u);
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < kBins1; ++k) c1[k] = h2[kBins1 * tid + k];
+  const uint32_t d2 = find_digit<kBins1>(c1, kr, sc, &above);
+  kr -= above;  // ties to take
+  const uint32_t T = (p22 << 10) | d2;
+
+  // per chunk: keys above T (above b0, plus candidates above T) and keys equal to T
+  for (int c = warp; c < nch; c += kWarps) {
+    const uint32_t m = __ldcg(w.chunk + 4 * c + 1);
+    const uint2* list = w.lists + (int64_t)c * p.wide_chunk;
+    uint32_t g = 0, q = 0;
+    for (uint32_t j = lane; j < m; j += 32) {
+      const uint32_t key = __ldcg(list + j).x;
+      g += key > T;
+      q += key == T;
+    }
+    g = __reduce_add_sync(0xffffffffu, g);
+    q = __reduce_add_sync(0xffffffffu, q);
+    if (lane == 0) {
+      gt_c[c] = g + __ldcg(w.chunk + 4 * c);
+      eq_c[c] = q;
+    }
+  }
+  __syncthreads();
+  // exclusive prefixes over the chunks (one chunk per thread; both sums stay below 2^32)
+  const uint64_t v = tid < nch ? ((uint64_t)eq_c[tid] << 32) | gt_c[tid] : 0ull;
+  uint64_t tot;
+  const uint64_t ex = block_excl_scan(v, sc, &tot);
+  if (tid < nch) {
+    w.chunk[4 * tid + 2] = (uint32_t)ex;
+    w.chunk[4 * tid + 3] = (uint32_t)(ex >> 32);
+  }
+  if (tid == 0) {
+    w.row[0] = T;
+    w.row[1] = kr;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) topk_wide_emit_kernel(const TopkParams p) {
+  __shared__ uint32_t sc[256];
+  pdl_launch_dependents();
+  const int c = blockIdx.x, t = blockIdx.y, tid = threadIdx.x;
+  pdl_wait();
+  const int n = visible_len(t + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid);
+  int32_t* out = p.idx + (int64_t)t * p.K;
+  const int64_t seq = (t + p.t_off) / p.q_per_seq;
+  const uint8_t* pf_kv = p.kv ? p.kv + seq * p.kv_seq_stride : nullptr;
+  const uint8_t* pf_v = p.kv_v ? p.kv_v + seq * p.v_seq_stride : nullptr;
+  auto prefetch_row = [&](uint32_t pos) {
+    if (!pf_kv) return;
+    prefetch_l2(pf_kv + (int64_t)pos * p.kv_row_stride, (uint32_t)p.kv_bytes);
+    if (pf_v) prefetch_l2(pf_v + (int64_t)pos * p.v_row_stride, (uint32_t)p.v_bytes);
+  };
+  const ChunkKeys ck(p, t, c, n);
+  if (n <= p.K) {  // every visible position, in order, then -1
+    for (int i = tid; i < ck.cnt; i += kThreads) {
+      out[ck.lo + i] = ck.lo + i;
+      prefetch_row((uint32_t)(ck.lo + i));
+    }
+    if (c == 0)
+      for (int i = n + tid; i < p.K; i += kThreads) out[i] = -1;
+    return;
+  }
+  const WideRow w = wide_row(p, t);
+  const uint32_t T = __ldcg(w.row), take = __ldcg(w.row + 1);
+  uint32_t gt_before = __ldcg(w.chunk + 4 * c + 2), eq_before = __ldcg(w.chunk + 4 * c + 3);
+  for (int base = 0; base < ck.cnt; base += kChunk) {
+    const int i = base + 4 * tid;
+    uint32_t k[4];
+    ck.load(i, k);
+    uint32_t g = 0, q = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const bool ok = i + j < ck.cnt;
+      g += ok && k[j] > T;
+      q += ok && k[j] == T;
+    }
+    uint64_t tot;
+    const uint64_t ex = block_excl_scan(((uint64_t)q << 32) | g, sc, &tot);
+    uint32_t ga = gt_before + (uint32_t)ex, qa = eq_before + (uint32_t)(ex >> 32);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (i + j >= ck.cnt) break;
+      const uint32_t pos = (uint32_t)(ck.lo + i + j);
+      uint32_t slot = kNoBin;
+      if (k[j] > T) {
+        slot = ga + min(qa, take);
+        ++ga;
+      } else if (k[j] == T) {
+        if (qa < take) slot = ga + qa;
+        ++qa;
+      }
+      if (slot != kNoBin) {
+        if (slot < (uint32_t)p.K) {  // always, when the counts of the row agree
+          out[slot] = (int32_t)pos;
+          prefetch_row(pos);
+        } else {
+          record_error(p.err, DSA_DEVERR_TOPK_COUNTS);
+        }
+      }
+    }
+    gt_before += (uint32_t)tot;
+    eq_before += (uint32_t)(tot >> 32);
+  }
+}
+
 // About kChunk keys per CTA, at most 16 CTAs per cluster; at most 8 when more clusters are needed
 // than 16-CTA clusters can run at once.
 int cluster_ctas(int n_max, int T, size_t smem16) {
@@ -611,19 +917,90 @@ int cluster_ctas_max(int n_max) {
   return c;
 }
 
-size_t topk_ws_bytes(int T, int L, int) {
+size_t topk_cluster_ws_bytes(int T, int L) {
   return align_up((size_t)T * ws_words(cluster_ctas_max(L)) * sizeof(uint32_t), 256);
 }
 
-cudaError_t launch_topk(const TopkParams& p, void* ws, cudaStream_t stream, bool pdl) {
+namespace {
+
+// Row-split plan: rows longer than a 16-CTA cluster can keep in shared memory are cut into
+// chunks of a multiple of kChunk positions, sized so that all rows together take about one CTA
+// per SM of a 152-SM part (a fixed figure, so that workspace sizing needs no device query).
+struct WidePlan {
+  bool use;
+  int chunk, nch;
+};
+
+WidePlan wide_plan(int T, int L) {
+  WidePlan w = {false, 0, 0};
+  // (decode-sized batches only: the candidate lists take 8 bytes per position of every row)
+  if (T <= 0 || T > 32 || (int64_t)L <= 16ll * kCachedKeys) return w;
+  const int64_t target = T >= 152 ? 1 : 152 / T;  // chunks per row
+  int64_t chunk = ((L + target - 1) / target + kChunk - 1) / kChunk * kChunk;
+  while ((L + chunk - 1) / chunk > kWideMaxChunks) chunk += kChunk;
+  w.use = true;
+  w.chunk = (int)chunk;
+  w.nch = (int)((L + chunk - 1) / chunk);
+  return w;
+}
+
+template <typename Kern>
+cudaError_t launch_plain(Kern kern, dim3 grid, const TopkParams& p, cudaStream_t stream, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+cudaError_t launch_wide(TopkParams q, const WidePlan& w, cudaStream_t stream, bool pdl) {
+  q.wide_chunk = w.chunk;
+  q.wide_nch = w.nch;
+  const dim3 chunks(w.nch, q.T);
+  cudaError_t e = cudaSuccess;
+  if (!q.hist) {
+    e = launch_plain(topk_wide_hist_kernel, chunks, q, stream, pdl);
+    pdl = true;
+  }
+  if (e == cudaSuccess) e = launch_plain(topk_wide_scan_kernel, chunks, q, stream, pdl);
+  if (e == cudaSuccess) e = launch_plain(topk_wide_resolve_kernel, dim3(q.T), q, stream, true);
+  if (e == cudaSuccess) e = launch_plain(topk_wide_emit_kernel, chunks, q, stream, true);
+  return e;
+}
+
+}  // namespace
+
+int topk_launches(int T, int L, bool hist_supplied) {
+  if (T <= 0) return 0;
+  return wide_plan(T, L).use ? (hist_supplied ? 3 : 4) : 1;
+}
+
+size_t topk_ws_bytes(int T, int L, int) {
+  const size_t cl = topk_cluster_ws_bytes(T, L);
+  const WidePlan w = wide_plan(T, L);
+  if (!w.use) return cl;
+  const size_t wide = align_up((size_t)T * wide_words(w.nch, w.chunk) * sizeof(uint32_t), 256);
+  return wide > cl ? wide : cl;
+}
+
+cudaError_t launch_topk(const TopkParams& p, void* ws, cudaStream_t stream, bool pdl,
+                        bool allow_wide) {
   if (p.T <= 0) return cudaSuccess;
   if (!ws) return cudaErrorInvalidValue;
+  if (p.K > kMaxK) return cudaErrorNotSupported;
   TopkParams q = p;
   q.work = reinterpret_cast<uint32_t*>(ws);
+  const WidePlan w = wide_plan(p.T, p.L);
+  if (allow_wide && w.use) return launch_wide(q, w, stream, pdl);
   auto kern = topk_cluster_kernel;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
-  if (p.K > kMaxK) return cudaErrorNotSupported;
   const size_t smem16 = (size_t)TopkSmem(slice_of(p.L, 16)).words * 4;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem16);
   if (e != cudaSuccess) return e;
@@ -700,7 +1077,7 @@ extern "C" dsa_status dsa_topk_noalloc(const float* scores, int64_t ld_scores, i
   if (scratch_address(&scratch) != cudaSuccess) return DSA_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // the histograms must start at zero; the array keeps whatever the previous call left
-  if (cudaMemsetAsync(scratch, 0, topk_ws_bytes(T, L, K), st) != cudaSuccess)
+  if (cudaMemsetAsync(scratch, 0, topk_cluster_ws_bytes(T, L), st) != cudaSuccess)
     return DSA_ERR_CUDA;
   TopkParams p = {};
   p.scores = scores;
@@ -713,5 +1090,5 @@ extern "C" dsa_status dsa_topk_noalloc(const float* scores, int64_t ld_scores, i
   p.L = L;
   p.K = K;
   p.err = device_error_word();
-  return launch_topk(p, scratch, st, false) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  return launch_topk(p, scratch, st, false, /*allow_wide=*/false) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
