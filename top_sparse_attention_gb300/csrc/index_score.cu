@@ -139,7 +139,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
   uint64_t* tempty = tfull + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 4);
   float* w_s = reinterpret_cast<float*>(smem + C::OFF_W);    // [G][NPAD]
-  float* qs_s = reinterpret_cast<float*>(smem + C::OFF_QS);  // [G][NPAD][GROUPS]
+  float* qs_s = reinterpret_cast<float*>(smem + C::OFF_QS);  // [GROUPS][G * NPAD]
   uint32_t* hist_s = reinterpret_cast<uint32_t*>(smem + C::OFF_HIST);  // G == 1 only
   const bool build_hist = G == 1 && p.hist != nullptr;
 
@@ -350,7 +350,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
           if (MX) {
 #pragma unroll
             for (int g = 0; g < C::GROUPS; ++g)
-              qs_s[i * C::GROUPS + g] =
+              qs_s[g * (G * NPAD) + i] =
                   valid ? e8m0_value(p.q_sf[((int64_t)(x.t0 + j) * p.H_idx + h) * C::GROUPS + g]) : 0.f;
           }
         }
@@ -377,27 +377,46 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
       if (ok) {
         tc_fence_after();
         const uint32_t tb = tmem + ((uint32_t)(q4 * 32) << 16) + ab * C::ACC_COLS;
-        constexpr int CW = C::COLS < 32 ? C::COLS : 32;  // columns per TMEM load
+        // columns per TMEM load (16 for MXFP8, which keeps each load beside its running sums)
+        constexpr int CW = C::COLS < (MX ? 16 : 32) ? C::COLS : (MX ? 16 : 32);
 #pragma unroll
         for (int c = 0; c < C::COLS / CW; ++c) {
           const int col = half * C::COLS + c * CW;  // first accumulator column of this load
           const int j = (c * CW) / NPAD;            // this warp's query the columns belong to
+          // columns in pairs: packed fp32x2 multiply-adds (same rounding as scalar fp32)
           float v[CW];
           if (!MX) {
             tmem_ld_sync(tb + col, v);
           } else {
+            float2 acc[CW / 2];
 #pragma unroll
-            for (int i = 0; i < CW; ++i) v[i] = 0.f;
+            for (int i = 0; i < CW / 2; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int g = 0; g < C::GROUPS; ++g) {
               float d[CW];
               tmem_ld_sync(tb + g * C::N + col, d);
+              const float2 k2 = make_float2(ks[g], ks[g]);
+              const float4* qv = reinterpret_cast<const float4*>(qs_s + g * (G * NPAD) + col);
 #pragma unroll
-              for (int i = 0; i < CW; ++i) v[i] = fmaf(ks[g] * qs_s[(col + i) * C::GROUPS + g], d[i], v[i]);
+              for (int i = 0; i < CW / 4; ++i) {
+                const float4 q4 = qv[i];
+                acc[2 * i] = ffma2(fmul2(k2, make_float2(q4.x, q4.y)), make_float2(d[4 * i], d[4 * i + 1]), acc[2 * i]);
+                acc[2 * i + 1] =
+                    ffma2(fmul2(k2, make_float2(q4.z, q4.w)), make_float2(d[4 * i + 2], d[4 * i + 3]), acc[2 * i + 1]);
+              }
             }
-          }
 #pragma unroll
-          for (int i = 0; i < CW; ++i) score[j] = fmaf(w_s[col + i], fmaxf(v[i], 0.f), score[j]);
+            for (int i = 0; i < CW / 2; ++i) v[2 * i] = acc[i].x, v[2 * i + 1] = acc[i].y;
+          }
+          float2 sc2 = make_float2(0.f, 0.f);
+          const float4* wv = reinterpret_cast<const float4*>(w_s + col);
+#pragma unroll
+          for (int i = 0; i < CW / 4; ++i) {
+            const float4 w4 = wv[i];
+            sc2 = ffma2(make_float2(w4.x, w4.y), make_float2(fmaxf(v[4 * i], 0.f), fmaxf(v[4 * i + 1], 0.f)), sc2);
+            sc2 = ffma2(make_float2(w4.z, w4.w), make_float2(fmaxf(v[4 * i + 2], 0.f), fmaxf(v[4 * i + 3], 0.f)), sc2);
+          }
+          score[j] += sc2.x + sc2.y;
         }
         tc_fence_before();
         __syncwarp();
