@@ -45,6 +45,10 @@ SCORE_CASES = [
     ("bf16_d128_h33", "decode_b8_l32k_bf16", dict(T=2, L=257, H_idx=33), None),
     ("mxfp8_d128_h64", "decode_b8_l32k_mxfp8", dict(T=2, L=777), None),
     ("mxfp8_d128_h20", "decode_b8_l32k_mxfp8", dict(T=3, L=200, H_idx=20), None),
+    ("mxfp8_d128_h8", "decode_b8_l32k_mxfp8", dict(T=3, L=300, H_idx=8), None),
+    ("mxfp8_d128_h40_t1", "decode_b8_l32k_mxfp8", dict(T=1, L=1000, H_idx=40), None),
+    ("mxfp8_wide_scales", "decode_b8_l32k_mxfp8", dict(T=3, L=900), None),
+    ("mxfp8_varlen", "decode_b8_l32k_mxfp8", dict(T=4, L=1300), [1300, 5, 0, 777]),
     ("varlen", "decode_b8_l32k_bf16", dict(T=4, L=1000), [0, 1, 129, 1000]),
     ("prefill_grouped", "prefill_t4096_l128k_bf16", dict(T=8, q_per_seq=8, L=600, q_pos0=400), None),
     ("prefill_ungrouped_t6", "prefill_t4096_l128k_bf16", dict(T=6, q_per_seq=6, L=700, q_pos0=10), None),
@@ -58,6 +62,12 @@ def test_index_score_parity(dsa, name, base, kw, n_valid):
     cpu = synth.make_inputs(wl, n_valid=n_valid)
     if name == "bf16_d128_h17":
         cpu["w"] = cpu["w"] - 0.5  # negative head weights
+    if name == "mxfp8_wide_scales":
+        # every group, row and head its own exponent: a scale applied to the wrong group, row or
+        # head changes the scores far beyond the bound
+        g = torch.Generator().manual_seed(5)
+        for key in ("q_idx_sf", "k_idx_sf"):
+            cpu[key] = torch.randint(118, 137, tuple(cpu[key].shape), generator=g, dtype=torch.int32).to(torch.uint8)
     dev = to_device(cpu)
     scores = dsa.dsa_index_score(dev["q_idx"], dev["w"], dev["k_idx"], q_idx_sf=dev["q_idx_sf"],
                                  k_idx_sf=dev["k_idx_sf"], q_per_seq=wl.q_per_seq, q_pos0=wl.q_pos0,

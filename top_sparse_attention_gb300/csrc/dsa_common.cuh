@@ -187,6 +187,34 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t
       : "memory");
 }
 
+// D[tmem] (+)= (A x 2^(sfA - 127)) * (B x 2^(sfB - 127))^T with E4M3 inputs and E8M0 scales per
+// 32 K-elements (kind::mxf8f6f4, scale_vec::1X: one K = 32 step per instruction).  Scale
+// factors live in tensor memory: A row m reads lane m, column sfa + m / 32; B column n reads
+// column sfb + n / 32 in the lane (n % 32) of every 32-lane quarter; the byte within the 32-bit
+// word is the scale-factor id of the instruction descriptor (make_idesc_mx).
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Registers -> TMEM: thread i of the warp writes lane (base + i), W consecutive columns.
+__device__ __forceinline__ void tmem_st_x4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b),
+               "r"(c), "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_x2(uint32_t taddr, uint32_t a, uint32_t b) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(a), "r"(b) : "memory");
+}
+// Waits until this thread's tcgen05.st writes are done.
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Arrive on `bar` once all previously issued tcgen05 operations of this thread complete.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile(
@@ -280,6 +308,16 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t a_fmt, uint32_t b_fmt
          | (a_fmt << 7) | (b_fmt << 10)  // A, B formats
          | ((uint32_t)(N >> 3) << 17)    // N / 8
          | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+// Instruction descriptor of the block-scaled kind::mxf8f6f4 MMA: E4M3 A and B (K-major), f32 D,
+// E8M0 scales; sfa_id / sfb_id pick the byte of each scale word that this K step uses.
+__host__ __device__ constexpr uint32_t make_idesc_mx(int M, int N, uint32_t sfa_id, uint32_t sfb_id) {
+  return (sfb_id << 4)                   // B scale-factor byte
+         | ((uint32_t)(N >> 3) << 17)    // N / 8
+         | (1u << 23)                    // scale type: E8M0
+         | ((uint32_t)(M >> 4) << 24)    // M / 16
+         | (sfa_id << 29);               // A scale-factor byte
 }
 
 // ------------------------------------------------------------------------------------------

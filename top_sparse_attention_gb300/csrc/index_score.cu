@@ -11,20 +11,20 @@
 // per-group E8M0 scales are applied in registers with no cross-thread reduction.
 //
 // Warp roles: warp 0 = producer (TMA for A and B), warp 1 = TMEM owner and MMA issuer, warps
-// 2-5 = epilogue.  Heavy epilogues (MXFP8 with N >= 32, four queries per tile) use 8 epilogue
-// warps in two groups that split the accumulator columns: by query (each group scores its own
-// queries) or, for one query, by head (group 1 hands its partial scores to group 0 through
-// shared memory).  A ring of shared-memory stages decouples loads
-// from MMAs; up to four TMEM accumulators let the epilogue trail the MMAs by several tiles.
+// 2-5 = epilogue.  The four-query prefill tiles (N = 256) use 16 epilogue warps in four groups,
+// one query each.  A ring of shared-memory stages decouples loads from MMAs; up to four TMEM
+// accumulators let the epilogue trail the MMAs by several tiles.
 // The grid is persistent: CTA c processes a contiguous range of (query group, tile) units.
 //
 // For the Top-K step, the epilogue also builds a histogram of the top 12 bits of each score's
 // order-preserving key (shared memory, flushed to a per-query global histogram with atomics on
 // non-zero bins), so selection starts with its first digit pass done.
 //
-// MXFP8: one kind::f8f6f4 MMA covers K = 32 = one scale group, so each group accumulates into
-// its own TMEM columns and the epilogue forms  sum_g 2^(ea_g) 2^(eb_g) D_g  (exact scaling of
-// fp32 partial sums by powers of two), i.e. the dequantisation happens in registers.
+// MXFP8: the tensor cores apply the scales.  One block-scaled kind::mxf8f6f4 MMA covers K = 32 =
+// one scale group, and reads each key row's and each head's E8M0 exponent for that group from
+// tensor memory, so a tile accumulates  sum_g 2^(ea_g + eb_g - 254) D_g  into one accumulator and
+// the epilogue is the bf16 one.  The epilogue warps write the scale words into tensor memory
+// (one slot per accumulator, a full pipeline depth ahead of the tile they read).
 #include <string.h>
 
 #include <utility>
@@ -54,17 +54,20 @@ struct Cfg {
   static constexpr int A_BYTES = kTileM * ROW_BYTES;
   static constexpr int B_BYTES = N * ROW_BYTES;
   static constexpr int B_BUFS = (2 * B_BYTES <= 64 * 1024) ? 2 : 1;
-  static constexpr int GROUPS = MX ? D / 32 : 1;  // accumulators per tile
-  static constexpr int ACC_COLS = GROUPS * N;
+  static constexpr int GROUPS = MX ? D / 32 : 1;  // scale groups per row (MMAs per tile)
+  static constexpr int ACC_COLS = N;
   // accumulators in flight between the MMA warp and the epilogue: as many as fit in 512 columns,
   // up to 4 (two were not enough to hide MMA completion + epilogue latency per tile)
   static constexpr int ACC_BUFS = 512 / ACC_COLS >= 4 ? 4 : 2;
-  static constexpr int TMEM_COLS = pow2_at_least(ACC_BUFS * ACC_COLS);
+  // MXFP8 scale slots after the accumulators, 16 columns each: A scales (4 copies of the row's
+  // scale word, so that quarter q finds it in column q) and, 8 columns in, B scales (one
+  // column per 32 heads, repeated in every lane quarter)
+  static constexpr int SF_BASE = ACC_BUFS * ACC_COLS;
+  static constexpr int SF_COLS = MX ? 16 * ACC_BUFS : 0;
+  static constexpr int TMEM_COLS = pow2_at_least(SF_BASE + SF_COLS);
   static constexpr int HIST_BYTES = G == 1 ? kHistBins * 4 : 0;  // fused score histogram
-  // MXFP8 epilogues do four times the work per tile: two warp groups split the head columns
-  // epilogue warps: eight (two groups splitting the accumulator columns) where a tile's epilogue
-  // is heavy: MXFP8 (four scale groups) and four queries per tile (N = 256)
-  static constexpr int EPI = G == 4 ? 16 : ((MX && N >= 32) ? 8 : 4);
+  // epilogue warps: sixteen (four groups, one query each) for four queries per tile (N = 256)
+  static constexpr int EPI = G == 4 ? 16 : 4;
   static constexpr int SPLITS = EPI / 4;      // column splits (each warp group covers all rows)
   static constexpr int THREADS = 64 + 32 * EPI;
   static constexpr int COLS = N / SPLITS;     // accumulator columns per epilogue warp
@@ -72,18 +75,18 @@ struct Cfg {
   // query (groups 1.. hand partial scores to group 0)
   static constexpr bool QSPLIT = COLS % NPAD == 0;
   static constexpr int PART_BYTES = QSPLIT ? 0 : 2 * (SPLITS - 1) * kTileM * 4;
-  static constexpr int AUX_BYTES = 1024 + 4096 + G * NPAD * 4 + G * NPAD * GROUPS * 4 + HIST_BYTES + PART_BYTES;
+  static constexpr int AUX_BYTES = 1024 + 4096 + G * NPAD * 4 + HIST_BYTES + PART_BYTES;
   static constexpr int STAGES_FIT = (kSmemBudget - B_BUFS * B_BYTES - AUX_BYTES) / A_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int OFF_B = STAGES * A_BYTES;
   static constexpr int OFF_BAR = OFF_B + B_BUFS * B_BYTES;
   static constexpr int OFF_W = OFF_BAR + 1024;
-  static constexpr int OFF_QS = OFF_W + G * NPAD * 4;
-  static constexpr int OFF_HIST = OFF_QS + G * NPAD * GROUPS * 4;
+  static constexpr int OFF_HIST = OFF_W + G * NPAD * 4;
   static constexpr int OFF_PART = OFF_HIST + HIST_BYTES;
   static constexpr int SMEM = OFF_PART + PART_BYTES + 1024;  // + alignment slack
   static_assert(N % 16 == 0 && N >= 16 && N <= 256, "MMA N out of range");
-  static_assert(ACC_BUFS * ACC_COLS <= 512, "accumulators exceed tensor memory");
+  static_assert(SF_BASE + SF_COLS <= 512, "accumulators exceed tensor memory");
+  static_assert(!MX || (G == 1 && (N == 32 || N == 64) && GROUPS <= 4), "MXFP8 tile shape");
   static_assert(STAGES >= 2, "not enough shared memory for the pipeline");
   static_assert(ROW_BYTES % 128 == 0, "rows must fill whole swizzle atoms");
   static_assert(QSPLIT || G == 1, "a head split needs one query per group");
@@ -95,11 +98,6 @@ template <int THREADS>
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory"); }
 template <int THREADS>
 __device__ __forceinline__ void part_bar() { asm volatile("bar.sync 2, %0;" ::"n"(THREADS) : "memory"); }
-
-// E8M0 byte -> 2^(e - 127) as an fp32 bit pattern (e = 0 is the subnormal 2^-127).
-__device__ __forceinline__ float e8m0_value(uint32_t e) {
-  return e == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(e << 23);
-}
 
 // Unit u -> (first query of its group, tile).  Returns false when the tile holds no position
 // visible to any query of the group.
@@ -137,9 +135,9 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
   uint64_t* bempty = bfull + 2;
   uint64_t* tfull = bempty + 2;
   uint64_t* tempty = tfull + 4;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 4);
+  uint64_t* sf_full = tempty + 4;  // MXFP8 scale slot written (one arrival per epilogue warp)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_full + 4);
   float* w_s = reinterpret_cast<float*>(smem + C::OFF_W);    // [G][NPAD]
-  float* qs_s = reinterpret_cast<float*>(smem + C::OFF_QS);  // [GROUPS][G * NPAD]
   uint32_t* hist_s = reinterpret_cast<uint32_t*>(smem + C::OFF_HIST);  // G == 1 only
   const bool build_hist = G == 1 && p.hist != nullptr;
 
@@ -162,6 +160,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     for (int i = 0; i < C::ACC_BUFS; ++i) {
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], C::EPI);  // one arrival per epilogue warp
+      mbar_init(&sf_full[i], C::EPI);
     }
     fence_mbar_init();
     prefetch_tmap(&tm_k);
@@ -242,7 +241,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = MX ? make_idesc(0, 0, kTileM, C::N) : make_idesc(1, 1, kTileM, C::N);
+    constexpr uint32_t idesc = make_idesc(1, 1, kTileM, C::N);
     int it = 0, qn = -1, cur_t0 = -1, ai = 0;
     bool ok = true;
     for (int u = u_begin; u < u_end && ok; ++u) {
@@ -260,19 +259,21 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
       const int ab = ai % C::ACC_BUFS;
       if (ok && ai >= C::ACC_BUFS)
         ok = __all_sync(0xffffffffu, mbar_wait(&tempty[ab], ((ai - C::ACC_BUFS) / C::ACC_BUFS) & 1, p.err));
+      if (MX && ok) ok = __all_sync(0xffffffffu, mbar_wait(&sf_full[ab], (ai / C::ACC_BUFS) & 1, p.err));
       if (!ok) break;
       tc_fence_after();
       if (lane == 0) {
         const uint32_t a_base = smem_u32(a_s + s * C::A_BYTES);
         const uint32_t b_base = smem_u32(b_s + (qn % C::B_BUFS) * C::B_BYTES);
         const uint32_t d0 = tmem + ab * C::ACC_COLS;
+        const uint32_t sf = tmem + C::SF_BASE + 16 * ab;  // this tile's scale slot (MXFP8)
 #pragma unroll
         for (int k = 0; k < C::KSTEPS; ++k) {
           const int box = k >> 2, off = (k & 3) * 32;
           const uint64_t ad = smem_desc_sw128(a_base + box * (kTileM * 128) + off);
           const uint64_t bd = smem_desc_sw128(b_base + box * (C::N * 128) + off);
-          if (MX)
-            mma_f8(d0 + k * C::N, ad, bd, idesc, 0u);
+          if (MX)  // K step k = scale group k: byte k of the scale words
+            mma_mxf8(d0, ad, bd, make_idesc_mx(kTileM, C::N, k, k), sf, sf + 8, k > 0 ? 1u : 0u);
           else
             mma_f16(d0, ad, bd, idesc, k > 0 ? 1u : 0u);
         }
@@ -305,31 +306,54 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     };
     if (build_hist)
       for (int b = et; b < kHistBins; b += ET) hist_s[b] = 0;
-    // MXFP8: this row's key scales are loaded one unit ahead, so the global load overlaps the
-    // previous unit's epilogue instead of stalling the current one
-    auto load_ks = [&](const Unit& y) -> uint32_t {
-      uint32_t raw = 0;
-      const int pos = y.tile * kTileM + row;
-      if (pos < y.n_max) {
-        const int sq = (y.t0 + p.t_off) / p.q_per_seq;
-        const uint8_t* src = p.k_sf + (int64_t)sq * p.k_sf_seq_stride + (int64_t)pos * C::GROUPS;
-        if (C::GROUPS == 4) raw = __ldg(reinterpret_cast<const uint32_t*>(src));
-        else
-          for (int g = 0; g < C::GROUPS; ++g) raw |= (uint32_t)__ldg(src + g) << (8 * g);
-      }
-      return raw;
-    };
     // the next visible unit after u (u_end when none)
     auto next_unit = [&](int u, Unit& y) -> int {
       for (++u; u < u_end; ++u)
         if (unit_of<G>(p, u, y)) return u;
       return u_end;
     };
-    uint32_t raw_next = 0;
-    if (MX) {
-      Unit y;
-      const int u0 = next_unit(u_begin - 1, y);
-      if (u0 < u_end) raw_next = load_ks(y);
+    // MXFP8 scale writer.  The n-th visible unit's scale words go to slot n % ACC_BUFS, a full
+    // pipeline depth ahead of the accumulator the epilogue reads; a unit's key-scale word is
+    // loaded when the previous unit is written, so the global load overlaps a tile's epilogue.
+    // Each lane writes its lane of the warp's quarter: its row's four group exponents (byte g =
+    // group g) into the four A columns, and those of heads (lane) and (32 + lane) of the unit's
+    // query into the two B columns.
+    Unit sf_unit = {0, 0, 0};
+    int sf_u = u_end, sf_n = 0, sf_t = -1;
+    uint32_t sf_a = 0, sf_b0 = 0, sf_b1 = 0;
+    auto sf_load_a = [&](const Unit& y) -> uint32_t {
+      const int pos = y.tile * kTileM + row;
+      if (pos >= y.n_max) return 0x7F7F7F7Fu;  // a row that is not scored: any finite scale
+      const int sq = (y.t0 + p.t_off) / p.q_per_seq;
+      return __ldg(reinterpret_cast<const uint32_t*>(p.k_sf + (int64_t)sq * p.k_sf_seq_stride + (int64_t)pos * 4));
+    };
+    auto q_word = [&](int t, int h) -> uint32_t {
+      if (h >= p.H_idx || t >= p.T) return 0x7F7F7F7Fu;  // padding heads meet zero weights
+      const uint8_t* q = p.q_sf + ((int64_t)t * p.H_idx + h) * 4;
+      return (uint32_t)q[0] | (uint32_t)q[1] << 8 | (uint32_t)q[2] << 16 | (uint32_t)q[3] << 24;
+    };
+    auto sf_write = [&]() {
+      const int slot = sf_n % C::ACC_BUFS;
+      if (sf_unit.t0 != sf_t) {
+        sf_t = sf_unit.t0;
+        sf_b0 = q_word(sf_t, lane);
+        sf_b1 = q_word(sf_t, 32 + lane);
+      }
+      const uint32_t addr = tmem + ((uint32_t)(q4 * 32) << 16) + C::SF_BASE + 16 * slot;
+      tmem_st_x4(addr, sf_a, sf_a, sf_a, sf_a);
+      tmem_st_x2(addr + 8, sf_b0, sf_b1);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sf_full[slot]);
+      ++sf_n;
+      sf_u = next_unit(sf_u, sf_unit);
+      if (sf_u < u_end) sf_a = sf_load_a(sf_unit);
+    };
+    if constexpr (MX) {
+      sf_u = next_unit(u_begin - 1, sf_unit);
+      if (sf_u < u_end) sf_a = sf_load_a(sf_unit);
+      for (int i = 0; i < C::ACC_BUFS && sf_u < u_end; ++i) sf_write();
     }
     // after a timed-out wait the epilogue warps keep walking the units (so that every named
     // barrier below is reached by every epilogue thread) but skip the waits and the tile work
@@ -347,23 +371,8 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
           const int j = i / NPAD, h = i % NPAD;
           const bool valid = h < p.H_idx && x.t0 + j < p.T;
           w_s[i] = valid ? p.w[(int64_t)(x.t0 + j) * p.H_idx + h] : 0.f;
-          if (MX) {
-#pragma unroll
-            for (int g = 0; g < C::GROUPS; ++g)
-              qs_s[g * (G * NPAD) + i] =
-                  valid ? e8m0_value(p.q_sf[((int64_t)(x.t0 + j) * p.H_idx + h) * C::GROUPS + g]) : 0.f;
-          }
         }
         epi_bar<ET>();
-      }
-      float ks[C::GROUPS];
-      if (MX) {
-        const uint32_t raw = raw_next;  // this unit's scales
-        Unit y;
-        const int un = next_unit(u, y);
-        if (un < u_end) raw_next = load_ks(y);
-#pragma unroll
-        for (int g = 0; g < C::GROUPS; ++g) ks[g] = e8m0_value((raw >> (8 * g)) & 0xFFu);
       }
       const int pos = x.tile * kTileM + row;
       const int ab = ai % C::ACC_BUFS;
@@ -376,38 +385,17 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
       for (int j = 0; j < QW; ++j) score[j] = 0.f;
       if (ok) {
         tc_fence_after();
+        // this slot's MMAs are complete: its scale slot takes the unit ACC_BUFS ahead
+        if (MX && sf_u < u_end) sf_write();
         const uint32_t tb = tmem + ((uint32_t)(q4 * 32) << 16) + ab * C::ACC_COLS;
-        // columns per TMEM load (16 for MXFP8, which keeps each load beside its running sums)
-        constexpr int CW = C::COLS < (MX ? 16 : 32) ? C::COLS : (MX ? 16 : 32);
+        constexpr int CW = C::COLS < 32 ? C::COLS : 32;  // columns per TMEM load
 #pragma unroll
         for (int c = 0; c < C::COLS / CW; ++c) {
           const int col = half * C::COLS + c * CW;  // first accumulator column of this load
           const int j = (c * CW) / NPAD;            // this warp's query the columns belong to
-          // columns in pairs: packed fp32x2 multiply-adds (same rounding as scalar fp32)
           float v[CW];
-          if (!MX) {
-            tmem_ld_sync(tb + col, v);
-          } else {
-            float2 acc[CW / 2];
-#pragma unroll
-            for (int i = 0; i < CW / 2; ++i) acc[i] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int g = 0; g < C::GROUPS; ++g) {
-              float d[CW];
-              tmem_ld_sync(tb + g * C::N + col, d);
-              const float2 k2 = make_float2(ks[g], ks[g]);
-              const float4* qv = reinterpret_cast<const float4*>(qs_s + g * (G * NPAD) + col);
-#pragma unroll
-              for (int i = 0; i < CW / 4; ++i) {
-                const float4 q4 = qv[i];
-                acc[2 * i] = ffma2(fmul2(k2, make_float2(q4.x, q4.y)), make_float2(d[4 * i], d[4 * i + 1]), acc[2 * i]);
-                acc[2 * i + 1] =
-                    ffma2(fmul2(k2, make_float2(q4.z, q4.w)), make_float2(d[4 * i + 2], d[4 * i + 3]), acc[2 * i + 1]);
-              }
-            }
-#pragma unroll
-            for (int i = 0; i < CW / 2; ++i) v[2 * i] = acc[i].x, v[2 * i + 1] = acc[i].y;
-          }
+          tmem_ld_sync(tb + col, v);
+          // columns in pairs: packed fp32x2 multiply-adds (same rounding as scalar fp32)
           float2 sc2 = make_float2(0.f, 0.f);
           const float4* wv = reinterpret_cast<const float4*>(w_s + col);
 #pragma unroll
@@ -518,8 +506,8 @@ cudaError_t launch_index_score(const void* q_idx, const void* k_idx, int64_t k_s
   if (hist_filled) *hist_filled = p.hist != nullptr;
   if (mx) {
     if (d_idx != 128) return cudaErrorNotSupported;
-    if (npad == 16) return launch_cfg<true, 128, 1, 16>(q_idx, k_idx, k_seq_stride, n_seq, p, stream, pdl);
-    if (npad == 32) return launch_cfg<true, 128, 1, 32>(q_idx, k_idx, k_seq_stride, n_seq, p, stream, pdl);
+    // block-scaled MMAs with N = 32 or 64 (fewer heads are padded to 32)
+    if (npad <= 32) return launch_cfg<true, 128, 1, 32>(q_idx, k_idx, k_seq_stride, n_seq, p, stream, pdl);
     return launch_cfg<true, 128, 1, 64>(q_idx, k_idx, k_seq_stride, n_seq, p, stream, pdl);
   }
   if (d_idx == 128) {
