@@ -10,10 +10,11 @@
 // lane = one position and all of its head columns, so ReLU, the head weights and (for MXFP8) the
 // per-group E8M0 scales are applied in registers with no cross-thread reduction.
 //
-// Warp roles: warp 0 = producer (TMA for A and B), warp 1 = TMEM owner and MMA issuer, warps
-// 2-5 = epilogue.  The four-query prefill tiles (N = 256) use 16 epilogue warps in four groups,
-// one query each.  A ring of shared-memory stages decouples loads from MMAs; up to four TMEM
-// accumulators let the epilogue trail the MMAs by several tiles.
+// Warp roles: warp 0 = producer (TMA for A and B), warp 1 = TMEM owner and MMA issuer, the rest
+// epilogue.  One-query tiles have two epilogue groups of four warps that take alternate tiles,
+// so two tiles' epilogues (TMEM loads, stores, histogram) overlap; the four-query prefill tiles
+// (N = 256) use four groups that split each tile by query.  A ring of shared-memory stages
+// decouples loads from MMAs; four TMEM accumulators let the epilogue trail the MMAs.
 // The grid is persistent: CTA c processes a contiguous range of (query group, tile) units.
 //
 // For the Top-K step, the epilogue also builds a histogram of the top 12 bits of each score's
@@ -66,38 +67,33 @@ struct Cfg {
   static constexpr int SF_COLS = MX ? 16 * ACC_BUFS : 0;
   static constexpr int TMEM_COLS = pow2_at_least(SF_BASE + SF_COLS);
   static constexpr int HIST_BYTES = G == 1 ? kHistBins * 4 : 0;  // fused score histogram
-  // epilogue warps: sixteen (four groups, one query each) for four queries per tile (N = 256)
-  static constexpr int EPI = G == 4 ? 16 : 4;
-  static constexpr int SPLITS = EPI / 4;      // column splits (each warp group covers all rows)
+  // epilogue groups of four warps (each group covers all 128 rows of a tile): SPLITS groups
+  // split a tile's columns by query, TG sets of them take alternate tiles
+  static constexpr int SPLITS = G;
+  static constexpr int TG = G == 1 ? 2 : 1;
+  static constexpr int EPI = 4 * SPLITS * TG;  // epilogue warps
   static constexpr int THREADS = 64 + 32 * EPI;
-  static constexpr int COLS = N / SPLITS;     // accumulator columns per epilogue warp
-  // the split falls between queries (each group scores its own queries) or between heads of one
-  // query (groups 1.. hand partial scores to group 0)
-  static constexpr bool QSPLIT = COLS % NPAD == 0;
-  static constexpr int PART_BYTES = QSPLIT ? 0 : 2 * (SPLITS - 1) * kTileM * 4;
-  static constexpr int AUX_BYTES = 1024 + 4096 + G * NPAD * 4 + HIST_BYTES + PART_BYTES;
+  static constexpr int COLS = N / SPLITS;     // accumulator columns per epilogue warp (= NPAD)
+  static constexpr int AUX_BYTES = 1024 + 4096 + G * NPAD * 4 + HIST_BYTES;
   static constexpr int STAGES_FIT = (kSmemBudget - B_BUFS * B_BYTES - AUX_BYTES) / A_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int OFF_B = STAGES * A_BYTES;
   static constexpr int OFF_BAR = OFF_B + B_BUFS * B_BYTES;
   static constexpr int OFF_W = OFF_BAR + 1024;
   static constexpr int OFF_HIST = OFF_W + G * NPAD * 4;
-  static constexpr int OFF_PART = OFF_HIST + HIST_BYTES;
-  static constexpr int SMEM = OFF_PART + PART_BYTES + 1024;  // + alignment slack
+  static constexpr int SMEM = OFF_HIST + HIST_BYTES + 1024;  // + alignment slack
   static_assert(N % 16 == 0 && N >= 16 && N <= 256, "MMA N out of range");
   static_assert(SF_BASE + SF_COLS <= 512, "accumulators exceed tensor memory");
   static_assert(!MX || (G == 1 && (N == 32 || N == 64) && GROUPS <= 4), "MXFP8 tile shape");
   static_assert(STAGES >= 2, "not enough shared memory for the pipeline");
   static_assert(ROW_BYTES % 128 == 0, "rows must fill whole swizzle atoms");
-  static_assert(QSPLIT || G == 1, "a head split needs one query per group");
+  static_assert(ACC_BUFS % TG == 0, "alternate tiles need an even number of accumulators");
   static_assert(COLS >= 8, "at least one 8-column TMEM load per warp");
 };
 
-// named barriers of the epilogue warps (ids 1 and 2; 0 is __syncthreads)
+// named barrier of the epilogue warps (id 1; 0 is __syncthreads)
 template <int THREADS>
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory"); }
-template <int THREADS>
-__device__ __forceinline__ void part_bar() { asm volatile("bar.sync 2, %0;" ::"n"(THREADS) : "memory"); }
 
 // Unit u -> (first query of its group, tile).  Returns false when the tile holds no position
 // visible to any query of the group.
@@ -159,8 +155,8 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     }
     for (int i = 0; i < C::ACC_BUFS; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], C::EPI);  // one arrival per epilogue warp
-      mbar_init(&sf_full[i], C::EPI);
+      mbar_init(&tempty[i], 4 * C::SPLITS);  // one arrival per warp that reads the tile
+      mbar_init(&sf_full[i], 4);              // one arrival per warp of the writing group
     }
     fence_mbar_init();
     prefetch_tmap(&tm_k);
@@ -288,10 +284,11 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     // ------------------------------------------------------------------ epilogue
     constexpr int ET = 32 * C::EPI;  // epilogue threads
     const int q4 = warp & 3;         // the TMEM lane quarter this warp may access
-    const int half = (warp - 2) >> 2;  // which column split of the accumulator this warp reads
+    const int grp = (warp - 2) >> 2;
+    const int half = grp % C::SPLITS;  // which query of the tile this warp scores
+    const int tg = grp / C::SPLITS;    // which of the alternate tiles this warp takes
     const int row = q4 * 32 + lane;
     const int et = threadIdx.x - 64;
-    float* part_s = reinterpret_cast<float*>(smem + C::OFF_PART);  // [2][SPLITS - 1][kTileM]
     int ai = 0, cur_t0 = -1;
     bool ok = true;
     // flushes the shared histogram of query t into the global one (non-zero bins only)
@@ -313,11 +310,11 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
       return u_end;
     };
     // MXFP8 scale writer.  The n-th visible unit's scale words go to slot n % ACC_BUFS, a full
-    // pipeline depth ahead of the accumulator the epilogue reads; a unit's key-scale word is
-    // loaded when the previous unit is written, so the global load overlaps a tile's epilogue.
-    // Each lane writes its lane of the warp's quarter: its row's four group exponents (byte g =
-    // group g) into the four A columns, and those of heads (lane) and (32 + lane) of the unit's
-    // query into the two B columns.
+    // pipeline depth ahead of the accumulator the epilogue reads, written by the group that takes
+    // that unit (n % TG); a unit's key-scale word is loaded when the group's previous unit is
+    // written, so the global load overlaps a tile's epilogue.  Each lane writes its lane of the
+    // warp's quarter: its row's four group exponents (byte g = group g) into the four A columns,
+    // and those of heads (lane) and (32 + lane) of the unit's query into the two B columns.
     Unit sf_unit = {0, 0, 0};
     int sf_u = u_end, sf_n = 0, sf_t = -1;
     uint32_t sf_a = 0, sf_b0 = 0, sf_b1 = 0;
@@ -331,6 +328,10 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
       if (h >= p.H_idx || t >= p.T) return 0x7F7F7F7Fu;  // padding heads meet zero weights
       const uint8_t* q = p.q_sf + ((int64_t)t * p.H_idx + h) * 4;
       return (uint32_t)q[0] | (uint32_t)q[1] << 8 | (uint32_t)q[2] << 16 | (uint32_t)q[3] << 24;
+    };
+    auto sf_step = [&]() {  // cursor to the next visible unit
+      sf_u = next_unit(sf_u, sf_unit);
+      ++sf_n;
     };
     auto sf_write = [&]() {
       const int slot = sf_n % C::ACC_BUFS;
@@ -346,14 +347,14 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sf_full[slot]);
-      ++sf_n;
-      sf_u = next_unit(sf_u, sf_unit);
+      for (int k = 0; k < C::TG && sf_u < u_end; ++k) sf_step();  // this group's next unit
       if (sf_u < u_end) sf_a = sf_load_a(sf_unit);
     };
     if constexpr (MX) {
       sf_u = next_unit(u_begin - 1, sf_unit);
+      for (int k = 0; k < tg && sf_u < u_end; ++k) sf_step();
       if (sf_u < u_end) sf_a = sf_load_a(sf_unit);
-      for (int i = 0; i < C::ACC_BUFS && sf_u < u_end; ++i) sf_write();
+      while (sf_u < u_end && sf_n < C::ACC_BUFS) sf_write();
     }
     // after a timed-out wait the epilogue warps keep walking the units (so that every named
     // barrier below is reached by every epilogue thread) but skip the waits and the tile work
@@ -374,15 +375,14 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         }
         epi_bar<ET>();
       }
+      if (ai % C::TG != tg) {  // the other group's tile
+        ++ai;
+        continue;
+      }
       const int pos = x.tile * kTileM + row;
       const int ab = ai % C::ACC_BUFS;
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&tfull[ab], (ai / C::ACC_BUFS) & 1, p.err));
-      // the queries this warp scores: its own group's with a query split, all G otherwise
-      constexpr int QW = C::QSPLIT ? C::COLS / NPAD : G;
-      const int j0 = C::QSPLIT ? half * QW : 0;
-      float score[QW];
-#pragma unroll
-      for (int j = 0; j < QW; ++j) score[j] = 0.f;
+      float score = 0.f;  // this warp's query: x.t0 + half
       if (ok) {
         tc_fence_after();
         // this slot's MMAs are complete: its scale slot takes the unit ACC_BUFS ahead
@@ -392,7 +392,6 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 #pragma unroll
         for (int c = 0; c < C::COLS / CW; ++c) {
           const int col = half * C::COLS + c * CW;  // first accumulator column of this load
-          const int j = (c * CW) / NPAD;            // this warp's query the columns belong to
           float v[CW];
           tmem_ld_sync(tb + col, v);
           // columns in pairs: packed fp32x2 multiply-adds (same rounding as scalar fp32)
@@ -404,32 +403,17 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             sc2 = ffma2(make_float2(w4.x, w4.y), make_float2(fmaxf(v[4 * i], 0.f), fmaxf(v[4 * i + 1], 0.f)), sc2);
             sc2 = ffma2(make_float2(w4.z, w4.w), make_float2(fmaxf(v[4 * i + 2], 0.f), fmaxf(v[4 * i + 3], 0.f)), sc2);
           }
-          score[j] += sc2.x + sc2.y;
+          score += sc2.x + sc2.y;
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[ab]);
-      }
-      if constexpr (!C::QSPLIT) {
-        // every epilogue thread meets this barrier once per unit, whatever happened to its waits
-        float* part = part_s + (ai & 1) * (C::SPLITS - 1) * kTileM;  // alternates per unit
-        if (half > 0) part[(half - 1) * kTileM + row] = score[0];
-        part_bar<ET>();
-        if (half == 0)
-#pragma unroll
-          for (int k = 0; k < C::SPLITS - 1; ++k) score[0] += part[k * kTileM + row];
-      }
-      // stores: each group its own queries with a query split, group 0 all of them otherwise
-      if (ok && (C::QSPLIT || half == 0)) {
-#pragma unroll
-        for (int j = 0; j < QW; ++j) {
-          const int t = x.t0 + j0 + j;
-          const bool vis = t < p.T && pos < visible_len(t + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid);
-          if (vis) p.scores[(int64_t)t * p.ld_scores + pos] = score[j];
-          // shared-memory atomics: lanes on the same bin serialise in the atomic unit, which costs
-          // far less than grouping them first with a warp match
-          if (build_hist && vis) atomicAdd(&hist_s[float_key(score[j]) >> 20], 1u);
-        }
+        const int t = x.t0 + half;
+        const bool vis = t < p.T && pos < visible_len(t + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid);
+        if (vis) p.scores[(int64_t)t * p.ld_scores + pos] = score;
+        // shared-memory atomics: lanes on the same bin serialise in the atomic unit, which costs
+        // far less than grouping them first with a warp match
+        if (build_hist && vis) atomicAdd(&hist_s[float_key(score) >> 20], 1u);
       }
       ++ai;
     }
