@@ -95,25 +95,48 @@ struct Cfg {
 template <int THREADS>
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory"); }
 
-// Unit u -> (first query of its group, tile).  Returns false when the tile holds no position
-// visible to any query of the group.
-struct Unit {
-  int t0, tile, n_max;
-};
-
+// Walks this CTA's (query group, tile) units u_begin .. u_end - 1 in order and stops at the ones
+// that hold a position visible to some query of the group.  Group facts (visible lengths, cache
+// sequence) are computed when the walk enters a group, so a step costs no division; the rest of
+// a group past its longest visible row is skipped at once.
 template <int G>
-__device__ __forceinline__ bool unit_of(const IndexScoreParams& p, int u, Unit& x) {
-  const int g = u / p.tiles;
-  x.tile = u - g * p.tiles;
-  x.t0 = g * G;
-  int n_max = 0;
+struct UnitWalk {
+  int u, u_end, g, tile, n_max, seq;
+  int n[G];  // visible length of each query of the group (0 past the last query)
+
+  __device__ __forceinline__ void enter_group(const IndexScoreParams& p) {
+    n_max = 0;
 #pragma unroll
-  for (int j = 0; j < G; ++j)
-    if (x.t0 + j < p.T)
-      n_max = max(n_max, visible_len(x.t0 + j + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid));
-  x.n_max = n_max;
-  return x.tile * kTileM < n_max;
-}
+    for (int j = 0; j < G; ++j) {
+      const int t = g * G + j;
+      n[j] = t < p.T ? visible_len(t + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid) : 0;
+      n_max = max(n_max, n[j]);
+    }
+    seq = (g * G + p.t_off) / p.q_per_seq;
+  }
+  __device__ __forceinline__ UnitWalk(const IndexScoreParams& p, int u_begin, int u_end_)
+      : u(u_begin - 1), u_end(u_end_) {
+    g = u_begin / p.tiles;
+    tile = u_begin - g * p.tiles - 1;  // one step before u_begin
+    enter_group(p);
+  }
+  // advances to the next visible unit; false when the range is done
+  __device__ __forceinline__ bool next(const IndexScoreParams& p) {
+    for (++u; u < u_end; ++u) {
+      if (++tile == p.tiles) {
+        tile = 0;
+        ++g;
+        enter_group(p);
+      }
+      if (tile * kTileM < n_max) return true;
+      const int rest = p.tiles - 1 - tile;  // the group's later tiles are not visible either
+      u += rest;
+      tile += rest;
+    }
+    return false;
+  }
+  __device__ __forceinline__ int t0() const { return g * G; }
+};
 
 template <bool MX, int D, int G, int NPAD>
 __global__ void __launch_bounds__(Cfg<MX, D, G, NPAD>::THREADS, 1)
@@ -181,11 +204,10 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     const uint64_t evict_first = l2_evict_first_policy();  // key tiles are read once
     int it = 0, qn = -1, cur_t0 = -1;
     bool ok = true;
-    for (int u = u_begin; u < u_end && ok; ++u) {
-      Unit x;
-      if (!unit_of<G>(p, u, x)) continue;
-      if (x.t0 != cur_t0) {
-        cur_t0 = x.t0;
+    UnitWalk<G> w(p, u_begin, u_end);
+    while (ok && w.next(p)) {
+      if (w.t0() != cur_t0) {
+        cur_t0 = w.t0();
         ++qn;
         const int bb = qn % C::B_BUFS;
         if (qn >= C::B_BUFS) ok = mbar_wait(&bempty[bb], ((qn - C::B_BUFS) / C::B_BUFS) & 1, p.err);
@@ -199,7 +221,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             mbar_arrive_expect_tx(&bfull[bb], C::B_BYTES);
 #pragma unroll
             for (int b = 0; b < C::BOXES; ++b)
-              tma_load_2d(bdst + b * (C::N * 128), &tm_q, &bfull[bb], b * C::BOX_COLS, x.t0 * p.H_idx);
+              tma_load_2d(bdst + b * (C::N * 128), &tm_q, &bfull[bb], b * C::BOX_COLS, w.t0() * p.H_idx);
           }
           __syncwarp();
         } else {
@@ -210,8 +232,8 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             const int r = i / CH, c = i % CH;
             const int j = r / NPAD, h = r % NPAD;
             uint4 v = make_uint4(0, 0, 0, 0);
-            if (h < p.H_idx && x.t0 + j < p.T)
-              v = *reinterpret_cast<const uint4*>(q_idx + ((int64_t)(x.t0 + j) * p.H_idx + h) * C::ROW_BYTES + c * 16);
+            if (h < p.H_idx && w.t0() + j < p.T)
+              v = *reinterpret_cast<const uint4*>(q_idx + ((int64_t)(w.t0() + j) * p.H_idx + h) * C::ROW_BYTES + c * 16);
             const int box = c >> 3, cc = c & 7;
             *reinterpret_cast<uint4*>(bdst + box * (C::N * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
           }
@@ -226,11 +248,10 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
       if (!ok) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(&full[s], C::A_BYTES);
-        const int seq = (x.t0 + p.t_off) / p.q_per_seq;
 #pragma unroll
         for (int b = 0; b < C::BOXES; ++b)
           tma_load_3d_hint(a_s + s * C::A_BYTES + b * (kTileM * 128), &tm_k, &full[s], b * C::BOX_COLS,
-                           x.tile * kTileM, seq, evict_first);
+                           w.tile * kTileM, w.seq, evict_first);
       }
       __syncwarp();
       ++it;
@@ -240,12 +261,11 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     constexpr uint32_t idesc = make_idesc(1, 1, kTileM, C::N);
     int it = 0, qn = -1, cur_t0 = -1, ai = 0;
     bool ok = true;
-    for (int u = u_begin; u < u_end && ok; ++u) {
-      Unit x;
-      if (!unit_of<G>(p, u, x)) continue;
-      if (x.t0 != cur_t0) {
+    UnitWalk<G> w(p, u_begin, u_end);
+    while (ok && w.next(p)) {
+      if (w.t0() != cur_t0) {
         if (qn >= 0 && lane == 0) tc_commit(&bempty[qn % C::B_BUFS]);
-        cur_t0 = x.t0;
+        cur_t0 = w.t0();
         ++qn;
         ok = __all_sync(0xffffffffu, mbar_wait(&bfull[qn % C::B_BUFS], (qn / C::B_BUFS) & 1, p.err));
         if (!ok) break;
@@ -303,26 +323,20 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     };
     if (build_hist)
       for (int b = et; b < kHistBins; b += ET) hist_s[b] = 0;
-    // the next visible unit after u (u_end when none)
-    auto next_unit = [&](int u, Unit& y) -> int {
-      for (++u; u < u_end; ++u)
-        if (unit_of<G>(p, u, y)) return u;
-      return u_end;
-    };
     // MXFP8 scale writer.  The n-th visible unit's scale words go to slot n % ACC_BUFS, a full
     // pipeline depth ahead of the accumulator the epilogue reads, written by the group that takes
     // that unit (n % TG); a unit's key-scale word is loaded when the group's previous unit is
     // written, so the global load overlaps a tile's epilogue.  Each lane writes its lane of the
     // warp's quarter: its row's four group exponents (byte g = group g) into the four A columns,
     // and those of heads (lane) and (32 + lane) of the unit's query into the two B columns.
-    Unit sf_unit = {0, 0, 0};
-    int sf_u = u_end, sf_n = 0, sf_t = -1;
+    UnitWalk<G> sfw(p, u_begin, u_end);
+    bool sf_more = false;
+    int sf_n = 0, sf_t = -1;
     uint32_t sf_a = 0, sf_b0 = 0, sf_b1 = 0;
-    auto sf_load_a = [&](const Unit& y) -> uint32_t {
-      const int pos = y.tile * kTileM + row;
-      if (pos >= y.n_max) return 0x7F7F7F7Fu;  // a row that is not scored: any finite scale
-      const int sq = (y.t0 + p.t_off) / p.q_per_seq;
-      return __ldg(reinterpret_cast<const uint32_t*>(p.k_sf + (int64_t)sq * p.k_sf_seq_stride + (int64_t)pos * 4));
+    auto sf_load_a = [&]() -> uint32_t {
+      const int pos = sfw.tile * kTileM + row;
+      if (pos >= sfw.n_max) return 0x7F7F7F7Fu;  // a row that is not scored: any finite scale
+      return __ldg(reinterpret_cast<const uint32_t*>(p.k_sf + (int64_t)sfw.seq * p.k_sf_seq_stride + (int64_t)pos * 4));
     };
     auto q_word = [&](int t, int h) -> uint32_t {
       if (h >= p.H_idx || t >= p.T) return 0x7F7F7F7Fu;  // padding heads meet zero weights
@@ -330,13 +344,13 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
       return (uint32_t)q[0] | (uint32_t)q[1] << 8 | (uint32_t)q[2] << 16 | (uint32_t)q[3] << 24;
     };
     auto sf_step = [&]() {  // cursor to the next visible unit
-      sf_u = next_unit(sf_u, sf_unit);
+      sf_more = sfw.next(p);
       ++sf_n;
     };
     auto sf_write = [&]() {
       const int slot = sf_n % C::ACC_BUFS;
-      if (sf_unit.t0 != sf_t) {
-        sf_t = sf_unit.t0;
+      if (sfw.t0() != sf_t) {
+        sf_t = sfw.t0();
         sf_b0 = q_word(sf_t, lane);
         sf_b1 = q_word(sf_t, 32 + lane);
       }
@@ -347,31 +361,30 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sf_full[slot]);
-      for (int k = 0; k < C::TG && sf_u < u_end; ++k) sf_step();  // this group's next unit
-      if (sf_u < u_end) sf_a = sf_load_a(sf_unit);
+      for (int k = 0; k < C::TG && sf_more; ++k) sf_step();  // this group's next unit
+      if (sf_more) sf_a = sf_load_a();
     };
     if constexpr (MX) {
-      sf_u = next_unit(u_begin - 1, sf_unit);
-      for (int k = 0; k < tg && sf_u < u_end; ++k) sf_step();
-      if (sf_u < u_end) sf_a = sf_load_a(sf_unit);
-      while (sf_u < u_end && sf_n < C::ACC_BUFS) sf_write();
+      sf_more = sfw.next(p);
+      for (int k = 0; k < tg && sf_more; ++k) sf_step();
+      if (sf_more) sf_a = sf_load_a();
+      while (sf_more && sf_n < C::ACC_BUFS) sf_write();
     }
     // after a timed-out wait the epilogue warps keep walking the units (so that every named
     // barrier below is reached by every epilogue thread) but skip the waits and the tile work
-    for (int u = u_begin; u < u_end; ++u) {
-      Unit x;
-      if (!unit_of<G>(p, u, x)) continue;
-      if (x.t0 != cur_t0) {
+    UnitWalk<G> w(p, u_begin, u_end);
+    while (w.next(p)) {
+      if (w.t0() != cur_t0) {
         epi_bar<ET>();
         if (build_hist && cur_t0 >= 0) {
           flush_hist(cur_t0);
           epi_bar<ET>();
         }
-        cur_t0 = x.t0;
+        cur_t0 = w.t0();
         for (int i = et; i < G * NPAD; i += ET) {
           const int j = i / NPAD, h = i % NPAD;
-          const bool valid = h < p.H_idx && x.t0 + j < p.T;
-          w_s[i] = valid ? p.w[(int64_t)(x.t0 + j) * p.H_idx + h] : 0.f;
+          const bool valid = h < p.H_idx && w.t0() + j < p.T;
+          w_s[i] = valid ? p.w[(int64_t)(w.t0() + j) * p.H_idx + h] : 0.f;
         }
         epi_bar<ET>();
       }
@@ -379,14 +392,14 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         ++ai;
         continue;
       }
-      const int pos = x.tile * kTileM + row;
+      const int pos = w.tile * kTileM + row;
       const int ab = ai % C::ACC_BUFS;
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&tfull[ab], (ai / C::ACC_BUFS) & 1, p.err));
-      float score = 0.f;  // this warp's query: x.t0 + half
+      float score = 0.f;  // this warp's query: the group's query `half`
       if (ok) {
         tc_fence_after();
         // this slot's MMAs are complete: its scale slot takes the unit ACC_BUFS ahead
-        if (MX && sf_u < u_end) sf_write();
+        if (MX && sf_more) sf_write();
         const uint32_t tb = tmem + ((uint32_t)(q4 * 32) << 16) + ab * C::ACC_COLS;
         constexpr int CW = C::COLS < 32 ? C::COLS : 32;  // columns per TMEM load
 #pragma unroll
@@ -408,9 +421,8 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[ab]);
-        const int t = x.t0 + half;
-        const bool vis = t < p.T && pos < visible_len(t + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid);
-        if (vis) p.scores[(int64_t)t * p.ld_scores + pos] = score;
+        const bool vis = pos < w.n[half];  // zero past the last query
+        if (vis) p.scores[(int64_t)(w.t0() + half) * p.ld_scores + pos] = score;
         // shared-memory atomics: lanes on the same bin serialise in the atomic unit, which costs
         // far less than grouping them first with a warp match
         if (build_hist && vis) atomicAdd(&hist_s[float_key(score) >> 20], 1u);
