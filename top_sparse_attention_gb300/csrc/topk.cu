@@ -718,15 +718,37 @@ __global__ void __launch_bounds__(kThreads) topk_wide_scan_kernel(const TopkPara
   }
 }
 
+// Adds 1 to arr[idx] for every lane with pred; a warp whose predicated lanes share one index adds
+// them with a single atomic (equal keys and long same-chunk runs do not serialise on one
+// address).  Every lane of the warp must call it.
+__device__ __forceinline__ void warp_count(uint32_t* arr, uint32_t idx, bool pred) {
+  const uint32_t m = __ballot_sync(0xffffffffu, pred);
+  if (!m) return;
+  const int first = __ffs(m) - 1;
+  const uint32_t i0 = __shfl_sync(0xffffffffu, idx, first);
+  if (__all_sync(0xffffffffu, !pred || idx == i0)) {
+    if ((threadIdx.x & 31) == first) atomicAdd(&arr[i0], (uint32_t)__popc(m));
+  } else if (pred) {
+    atomicAdd(&arr[idx], 1u);
+  }
+}
+
+constexpr int kStash = 2048;  // candidates that share the first 22 bits of T, kept in shared memory
+
 __global__ void __launch_bounds__(kThreads) topk_wide_resolve_kernel(const TopkParams p) {
   __shared__ uint32_t h2[kLevelBins];
   __shared__ uint32_t sc[256];
-  __shared__ uint32_t gt_c[kWideMaxChunks];
-  __shared__ uint32_t eq_c[kWideMaxChunks];
+  __shared__ uint32_t off_c[kWideMaxChunks + 1];  // first flattened candidate of each chunk
+  __shared__ uint32_t gt_c[kWideMaxChunks];       // per chunk: candidates above T
+  __shared__ uint32_t eq_c[kWideMaxChunks];       // per chunk: keys equal to T
+  __shared__ uint2 stash[kStash];                 // (chunk, key) of the candidates in T's 22-bit bin
   pdl_launch_dependents();
   const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nch = p.wide_nch;
 #pragma unroll
   for (int k = 0; k < kBins1; ++k) h2[kBins1 * tid + k] = 0;
+  for (int c = tid; c < kWideMaxChunks; c += kThreads) gt_c[c] = eq_c[c] = 0;
+  if (tid == 0) sc[kScCand] = 0;
   pdl_wait();
   const int n = visible_len(t + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid);
   const WideRow w = wide_row(p, t);
@@ -736,13 +758,15 @@ __global__ void __launch_bounds__(kThreads) topk_wide_resolve_kernel(const TopkP
         reinterpret_cast<uint4*>(w.gh0)[b] = make_uint4(0u, 0u, 0u, 0u);
     return;
   }
-  uint32_t above, kr = (uint32_t)p.K;
-  uint32_t c0[kBins0];
+  // all loads of the row's small data at once: histograms and this thread's chunk counts
+  uint32_t c0[kBins0], c1[kBins1];
   load_bins<kBins0>(w.gh0, c0);
+  load_bins<kBins1>(w.gh1, c1);
+  const uint32_t above_b0 = tid < nch ? __ldcg(w.chunk + 4 * tid) : 0u;
+  const uint32_t cand = tid < nch ? __ldcg(w.chunk + 4 * tid + 1) : 0u;
+  uint32_t above, kr = (uint32_t)p.K;
   const uint32_t b0 = find_digit<kBins0>(c0, kr, sc, &above);
   kr -= above;
-  uint32_t c1[kBins1];
-  load_bins<kBins1>(w.gh1, c1);
   const uint32_t d1 = find_digit<kBins1>(c1, kr, sc, &above);
   kr -= above;
   const uint32_t p22 = (b0 << 10) | d1;  // the first 22 bits of T
@@ -751,49 +775,76 @@ __global__ void __launch_bounds__(kThreads) topk_wide_resolve_kernel(const TopkP
     reinterpret_cast<uint4*>(w.gh0)[b] = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
   for (int k = 0; k < kBins1; ++k) w.gh1[kBins1 * tid + k] = 0;
+  uint64_t total;
+  const uint64_t ex = block_excl_scan(cand, sc, &total);
+  if (tid < nch) off_c[tid] = (uint32_t)ex;
+  if (tid == 0) off_c[nch] = (uint32_t)total;
+  __syncthreads();
+  const uint32_t n_cand = (uint32_t)total;
 
-  // level 2 over the candidates that share p22, one warp per chunk list
-  const int nch = p.wide_nch;
-  for (int c = warp; c < nch; c += kWarps) {
-    const uint32_t m = __ldcg(w.chunk + 4 * c + 1);
-    const uint2* list = w.lists + (int64_t)c * p.wide_chunk;
-    for (uint32_t j = lane; j < m; j += 32) {
-      const uint32_t key = __ldcg(list + j).x;
-      if ((key >> 10) == p22) atomicAdd(&h2[key & (kLevelBins - 1)], 1u);
+  // candidate i of the flattened lists: its chunk (binary search over off_c) and its key
+  auto cand_key = [&](uint32_t i, uint32_t* c_out) -> uint32_t {
+    int lo = 0, hi = nch - 1;  // largest c with off_c[c] <= i
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (off_c[mid] <= i) lo = mid;
+      else hi = mid - 1;
+    }
+    *c_out = (uint32_t)lo;
+    return __ldcg(&w.lists[(int64_t)lo * p.wide_chunk + (i - off_c[lo])].x);
+  };
+
+  // level 2 over the candidates in T's 22-bit bin; candidates above that bin count for their
+  // chunk now; the bin's candidates are stashed for the per-chunk counts
+  for (uint32_t base = (uint32_t)warp * 32; base < n_cand; base += kThreads) {
+    const uint32_t i = base + lane;
+    uint32_t c = 0, key = 0;
+    if (i < n_cand) key = cand_key(i, &c);
+    const bool in_bin = i < n_cand && (key >> 10) == p22;
+    warp_count(gt_c, c, i < n_cand && (key >> 10) > p22);
+    hist_add(h2, in_bin ? (key & (kLevelBins - 1)) : kNoBin);
+    const uint32_t m = __ballot_sync(0xffffffffu, in_bin);
+    if (m) {
+      uint32_t at = 0;
+      if (lane == 0) at = atomicAdd(&sc[kScCand], (uint32_t)__popc(m));
+      at = __shfl_sync(0xffffffffu, at, 0) + __popc(m & ((1u << lane) - 1u));
+      if (in_bin && at < kStash) stash[at] = make_uint2(c, key);
     }
   }
   __syncthreads();
+  const uint32_t n_bin = sc[kScCand];
 #pragma unroll
   for (int k = 0; k < kBins1; ++k) c1[k] = h2[kBins1 * tid + k];
   const uint32_t d2 = find_digit<kBins1>(c1, kr, sc, &above);
   kr -= above;  // ties to take
   const uint32_t T = (p22 << 10) | d2;
 
-  // per chunk: keys above T (above b0, plus candidates above T) and keys equal to T
-  for (int c = warp; c < nch; c += kWarps) {
-    const uint32_t m = __ldcg(w.chunk + 4 * c + 1);
-    const uint2* list = w.lists + (int64_t)c * p.wide_chunk;
-    uint32_t g = 0, q = 0;
-    for (uint32_t j = lane; j < m; j += 32) {
-      const uint32_t key = __ldcg(list + j).x;
-      g += key > T;
-      q += key == T;
+  // per chunk: bin candidates above T and keys equal to T (from the stash, or the lists again
+  // when the bin held more than the stash)
+  if (n_bin <= (uint32_t)kStash) {
+    for (uint32_t base = (uint32_t)warp * 32; base < n_bin; base += kThreads) {
+      const uint32_t i = base + lane;
+      const uint2 e = i < n_bin ? stash[i] : make_uint2(0u, 0u);
+      warp_count(gt_c, e.x, i < n_bin && e.y > T);
+      warp_count(eq_c, e.x, i < n_bin && e.y == T);
     }
-    g = __reduce_add_sync(0xffffffffu, g);
-    q = __reduce_add_sync(0xffffffffu, q);
-    if (lane == 0) {
-      gt_c[c] = g + __ldcg(w.chunk + 4 * c);
-      eq_c[c] = q;
+  } else {
+    for (uint32_t base = (uint32_t)warp * 32; base < n_cand; base += kThreads) {
+      const uint32_t i = base + lane;
+      uint32_t c = 0, key = 0;
+      if (i < n_cand) key = cand_key(i, &c);
+      const bool in_bin = i < n_cand && (key >> 10) == p22;
+      warp_count(gt_c, c, in_bin && key > T);
+      warp_count(eq_c, c, in_bin && key == T);
     }
   }
   __syncthreads();
   // exclusive prefixes over the chunks (one chunk per thread; both sums stay below 2^32)
-  const uint64_t v = tid < nch ? ((uint64_t)eq_c[tid] << 32) | gt_c[tid] : 0ull;
-  uint64_t tot;
-  const uint64_t ex = block_excl_scan(v, sc, &tot);
+  const uint64_t v = tid < nch ? ((uint64_t)eq_c[tid] << 32) | (gt_c[tid] + above_b0) : 0ull;
+  const uint64_t exc = block_excl_scan(v, sc, &total);
   if (tid < nch) {
-    w.chunk[4 * tid + 2] = (uint32_t)ex;
-    w.chunk[4 * tid + 3] = (uint32_t)(ex >> 32);
+    w.chunk[4 * tid + 2] = (uint32_t)exc;
+    w.chunk[4 * tid + 3] = (uint32_t)(exc >> 32);
   }
   if (tid == 0) {
     w.row[0] = T;
