@@ -402,29 +402,47 @@ sparse_attn_kernel(const SparseAttnParams p) {
 }
 
 // Merges split partials: out = sum_j 2^(m_j - M) o_j / sum_j 2^(m_j - M) l_j and
-// lse = (M + log2 sum_j 2^(m_j - M) l_j) * ln 2.  One CTA per (query, head).
+// lse = (M + log2 sum_j 2^(m_j - M) l_j) * ln 2.  One CTA per (query, head); each thread owns four
+// value columns.  The partials are read eight splits per batch (all loads of a batch in flight
+// at once) and merged with an online rescale, so a batch costs one memory round trip.
 template <int DV>
 __global__ void __launch_bounds__(DV / 4) lse_combine_kernel(const SparseAttnParams p) {
   pdl_launch_dependents();
   pdl_wait();
+  constexpr int kBatch = 8;
   const int t = blockIdx.x, h = blockIdx.y;
   const int64_t row = ((int64_t)t * p.H + h) * p.splits;
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + row;
-  float M = -INFINITY;
-  for (int j = 0; j < p.splits; ++j) M = fmaxf(M, ml[j].x);
-  const float Mu = (M == -INFINITY) ? 0.f : M;
-  float lsum = 0.f;
-  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
   const int c = threadIdx.x * 4;
-  for (int j = 0; j < p.splits; ++j) {
-    const float2 mlj = ml[j];
-    const float wj = exp2f(mlj.x - Mu);
-    lsum += wj * mlj.y;
-    const float4 v = *reinterpret_cast<const float4*>(p.part_o + (row + j) * DV + c);
-    o.x += wj * v.x;
-    o.y += wj * v.y;
-    o.z += wj * v.z;
-    o.w += wj * v.w;
+  float M = -INFINITY, lsum = 0.f;
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j0 = 0; j0 < p.splits; j0 += kBatch) {
+    float2 mlb[kBatch];
+    float4 ob[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const bool in = j0 + k < p.splits;
+      mlb[k] = in ? ml[j0 + k] : make_float2(-INFINITY, 0.f);
+      ob[k] = in ? *reinterpret_cast<const float4*>(p.part_o + (row + j0 + k) * DV + c)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float Mb = M;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) Mb = fmaxf(Mb, mlb[k].x);
+    const float Mu = (Mb == -INFINITY) ? 0.f : Mb;
+    const float a = exp2f(M - Mu);  // rescales what the earlier batches gave (0 when empty)
+    lsum *= a;
+    o.x *= a, o.y *= a, o.z *= a, o.w *= a;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const float wj = exp2f(mlb[k].x - Mu);
+      lsum += wj * mlb[k].y;
+      o.x += wj * ob[k].x;
+      o.y += wj * ob[k].y;
+      o.z += wj * ob[k].z;
+      o.w += wj * ob[k].w;
+    }
+    M = Mb;
   }
   const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
   __nv_bfloat16* out = p.out + ((int64_t)t * p.H + h) * DV + c;
