@@ -186,6 +186,15 @@ def test_topk_row_split_workspace_reuse(dsa):
             assert np.array_equal(want, idx[t]), f"rep={rep} t={t}"
 
 
+def test_topk_uncached_cluster_rows(dsa):
+    # more rows than the row-split path takes (T > 32): 16-CTA clusters whose slices exceed the
+    # shared-memory key cache re-read their keys from L2
+    rng = np.random.default_rng(25)
+    s = (rng.standard_normal((33, 270001)) * 30 + 140).astype(np.float32)
+    s[5] = np.round(s[5] / 8) * 8  # heavy ties in one row
+    _topk_case(dsa, s, 2048, 270001)
+
+
 def test_topk_causal_rows(dsa):
     rng = np.random.default_rng(15)
     s = rng.standard_normal((6, 2600)).astype(np.float32)
