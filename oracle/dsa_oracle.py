@@ -36,6 +36,7 @@ import numpy as np
 
 __all__ = [
     "bf16_bits_to_f64", "e4m3_to_f64", "e8m0_to_f64", "dequant_mxfp8", "dequant_fp8_rows",
+    "e4m3_encode", "quantize_mxfp8", "quantize_fp8_rows",
     "index_scores", "topk_positions", "sparse_attention", "visible_length", "query_sequence",
     "Chain", "chain_query",
 ]
@@ -90,6 +91,99 @@ def dequant_mxfp8(codes, sf, group: int = 32) -> np.ndarray:
 def dequant_fp8_rows(codes, row_scale) -> np.ndarray:
     """FP8 E4M3 cache rows with one fp32 scale per row (token) -> fp64."""
     return e4m3_to_f64(codes) * np.asarray(row_scale, dtype=np.float64)[..., None]
+
+
+# ----------------------------------------------------------------------------------------------
+# Values -> stored formats: the online quantisation that writes the caches
+# (Day 0 Support for New LLM Architectures, Key Optimization 2: the indexer stores MXFP8 -- E4M3
+#  elements, one shared power-of-two scale per group of 32 -- and the sparse-attention KV cache
+#  stores FP8.  The group scale follows the OCP Microscaling Formats specification v1.0: the
+#  shared exponent is floor(log2(amax)) minus the element format's largest exponent, 8 for E4M3.)
+
+_E4M3_MAX = 448.0  # S.1111.110, the largest finite E4M3 value
+
+
+def e4m3_encode(values) -> np.ndarray:
+    """Values (fp64; exactly representable) -> E4M3 ('fn') codes, rounding to the nearest
+    representable value with ties to the even code and saturating to +-448 (no NaN produced).
+
+    Magnitudes below 2^-6 use the subnormal step 2^-9; a magnitude a >= 2^-6 with binary exponent
+    E = floor(log2 a) uses the step 2^(E-3) (three mantissa bits).  The sign is kept, so values
+    that round to zero from below give the negative zero code 0x80.
+    """
+    v = np.asarray(values, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint8)
+    flat_v, flat_o = v.reshape(-1), out.reshape(-1)
+    for i, x in enumerate(flat_v):
+        if math.isnan(x):
+            raise ValueError("NaN cannot be encoded")
+        sign = 0x80 if math.copysign(1.0, x) < 0 else 0
+        a = abs(x)
+        if a >= _E4M3_MAX:
+            code = 0x7E
+        elif a < 2.0 ** -6:
+            m = _round_half_even(a / 2.0 ** -9)  # 0..8; 8 is the smallest normal, code 0x08
+            code = m
+        else:
+            e = math.floor(math.log2(a))
+            # log2 of a value just below a power of two can round up: correct the exponent
+            if 2.0 ** e > a:
+                e -= 1
+            elif 2.0 ** (e + 1) <= a:
+                e += 1
+            r = _round_half_even(a / 2.0 ** (e - 3))  # 8..16
+            if r == 16:
+                e, r = e + 1, 8
+            code = ((e + 7) << 3) | (r - 8)
+            code = min(code, 0x7E)
+        flat_o[i] = sign | code
+    return out
+
+
+def _round_half_even(q: float) -> int:
+    f = math.floor(q)
+    d = q - f
+    if d > 0.5 or (d == 0.5 and f % 2 == 1):
+        return int(f) + 1
+    return int(f)
+
+
+def quantize_mxfp8(x, group: int = 32):
+    """Rows of values (fp64, last axis a multiple of `group`) -> (E4M3 codes, E8M0 exponents).
+
+    For each group of 32: amax = max |x|; shared exponent X = floor(log2 amax) - 8, clamped to
+    E8M0's range [-127, 127] (0 for an all-zero group); the exponent byte is X + 127 and each
+    element is e4m3_encode(x / 2^X).  Dividing by a power of two is exact.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    *lead, d = x.shape
+    if d % group:
+        raise ValueError("row length must be a multiple of the group size")
+    g = x.reshape(*lead, d // group, group)
+    amax = np.max(np.abs(g), axis=-1)
+    exps = np.zeros(amax.shape, dtype=np.int64)
+    nz = amax > 0
+    exps[nz] = np.floor(np.log2(amax[nz])).astype(np.int64)
+    # the same exact correction as in e4m3_encode
+    too_big = nz & (np.ldexp(1.0, exps) > amax)
+    exps[too_big] -= 1
+    too_small = nz & (np.ldexp(1.0, exps + 1) <= amax)
+    exps[too_small] += 1
+    shared = np.where(nz, np.clip(exps - 8, -127, 127), 0)
+    codes = e4m3_encode(g / np.ldexp(1.0, shared)[..., None]).reshape(*lead, d)
+    return codes, (shared + 127).astype(np.uint8)
+
+
+def quantize_fp8_rows(x):
+    """Rows of values (exact in fp32) -> (E4M3 codes, fp32 scale per row), computed in fp32:
+    s = amax / 448 rounded to fp32 (1 for an all-zero row) and codes = e4m3_encode of the fp32
+    quotient x / s.  The quotient is not exact, so it is formed in the precision the cache
+    writer uses (IEEE fp32 division, round to nearest)."""
+    x32 = np.asarray(x, dtype=np.float64).astype(np.float32)
+    amax = np.max(np.abs(x32), axis=-1)
+    s = np.where(amax > 0, amax / np.float32(_E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    q = (x32 / s[..., None]).astype(np.float32)
+    return e4m3_encode(q.astype(np.float64)), s
 
 
 # ----------------------------------------------------------------------------------------------

@@ -114,6 +114,88 @@ def test_synth_encoders_roundtrip_through_oracle_decoders():
 
 
 # ------------------------------------------------------------------------------------------------
+# online quantisation (the cache writer): values -> stored formats
+
+
+def test_e4m3_encode_round_trips_every_code():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    np.testing.assert_array_equal(oracle.e4m3_encode(oracle.e4m3_to_f64(codes)), codes)
+
+
+def test_e4m3_encode_matches_torch_cast_on_random_values_and_ties():
+    rng = np.random.default_rng(7)
+    pos = np.sort(oracle.e4m3_to_f64(np.arange(0, 0x7F, dtype=np.uint8)))
+    mids = (pos[:-1] + pos[1:]) / 2  # exact midpoints between neighbouring codes: ties to even
+    x = np.concatenate([rng.uniform(-440, 440, 4000), rng.standard_normal(4000),
+                        rng.standard_normal(2000) * 2.0 ** -8, mids, -mids]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(oracle.e4m3_encode(x.astype(np.float64)), ref)
+
+
+def test_e4m3_encode_saturates_and_keeps_the_sign_of_zero():
+    got = oracle.e4m3_encode([448.0, 449.0, 464.0, 500.0, 1e9, -1e9, -0.0, -2.0 ** -11, 2.0 ** -11])
+    np.testing.assert_array_equal(got, [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0x80, 0x80, 0x00])
+
+
+def test_online_quant_hand_worked():
+    g = _golden("hand_worked_online_quant.json")
+    codes, sf = oracle.quantize_mxfp8(np.array(g["mx_groups"]).reshape(1, -1))
+    np.testing.assert_array_equal(sf[0], g["expect_mx_sf"])
+    np.testing.assert_array_equal(codes.reshape(4, 32)[:, :4], g["expect_mx_codes_first4"])
+    assert np.all(codes.reshape(4, 32)[:, 4:] == 0)
+    codes, s = oracle.quantize_fp8_rows(np.array(g["fp8_rows"]))
+    np.testing.assert_array_equal(s[:2], g["expect_fp8_scales_exact"])
+    assert s[2] == np.float32(3.0) / np.float32(448.0)
+    np.testing.assert_array_equal(codes, g["expect_fp8_codes"])
+
+
+def _torch_mxfp8(x64):
+    """The same OCP MX rule from torch primitives: frexp for the exponent, the float8 cast for
+    the elements (after saturating to 448)."""
+    x = torch.from_numpy(x64).reshape(x64.shape[0], -1, 32)
+    amax = x.abs().amax(-1)
+    _, e = torch.frexp(amax)  # amax = m * 2^e, m in [0.5, 1): floor(log2 amax) = e - 1
+    shared = torch.where(amax > 0, (e - 1 - 8).clamp(-127, 127), torch.zeros_like(e))
+    scaled = torch.ldexp(x, -shared[..., None].to(torch.float64)).clamp(-448, 448)
+    codes = scaled.to(torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).reshape(x64.shape)
+    return codes.numpy(), (shared + 127).to(torch.uint8).numpy()
+
+
+def test_quantize_mxfp8_matches_torch_and_scales_by_powers_of_two():
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((64, 128)) * np.ldexp(1.0, rng.integers(-30, 30, (64, 4))).repeat(32, 1)
+    x = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()  # bf16 inputs, as cached
+    x[3, 32:64] = 0.0  # an all-zero group
+    codes, sf = oracle.quantize_mxfp8(x)
+    tc, tsf = _torch_mxfp8(x)
+    np.testing.assert_array_equal(codes, tc)
+    np.testing.assert_array_equal(sf, tsf)
+    assert sf[3, 1] == 127 and np.all(codes[3, 32:64] == 0)
+    # scaling a group by 2^k moves its exponent byte by k and leaves the element codes alone
+    c2, s2 = oracle.quantize_mxfp8(x * 8.0)
+    np.testing.assert_array_equal(c2, codes)
+    np.testing.assert_array_equal(s2.astype(int) - sf.astype(int), np.where(sf == 127, np.where(np.abs(x).reshape(64, 4, 32).max(-1) > 0, 3, 0), 3))
+    # dequantised error: E4M3 rounding (half a step, <= amax / 32) or saturation (< amax / 8)
+    back = oracle.dequant_mxfp8(codes, sf)
+    amax = np.abs(x).reshape(64, 4, 32).max(-1).repeat(32, 1)
+    assert np.all(np.abs(back - x) <= amax / 8 + 1e-300)
+
+
+def test_quantize_fp8_rows_matches_torch_fp32():
+    rng = np.random.default_rng(9)
+    x = torch.from_numpy(rng.standard_normal((50, 576)) * np.ldexp(1.0, rng.integers(-10, 10, (50, 1))))
+    x = x.to(torch.bfloat16).to(torch.float32)
+    x[7] = 0.0
+    codes, s = oracle.quantize_fp8_rows(x.double().numpy())
+    amax = x.abs().amax(-1)
+    ts = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    tq = (x / ts[:, None]).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+    np.testing.assert_array_equal(s, ts.numpy())
+    np.testing.assert_array_equal(codes, tq.numpy())
+    assert s[7] == 1.0 and np.all(codes[7] == 0)
+
+
+# ------------------------------------------------------------------------------------------------
 # indexer scores
 
 
