@@ -176,19 +176,13 @@ def quantize_mxfp8(x, group: int = 32):
 
 def quantize_fp8_rows(x):
     """Rows of values (exact in fp32) -> (E4M3 codes, fp32 scale per row), computed in fp32:
-    the stored scale is s = amax / 448 rounded to fp32 (1 for an all-zero row); the codes are
-    e4m3_encode(x * r) with r = 448 / amax rounded to fp32 (r = 1 for an all-zero row), one
-    rounded fp32 product per element.  The pages fix only the per-row fp32 scale; forming the
-    codes with the row's reciprocal (one division per row) is the reading taken.  The product is
-    not exact, so it is formed in the precision the cache writer uses (IEEE fp32, round to
-    nearest)."""
+    s = amax / 448 rounded to fp32 (1 for an all-zero row) and codes = e4m3_encode of the fp32
+    quotient x / s.  The quotient is not exact, so it is formed in the precision the cache
+    writer uses (IEEE fp32 division, round to nearest)."""
     x32 = np.asarray(x, dtype=np.float64).astype(np.float32)
     amax = np.max(np.abs(x32), axis=-1)
-    nz = amax > 0
-    safe = np.where(nz, amax, np.float32(1.0)).astype(np.float32)
-    s = np.where(nz, safe / np.float32(_E4M3_MAX), np.float32(1.0)).astype(np.float32)
-    r = np.where(nz, np.float32(_E4M3_MAX) / safe, np.float32(1.0)).astype(np.float32)
-    q = (x32 * r[..., None]).astype(np.float32)
+    s = np.where(amax > 0, amax / np.float32(_E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    q = (x32 / s[..., None]).astype(np.float32)
     return e4m3_encode(q.astype(np.float64)), s
 
 

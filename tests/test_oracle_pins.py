@@ -189,11 +189,7 @@ def test_quantize_fp8_rows_matches_torch_fp32():
     codes, s = oracle.quantize_fp8_rows(x.double().numpy())
     amax = x.abs().amax(-1)
     ts = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
-    # tensor / tensor division (IEEE, round to nearest); a Python scalar numerator can take a
-    # reciprocal-multiply path in torch that is not correctly rounded
-    tr = torch.where(amax > 0, torch.full_like(amax, 448.0) / torch.where(amax > 0, amax, torch.ones_like(amax)),
-                     torch.ones_like(amax))
-    tq = (x * tr[:, None]).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+    tq = (x / ts[:, None]).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
     np.testing.assert_array_equal(s, ts.numpy())
     np.testing.assert_array_equal(codes, tq.numpy())
     assert s[7] == 1.0 and np.all(codes[7] == 0)
