@@ -423,6 +423,7 @@ def run_ours(args, wl):
             "hbm_frac_of_measured": chain_gbs / peak,
             "roofline": roofline,
             "kernels_us": kern,
+            "next_rows": {"quant_append": quant_append_time(dsa, wl, stream)} if wl.q_pos0 < 0 else {},
             "serial": serial,
             "cpu_baseline": cpu_base,
             "e2e": e2e,
@@ -496,6 +497,60 @@ def kernel_times(dsa, wl, dev_sets, stream, reps):
     out["topk_us"] = timed(topk)
     out["sparse_attn_us"] = timed(attn)
     return out
+
+
+def quant_append_time(dsa, wl, stream, rows=65536, reps=20):
+    """The cache writer (the row of the method just before the chain): one chunk of `rows` new
+    tokens, bf16 indexer-key rows (d_idx) to MXFP8 and bf16 latent rows (D_qk) to FP8, written
+    into caches of `rows` rows.  Two source sets rotate (their bytes exceed L2); timed like the
+    kernels (CUDA graph replay, events on the launching stream).  Bytes: the bf16 sources read
+    plus the codes and scales written."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    g = torch.Generator(device=dev).manual_seed(7)
+    k_src = [torch.randn(rows, wl.d_idx, device=dev, generator=g).to(torch.bfloat16) for _ in range(2)]
+    v_src = [torch.randn(rows, wl.D_qk, device=dev, generator=g).to(torch.bfloat16) for _ in range(2)]
+    k_codes = torch.empty(rows, wl.d_idx, dtype=torch.uint8, device=dev)
+    k_sf = torch.empty(rows, wl.d_idx // 32, dtype=torch.uint8, device=dev)
+    v_codes = torch.empty(rows, wl.D_qk, dtype=torch.uint8, device=dev)
+    v_scale = torch.empty(rows, dtype=torch.float32, device=dev)
+    dst = torch.arange(rows, dtype=torch.int64, device=dev)
+
+    def mx(i):
+        dsa.dsa_quantize_mxfp8(k_src[i], codes=k_codes, sf=k_sf, dst_rows=dst, stream=stream)
+
+    def fp8(i):
+        dsa.dsa_quantize_fp8_rows(v_src[i], codes=v_codes, scales=v_scale, dst_rows=dst, stream=stream)
+
+    def step(i):
+        mx(i)
+        fp8(i)
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                fn(i % 2)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for i in range(reps):
+                fn(i % 2)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            gr.replay()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            gr.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    us = timed(step)
+    nbytes = rows * (2 * wl.d_idx + 2 * wl.D_qk + wl.d_idx + wl.d_idx // 32 + wl.D_qk + 4 + 8)
+    peak, kind = measured_hbm_peak()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"rows": rows, "us": us, "mxfp8_us": timed(mx), "fp8_rows_us": timed(fp8), "bytes": nbytes,
+            "achieved_gbs": gbs, "peak_gbs": peak, "frac": gbs / peak, "peak_kind": kind,
+            "launches_per_chunk": 2}
 
 
 def end_to_end(dsa, wl, cpu_sets, dev_sets, stream, steps, inflight=1):

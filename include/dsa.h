@@ -182,6 +182,39 @@ dsa_status dsa_sparse_attn(const void* q, const void* kv, const void* kv_v, cons
 size_t dsa_sparse_attn_workspace_size(int T, int H, int K, int D_v);
 
 /* --------------------------------------------------------------------------------------------
+ * dsa_quantize_mxfp8 / dsa_quantize_fp8_rows -- online quantisation that writes the caches the
+ * chain reads ("Day 0 Support for New LLM Architectures", Key Optimization 2: the indexer stores
+ * MXFP8, groups of 32 elements sharing one scale factor; the sparse-attention KV cache stores
+ * FP8).  Input row r (bf16) goes to destination row dst_rows[r] of the outputs (dst_rows NULL:
+ * row r; a negative entry drops the row), so appending new tokens to a cache laid out
+ * [sequence][L][...] is a call with dst_rows[r] = sequence * L + position.
+ *
+ * dsa_quantize_mxfp8 (OCP Microscaling Formats v1.0): per group of 32 elements, amax = max |x|,
+ * shared exponent e = floor(log2 amax) - 8 clamped to [-127, 127] (e = 0 for an all-zero
+ * group); sf byte = e + 127; each code = E4M3(x / 2^e), round to nearest, ties to even,
+ * saturating to +-448.
+ *   x        device bf16, row r at x + r * x_row_stride ELEMENTS (x_row_stride >= d), 2-byte
+ *            aligned; finite values
+ *   codes    device E4M3 bytes, destination row q at codes + q * d
+ *   sf       device E8M0 bytes, destination row q at sf + q * (d / 32)
+ *   dst_rows device int64 [rows] or NULL
+ * Supported: d a positive multiple of 32.
+ *
+ * dsa_quantize_fp8_rows: per row, s = amax / 448 (IEEE fp32 division; s = 1 for an all-zero
+ * row); each code = E4M3(x / s) (IEEE fp32 division), rounded and saturated as above;
+ * scales[q] = s for destination row q.
+ *   codes    device E4M3 bytes, destination row q at codes + q * code_row_stride (>= width)
+ *   scales   device fp32, destination row q at scales[q]
+ * Both return DSA_ERR_INVALID_ARG for bad sizes or pointers before any launch; destination rows
+ * must lie inside the caller's buffers (not checked).
+ * ------------------------------------------------------------------------------------------ */
+dsa_status dsa_quantize_mxfp8(const void* x, int64_t x_row_stride, int rows, int d, uint8_t* codes,
+                              uint8_t* sf, const int64_t* dst_rows, void* stream);
+dsa_status dsa_quantize_fp8_rows(const void* x, int64_t x_row_stride, int rows, int width,
+                                 uint8_t* codes, int64_t code_row_stride, float* scales,
+                                 const int64_t* dst_rows, void* stream);
+
+/* --------------------------------------------------------------------------------------------
  * Fused chain: dsa_decode / dsa_prefill run steps 1-3 back to back on `stream` (the indexer's
  * "score-weight-TopK" chain followed by the sparse gather kernel, Day 0 Support for New LLM
  * Architectures, Key Optimization 1), keeping the scores in the workspace.  dsa_decode expects

@@ -13,7 +13,8 @@ import torch
 from . import _native as N
 
 __all__ = ["dsa_index_score", "dsa_topk", "dsa_sparse_attn", "DsaCall", "dsa_decode", "dsa_prefill",
-           "dsa_workspace_size", "dsa_launch_count", "dsa_get_device_error", "ld_scores_for"]
+           "dsa_workspace_size", "dsa_launch_count", "dsa_get_device_error", "ld_scores_for",
+           "dsa_quantize_mxfp8", "dsa_quantize_fp8_rows"]
 
 
 def _p(t: Optional[torch.Tensor]):
@@ -165,6 +166,34 @@ def dsa_workspace_size(args: N.DsaArgs, prefill: bool) -> int:
     N.check(N.lib.dsa_workspace_size(ctypes.byref(args), int(bool(prefill)), ctypes.byref(n)),
             "dsa_workspace_size")
     return n.value
+
+
+def dsa_quantize_mxfp8(x, *, codes=None, sf=None, dst_rows=None, stream=None):
+    """bf16 rows x [rows, d] -> (E4M3 codes, E8M0 exponents per 32).  With `dst_rows` (int64
+    [rows]) input row r is written to row dst_rows[r] of the given `codes` [*, d] / `sf`
+    [*, d/32] (a cache append); without it new [rows, d] / [rows, d/32] tensors are returned."""
+    rows, d = x.shape
+    if codes is None:
+        codes = torch.empty(rows, d, dtype=torch.uint8, device=x.device)
+    if sf is None:
+        sf = torch.empty(rows, d // 32, dtype=torch.uint8, device=x.device)
+    N.check(N.lib.dsa_quantize_mxfp8(_p(x), x.stride(0), rows, d, _p(codes), _p(sf), _p(dst_rows),
+                                     _stream(stream)), "dsa_quantize_mxfp8")
+    return codes, sf
+
+
+def dsa_quantize_fp8_rows(x, *, codes=None, scales=None, dst_rows=None, stream=None):
+    """bf16 rows x [rows, width] -> (E4M3 codes, one fp32 scale per row); `dst_rows` as in
+    dsa_quantize_mxfp8 (codes [*, >= width] with any row pitch, scales [*])."""
+    rows, width = x.shape
+    if codes is None:
+        codes = torch.empty(rows, width, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(rows, dtype=torch.float32, device=x.device)
+    N.check(N.lib.dsa_quantize_fp8_rows(_p(x), x.stride(0), rows, width, _p(codes), codes.stride(0),
+                                        _p(scales), _p(dst_rows), _stream(stream)),
+            "dsa_quantize_fp8_rows")
+    return codes, scales
 
 
 def dsa_launch_count(args: N.DsaArgs, prefill: bool) -> int:
