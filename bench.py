@@ -64,14 +64,25 @@ def bytes_per_query(wl, n_visible=None):
     return k_idx + q_side + kv + q_out
 
 
+def step_bytes(wl):
+    """Compulsory HBM bytes of one step (all queries; each query's own visible length)."""
+    if wl.lengths:
+        return sum(bytes_per_query(wl, n) for n in wl.lengths)
+    return bytes_per_query(wl) * wl.T
+
+
 def index_score_bytes(wl, T):
     """Compulsory bytes of one index-score launch over T decode queries: keys (+scales) read,
-    query-side inputs read, fp32 scores written."""
+    query-side inputs read, fp32 scores written (visible positions only)."""
     e = idx_elem_bytes(wl)
-    per_q = wl.L * wl.d_idx * e + wl.H_idx * wl.d_idx * e + wl.H_idx * 4 + wl.L * 4
-    if wl.idx_dtype == "mxfp8":
-        per_q += wl.L * wl.d_idx // 32 + wl.H_idx * wl.d_idx // 32
-    return T * per_q
+    total = 0
+    for t in range(T):
+        n = wl.lengths[t] if wl.lengths else wl.L
+        per_q = n * wl.d_idx * e + wl.H_idx * wl.d_idx * e + wl.H_idx * 4 + n * 4
+        if wl.idx_dtype == "mxfp8":
+            per_q += n * wl.d_idx // 32 + wl.H_idx * wl.d_idx // 32
+        total += per_q
+    return total
 
 
 # ------------------------------------------------------------------------------------------------
@@ -292,7 +303,7 @@ def run_ours(args, wl):
     _build.build()
 
     # input sets: each rank draws its own (seed offset by rank) and rotates over R of them
-    per_step = bytes_per_query(wl) * wl.T
+    per_step = step_bytes(wl)
     n_sets = max(3, min(8, -(-3 * L2_BYTES // max(per_step, 1))))
     if args.sets:
         n_sets = args.sets
@@ -482,8 +493,8 @@ def kernel_times(dsa, wl, dev_sets, stream, reps):
                             stream=stream)
 
     def topk(i):
-        dsa.dsa_topk(scores[i], wl.K, L=L, q_per_seq=wl.q_per_seq, q_pos0=wl.q_pos0, idx=idx[i], ws=topk_ws,
-                     stream=stream)
+        dsa.dsa_topk(scores[i], wl.K, L=L, q_per_seq=wl.q_per_seq, q_pos0=wl.q_pos0,
+                     n_valid=dev_sets[i]["n_valid"], idx=idx[i], ws=topk_ws, stream=stream)
 
     outs = [torch.empty(wl.T, wl.H, wl.D_v, dtype=torch.bfloat16, device=s["q"].device) for s in dev_sets]
     lses = [torch.empty(wl.T, wl.H, dtype=torch.float32, device=s["q"].device) for s in dev_sets]

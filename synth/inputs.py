@@ -23,7 +23,7 @@ from __future__ import annotations
 
 import dataclasses
 import math
-from typing import Dict, Optional, Sequence
+from typing import Dict, Optional, Sequence, Tuple
 
 import torch
 
@@ -47,6 +47,8 @@ class Workload:
     q_pos0     -1 for decode (query t sees n_valid[t] or L positions);
                >= 0 for a causal chunk: query t sits at q_pos0 + t % q_per_seq
                and sees positions 0 .. q_pos0 + t % q_per_seq
+    lengths    decode only: the visible length of each query (n_valid), or None
+               for L everywhere
     """
 
     name: str
@@ -64,6 +66,7 @@ class Workload:
     separate_v: bool
     q_pos0: int
     seed: int
+    lengths: Optional[Tuple[int, ...]] = None
 
     @property
     def n_seq(self) -> int:
@@ -98,6 +101,12 @@ WORKLOADS: Dict[str, Workload] = {
     "decode_b1_l1m_mxfp8": Workload("decode_b1_l1m_mxfp8", T=1, q_per_seq=1, L=1 << 20, H_idx=64,
                                     d_idx=128, idx_dtype="mxfp8", K=2048, H=16, D_qk=576, D_v=512,
                                     kv_dtype="fp8", separate_v=False, q_pos0=-1, seed=1003),
+    # a batch of 8 sequences of different lengths in caches of 65536 positions (the N3 row of the
+    # scope table: variable-length batches, some shorter than K); otherwise as decode_b8_l32k_bf16.
+    "decode_b8_varlen_bf16": Workload("decode_b8_varlen_bf16", T=8, q_per_seq=1, L=65536, H_idx=64,
+                                      d_idx=128, idx_dtype="bf16", K=2048, H=16, D_qk=576, D_v=512,
+                                      kv_dtype="bf16", separate_v=False, q_pos0=-1, seed=1005,
+                                      lengths=(65536, 512, 33000, 2048, 16384, 100, 60000, 8000)),
     # causal prefill chunk: 4096 queries at positions 126976..131071 of L=131072, bf16.
     "prefill_t4096_l128k_bf16": Workload("prefill_t4096_l128k_bf16", T=4096, q_per_seq=4096,
                                          L=131072, H_idx=64, d_idx=128, idx_dtype="bf16", K=2048,
@@ -241,6 +250,8 @@ def make_inputs(wl: Workload, seed_offset: int = 0, n_valid: Optional[Sequence[i
         out["kv_v"], _ = _cache_rows(S, wl.L, wl.D_v, seed, 6, "bf16")
     else:
         out["kv_v"] = None
+    if n_valid is None:
+        n_valid = wl.lengths
     out["n_valid"] = None if n_valid is None else torch.tensor(list(n_valid), dtype=torch.int32)
     return out
 

@@ -286,7 +286,8 @@ def test_sparse_attn_out_of_range_index_is_skipped_and_recorded(dsa):
 _check_chain = check_chain
 
 
-@pytest.mark.parametrize("name", ["tiny_decode_l2k", "decode_b8_l32k_bf16", "decode_b8_l32k_mxfp8"])
+@pytest.mark.parametrize("name", ["tiny_decode_l2k", "decode_b8_l32k_bf16", "decode_b8_l32k_mxfp8",
+                                  "decode_b8_varlen_bf16"])
 def test_chain_full_decode_workloads(dsa, name):
     wl = synth.WORKLOADS[name]
     _check_chain(dsa, wl, synth.make_inputs(wl))

@@ -185,8 +185,10 @@ cudaError_t run_topk(const dsa_args& a, int t_off, int T, const float* scores, i
   return launch_topk(p, ws, st, pdl);
 }
 
+// valid_prefix: idx rows hold each query's min(K, n_t) selected positions first and -1 after
+// them (the chain's own Top-K output), so the attention may stop at the last valid row.
 cudaError_t run_sparse_attn(const dsa_args& a, int t_off, int T, const int32_t* idx, void* ws,
-                            cudaStream_t st, bool pdl) {
+                            cudaStream_t st, bool pdl, bool valid_prefix) {
   SparseAttnParams p = {};
   p.q = reinterpret_cast<const __nv_bfloat16*>(a.q) + (int64_t)t_off * a.H * a.D_qk;
   p.kv = reinterpret_cast<const uint8_t*>(a.kv);
@@ -207,6 +209,9 @@ cudaError_t run_sparse_attn(const dsa_args& a, int t_off, int T, const int32_t* 
   p.out = reinterpret_cast<__nv_bfloat16*>(a.out) + (int64_t)t_off * a.H * a.D_v;
   p.lse = a.lse ? a.lse + (int64_t)t_off * a.H : nullptr;
   p.err = device_error_ptr();
+  p.valid_prefix = valid_prefix;
+  p.q_pos0 = a.q_pos0;
+  p.n_valid = a.n_valid;
   return launch_sparse_attn(p, a.D_qk, a.D_v, a.kv_dtype == DSA_FP8_E4M3, a.kv_v != nullptr, ws, st, pdl);
 }
 
@@ -289,7 +294,8 @@ dsa_status run_chain(const dsa_args* a, void* ws, size_t ws_bytes, void* stream,
     if (a->L > 0) e = run_index_score(*a, t0, tn, scores, ld, hist, &filled, st, true);
     if (e == cudaSuccess)
       e = run_topk(*a, t0, tn, scores, ld, idx_slice, filled ? hist : nullptr, base + l.topk, st, true);
-    if (e == cudaSuccess) e = run_sparse_attn(*a, t0, tn, idx_slice, base + l.attn, st, true);
+    if (e == cudaSuccess)
+      e = run_sparse_attn(*a, t0, tn, idx_slice, base + l.attn, st, true, /*valid_prefix=*/true);
     if (e != cudaSuccess) return from_cuda(e);
   }
   return DSA_OK;
@@ -459,7 +465,8 @@ dsa_status dsa_sparse_attn(const void* q, const void* kv, const void* kv_v, cons
   a.v_seq_stride = v_seq_stride;
   a.out = out;
   a.lse = lse;
-  return from_cuda(run_sparse_attn(a, 0, T, idx, ws, reinterpret_cast<cudaStream_t>(stream), false));
+  return from_cuda(run_sparse_attn(a, 0, T, idx, ws, reinterpret_cast<cudaStream_t>(stream), false,
+                                   /*valid_prefix=*/false));
 }
 
 dsa_status dsa_workspace_size(const dsa_args* a, int prefill, size_t* bytes) {

@@ -117,6 +117,11 @@ struct SparseAttnParams {
   int splits;
   int rows_per_split;
   int* err;                // device error word
+  // Set by the fused chain, whose index rows hold the min(K, n_t) selected positions first and
+  // -1 after them: a split then stops at the query's last valid row (q_pos0 / n_valid give n_t).
+  bool valid_prefix;
+  int q_pos0;
+  const int32_t* n_valid;
 };
 
 int sparse_attn_splits(int T, int H, int K);

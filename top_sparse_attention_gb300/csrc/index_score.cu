@@ -100,15 +100,27 @@ struct Cfg {
 template <int THREADS>
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory"); }
 
-// Walks this CTA's (query group, tile) units u_begin .. u_end - 1 in order and stops at the ones
-// that hold a position visible to some query of the group.  Group facts (visible lengths, cache
-// sequence) are computed when the walk enters a group, so a step costs no division; the rest of
-// a group past its longest visible row is skipped at once.
+// Walks this CTA's share of the visible (query group, tile) units, in order.  A unit is visible
+// when its tile holds a position that some query of the group sees (a prefix of the group's
+// tiles).  The visible units are numbered group by group and CTA b of B takes numbers
+// [V*b/B, V*(b+1)/B) of the V in total, so the CTAs get equal work whatever the queries' lengths
+// (a batch of sequences of different lengths, or the causal rows of a prefill chunk).  Group facts
+// (visible lengths, cache sequence) are computed on entering a group; a step costs no division.
 template <int G>
 struct UnitWalk {
-  int u, u_end, g, tile, n_max, seq;
+  int left;  // units of this CTA still to visit
+  int g, tile, vt, n_max, seq;
   int n[G];  // visible length of each query of the group (0 past the last query)
 
+  __device__ __forceinline__ static int visible_tiles(const IndexScoreParams& p, int g) {
+    int m = 0;
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const int t = g * G + j;
+      if (t < p.T) m = max(m, visible_len(t + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid));
+    }
+    return min(p.tiles, (m + kTileM - 1) / kTileM);
+  }
   __device__ __forceinline__ void enter_group(const IndexScoreParams& p) {
     n_max = 0;
 #pragma unroll
@@ -117,31 +129,69 @@ struct UnitWalk {
       n[j] = t < p.T ? visible_len(t + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid) : 0;
       n_max = max(n_max, n[j]);
     }
+    vt = min(p.tiles, (n_max + kTileM - 1) / kTileM);
     seq = (g * G + p.t_off) / p.q_per_seq;
   }
-  __device__ __forceinline__ UnitWalk(const IndexScoreParams& p, int u_begin, int u_end_)
-      : u(u_begin - 1), u_end(u_end_) {
-    g = u_begin / p.tiles;
-    tile = u_begin - g * p.tiles - 1;  // one step before u_begin
+  // starts at visible unit `first` of group g0 (acc = visible units before g0), `count` units
+  __device__ __forceinline__ UnitWalk(const IndexScoreParams& p, const int* share) {
+    g = share[0];
+    left = share[2];
     enter_group(p);
+    tile = share[1] - 1;  // one step before this CTA's first unit
   }
-  // advances to the next visible unit; false when the range is done
+  // advances to the next unit; false when this CTA's share is done
   __device__ __forceinline__ bool next(const IndexScoreParams& p) {
-    for (++u; u < u_end; ++u) {
-      if (++tile == p.tiles) {
-        tile = 0;
+    if (left <= 0) return false;
+    --left;
+    if (++tile >= vt) {
+      do {  // a later group with a visible tile exists while units are left
         ++g;
         enter_group(p);
-      }
-      if (tile * kTileM < n_max) return true;
-      const int rest = p.tiles - 1 - tile;  // the group's later tiles are not visible either
-      u += rest;
-      tile += rest;
+      } while (vt == 0);
+      tile = 0;
     }
-    return false;
+    return true;
   }
   __device__ __forceinline__ int t0() const { return g * G; }
 };
+
+// This CTA's share of the visible units, found by one warp: lane l sums the visible tiles of a
+// contiguous block of groups, a warp scan gives the total V and each block's start, and the lane
+// whose block holds unit V*b/B walks it to the exact group.  share = {group, first visible tile
+// in it, units to visit}.
+template <int G>
+__device__ __forceinline__ void unit_share(const IndexScoreParams& p, int* share) {
+  const int lane = threadIdx.x & 31;
+  const int n_groups = (p.T + G - 1) / G;
+  const int g_lo = (int)((int64_t)n_groups * lane / 32), g_hi = (int)((int64_t)n_groups * (lane + 1) / 32);
+  int64_t mine = 0;
+  for (int g = g_lo; g < g_hi; ++g) mine += UnitWalk<G>::visible_tiles(p, g);
+  int64_t incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const int64_t V = __shfl_sync(0xffffffffu, incl, 31);
+  const int64_t b0 = V * blockIdx.x / gridDim.x, b1 = V * (blockIdx.x + 1) / gridDim.x;
+  const int64_t before = incl - mine;  // visible units before this lane's block
+  // the lane whose block holds unit b0 (the last lane when b0 == V)
+  const bool holds = (b0 >= before && b0 < incl) || (lane == 31 && b0 >= incl);
+  const uint32_t m = __ballot_sync(0xffffffffu, holds);
+  if (lane == __ffs(m) - 1) {
+    int g = g_lo;
+    int64_t acc = before;
+    for (; g < g_hi - 1; ++g) {
+      const int v = UnitWalk<G>::visible_tiles(p, g);
+      if (acc + v > b0) break;
+      acc += v;
+    }
+    if (g_hi <= g_lo) g = min(g_lo, n_groups - 1);  // an empty block (more lanes than groups)
+    share[0] = g;
+    share[1] = (int)(b0 - acc);
+    share[2] = (int)(b1 - b0);
+  }
+}
 
 template <bool MX, int D, int G, int NPAD>
 __global__ void __launch_bounds__(Cfg<MX, D, G, NPAD>::THREADS, Cfg<MX, D, G, NPAD>::CTAS_PER_SM)
@@ -161,16 +211,13 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
   uint64_t* tempty = tfull + 4;
   uint64_t* sf_full = tempty + 4;  // MXFP8 scale slot written (one arrival per epilogue warp)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_full + 4);
+  int* share = reinterpret_cast<int*>(tmem_slot + 1);  // [3]: this CTA's units (unit_share)
   float* w_s = reinterpret_cast<float*>(smem + C::OFF_W);    // [G][NPAD]
   uint32_t* hist_s = reinterpret_cast<uint32_t*>(smem + C::OFF_HIST);  // G == 1 only
   const bool build_hist = G == 1 && p.hist != nullptr;
 
   const int warp = warp_id();
   const int lane = lane_id();
-  const int n_groups = (p.T + G - 1) / G;
-  const int64_t U = (int64_t)n_groups * p.tiles;  // < 2^31 (checked on the host)
-  const int u_begin = (int)(U * blockIdx.x / gridDim.x);
-  const int u_end = (int)(U * (blockIdx.x + 1) / gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -194,6 +241,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
+  if (warp == 2) unit_share<G>(p, share);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -209,7 +257,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     const uint64_t evict_first = l2_evict_first_policy();  // key tiles are read once
     int it = 0, qn = -1, cur_t0 = -1;
     bool ok = true;
-    UnitWalk<G> w(p, u_begin, u_end);
+    UnitWalk<G> w(p, share);
     while (ok && w.next(p)) {
       if (w.t0() != cur_t0) {
         cur_t0 = w.t0();
@@ -266,7 +314,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     constexpr uint32_t idesc = make_idesc(1, 1, kTileM, C::N);
     int it = 0, qn = -1, cur_t0 = -1, ai = 0;
     bool ok = true;
-    UnitWalk<G> w(p, u_begin, u_end);
+    UnitWalk<G> w(p, share);
     while (ok && w.next(p)) {
       if (w.t0() != cur_t0) {
         if (qn >= 0 && lane == 0) tc_commit(&bempty[qn % C::B_BUFS]);
@@ -334,7 +382,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     // written, so the global load overlaps a tile's epilogue.  Each lane writes its lane of the
     // warp's quarter: its row's four group exponents (byte g = group g) into the four A columns,
     // and those of heads (lane) and (32 + lane) of the unit's query into the two B columns.
-    UnitWalk<G> sfw(p, u_begin, u_end);
+    UnitWalk<G> sfw(p, share);
     bool sf_more = false;
     int sf_n = 0, sf_t = -1;
     uint32_t sf_a = 0, sf_b0 = 0, sf_b1 = 0;
@@ -377,7 +425,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     }
     // after a timed-out wait the epilogue warps keep walking the units (so that every named
     // barrier below is reached by every epilogue thread) but skip the waits and the tile work
-    UnitWalk<G> w(p, u_begin, u_end);
+    UnitWalk<G> w(p, share);
     while (w.next(p)) {
       if (w.t0() != cur_t0) {
         epi_bar<ET>();

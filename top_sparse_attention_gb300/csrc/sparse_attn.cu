@@ -103,7 +103,11 @@ sparse_attn_kernel(const SparseAttnParams p) {
   const int h0 = blockIdx.z * kHeads;
   const int seq = (t + p.t_off) / p.q_per_seq;
   const int row_begin = split * p.rows_per_split;
-  const int row_end = min(p.K, row_begin + p.rows_per_split);
+  // rows past the query's selected positions hold -1: the chain's splits stop before them
+  const int k_rows = p.valid_prefix
+                         ? min(p.K, visible_len(t + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid))
+                         : p.K;
+  const int row_end = min(k_rows, row_begin + p.rows_per_split);
   const int nrows = max(0, row_end - row_begin);
   const int nblk = (nrows + kRows - 1) / kRows;
 
