@@ -54,12 +54,13 @@ struct Cfg {
   static constexpr int N = G * NPAD;              // MMA N
   static constexpr int A_BYTES = kTileM * ROW_BYTES;
   static constexpr int B_BYTES = N * ROW_BYTES;
-  static constexpr int B_BUFS = (2 * B_BYTES <= 64 * 1024) ? 2 : 1;
+  static constexpr int B_BUFS = (G == 1 && !MX) ? 1 : ((2 * B_BYTES <= 64 * 1024) ? 2 : 1);
   static constexpr int GROUPS = MX ? D / 32 : 1;  // scale groups per row (MMAs per tile)
-  // MXFP8 tiles (16 KB) run two CTAs per SM: each CTA's pipeline spends much of its time in the
+  // One-query tiles run two CTAs per SM: each CTA's pipeline spends much of its time in the
   // handshakes between stage ring, accumulators and epilogue, and a second CTA fills those gaps
-  // (B = 1, L = 1M: 36.8 -> 26.0 us).  bf16 tiles are 32 KB: two CTAs would leave one stage each.
-  static constexpr int CTAS_PER_SM = MX ? 2 : 1;
+  // (MXFP8, B = 1, L = 1M: 36.8 -> 25.4 us; bf16, B = 8, L = 32K: 15.1 -> 13.8 us, with two
+  // 32 KB stages and one query buffer per CTA).  Four-query prefill tiles keep one CTA per SM.
+  static constexpr int CTAS_PER_SM = G == 1 ? 2 : 1;
   static constexpr int ACC_COLS = N;
   // accumulators in flight between the MMA warp and the epilogue: as many as fit in 512 columns,
   // up to 4 (two were not enough to hide MMA completion + epilogue latency per tile)
