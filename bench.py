@@ -434,7 +434,8 @@ def run_ours(args, wl):
             "hbm_frac_of_measured": chain_gbs / peak,
             "roofline": roofline,
             "kernels_us": kern,
-            "next_rows": {"quant_append": quant_append_time(dsa, wl, stream)} if wl.q_pos0 < 0 else {},
+            "next_rows": ({"quant_append": quant_append_time(dsa, wl, stream),
+                           "paged_chain": paged_chain_time(dsa, wl, dev_sets, stream)} if wl.q_pos0 < 0 else {}),
             "serial": serial,
             "cpu_baseline": cpu_base,
             "e2e": e2e,
@@ -562,6 +563,67 @@ def quant_append_time(dsa, wl, stream, rows=65536, reps=20):
     return {"rows": rows, "us": us, "mxfp8_us": timed(mx), "fp8_rows_us": timed(fp8), "bytes": nbytes,
             "achieved_gbs": gbs, "peak_gbs": peak, "frac": gbs / peak, "peak_kind": kind,
             "launches_per_chunk": 2}
+
+
+def paged_chain_time(dsa, wl, dev_sets, stream, block_size=64, steps=500, max_sets=3):
+    """The fused chain over paged caches (the N2 row of the scope table): each input set's caches
+    copied into pools of `block_size`-position blocks in a random order and read through a block
+    table.  One batch at a time, CUDA-graph replay rotating over the sets; compare with `serial`
+    (the same chain over contiguous caches)."""
+    if wl.q_pos0 >= 0:
+        return None
+    dev = dev_sets[0]["q"].device
+    per_seq = -(-wl.L // block_size)
+    n_seq = wl.n_seq
+    n_blocks = n_seq * per_seq + 7
+    sets = dev_sets[:max_sets]
+    g = torch.Generator().manual_seed(17)
+    calls, graphs = [], []
+    for s in sets:
+        table = torch.randperm(n_blocks, generator=g)[: n_seq * per_seq].to(torch.int32).reshape(n_seq, per_seq)
+        flat = table.reshape(-1).to(dev).long()
+        pools = {}
+        for key in ("k_idx", "k_idx_sf", "kv", "kv_v", "kv_scale"):
+            c = s[key]
+            if c is None:
+                pools[key] = None
+                continue
+            rest = tuple(c.shape[2:])
+            pad = per_seq * block_size - wl.L
+            if pad:
+                c = torch.cat([c, torch.zeros((n_seq, pad) + rest, dtype=c.dtype, device=dev)], dim=1)
+            pool = torch.zeros((n_blocks, block_size) + rest, dtype=c.dtype, device=dev)
+            pool[flat] = c.reshape((n_seq * per_seq, block_size) + rest)
+            pools[key] = pool.reshape((n_blocks * block_size,) + rest)
+        call = dsa.DsaCall(q_idx=s["q_idx"], w=s["w"], k_idx=pools["k_idx"], q=s["q"], kv=pools["kv"], K=wl.K,
+                           sm_scale=wl.sm_scale, q_idx_sf=s["q_idx_sf"], k_idx_sf=pools["k_idx_sf"],
+                           kv_scale=pools["kv_scale"], kv_v=pools["kv_v"], D_v=wl.D_v, q_per_seq=wl.q_per_seq,
+                           q_pos0=wl.q_pos0, n_valid=s["n_valid"], block_table=table.to(dev),
+                           block_size=block_size, L=wl.L)
+        call._pools = pools  # keep the pools alive with the call
+        calls.append(call)
+    with torch.cuda.stream(stream):
+        for c in calls:
+            c(stream)
+    torch.cuda.synchronize()
+    for c in calls:
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            c(stream)
+        graphs.append(gr)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            graphs[i % len(graphs)].replay()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(steps):
+            graphs[i % len(graphs)].replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"block_size": block_size, "ms_per_step": ms, "value": wl.T / (ms * 1e-3), "unit": "queries/s",
+            "batches_in_flight": 1, "steps": steps}
 
 
 def end_to_end(dsa, wl, cpu_sets, dev_sets, stream, steps, inflight=1):

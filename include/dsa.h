@@ -37,7 +37,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 1
+#define DSA_ABI_VERSION 2
 
 typedef enum dsa_status {
   DSA_OK = 0,
@@ -247,7 +247,20 @@ typedef struct dsa_args {
   void* out;          /* bf16 [T, H, D_v] */
   float* lse;         /* fp32 [T, H] or NULL */
   int32_t* idx_out;   /* int32 [T, K] or NULL (then kept in the workspace) */
-  const void* block_table; /* reserved for a paged cache layout; must be NULL */
+  /* Paged caches (the pages' block-wise KV layout read through an index table, "Achieving
+   * Day-0 Readiness...", section 2.2; "reads directly from the paged K cache", Day 0 Support for
+   * New LLM Architectures, Key Optimization 1).  NULL block_table: every cache is contiguous per
+   * sequence as described above.  Otherwise each cache is one pool of num_blocks * block_size
+   * rows shared by all sequences: k_idx rows packed (row pitch d_idx * element size), k_idx_sf
+   * rows of d_idx/32 bytes, kv / kv_v rows at kv_row_stride / v_row_stride, kv_scale one fp32
+   * per row; the *_seq_stride fields are ignored.  Position s of sequence q (= query t /
+   * q_per_seq) lives in pool row block_table[q * max_blocks + s / block_size] * block_size +
+   * s % block_size.  Entries for every position a query sees (s < n_t) must hold block ids in
+   * [0, num_blocks); the others are never read. */
+  const int32_t* block_table; /* device int32 [n_seq][max_blocks] or NULL */
+  int block_size;             /* positions per block: a positive multiple of 64 */
+  int max_blocks;             /* entries per sequence in block_table, >= ceil(L / block_size) */
+  int num_blocks;             /* blocks in each pool; num_blocks * block_size < 2^31 */
 } dsa_args;
 
 /* Workspace bytes that dsa_decode (prefill = 0) or dsa_prefill (prefill = 1) needs for `a`.

@@ -66,7 +66,7 @@ def test_header_compiles_as_cxx(tmp_path):
 
 
 def test_status_strings_and_version(native):
-    assert native.lib.dsa_abi_version() == 1
+    assert native.lib.dsa_abi_version() == 2
     for s in range(6):
         assert native.status_string(s).startswith("DSA_")
     assert "unknown" in native.status_string(99)
@@ -140,9 +140,16 @@ def test_fused_validation(native):
     a.L, a.K, a.k_seq_stride, a.kv_seq_stride = 64, 8, 64 * 128, 128 * 64
     # decode entry with a causal q_pos0, prefill entry without one, and a block table
     assert native.lib.dsa_workspace_size(ctypes.byref(a), 1, ctypes.byref(n)) == 1
+    # a block table with a block size that is not a multiple of 64, or too few entries per sequence
     a.block_table = F
-    assert native.lib.dsa_workspace_size(ctypes.byref(a), 0, ctypes.byref(n)) == 2
+    a.block_size, a.max_blocks, a.num_blocks = 48, 2, 4
+    assert native.lib.dsa_workspace_size(ctypes.byref(a), 0, ctypes.byref(n)) == 1
+    a.block_size, a.max_blocks = 64, 0
+    assert native.lib.dsa_workspace_size(ctypes.byref(a), 0, ctypes.byref(n)) == 1
+    a.max_blocks = 1
+    assert native.lib.dsa_workspace_size(ctypes.byref(a), 0, ctypes.byref(n)) == 0
     a.block_table = None
+    a.block_size = a.max_blocks = a.num_blocks = 0
     # too-small workspace is reported before any launch
     assert native.lib.dsa_decode(ctypes.byref(a), F, 16, None) == 3
     assert native.lib.dsa_decode(None, F, 16, None) == 1

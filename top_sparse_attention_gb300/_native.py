@@ -50,6 +50,7 @@ class DsaArgs(ctypes.Structure):
         ("v_row_stride", ctypes.c_int64), ("v_seq_stride", ctypes.c_int64),
         ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("idx_out", ctypes.c_void_p),
         ("block_table", ctypes.c_void_p),
+        ("block_size", ctypes.c_int), ("max_blocks", ctypes.c_int), ("num_blocks", ctypes.c_int),
     ]
 
 

@@ -113,10 +113,19 @@ class DsaCall:
 
     def __init__(self, *, q_idx, w, k_idx, q, kv, K, sm_scale, q_idx_sf=None, k_idx_sf=None,
                  kv_scale=None, kv_v=None, D_v=None, q_per_seq=1, q_pos0=-1, n_valid=None,
-                 out=None, lse=None, idx_out=None, keep_idx=True, ws=None):
+                 out=None, lse=None, idx_out=None, keep_idx=True, ws=None,
+                 block_table=None, block_size=0, L=None):
+        """Caches are [n_seq, L, ...] per sequence, or, with `block_table` (int32 [n_seq,
+        max_blocks]) and `block_size`, pools of rows ([rows, ...]; kv_scale [rows]) shared by all
+        sequences, with the positions per sequence `L` given explicitly."""
         T, H_idx, d_idx = q_idx.shape
         _, H, D_qk = q.shape
-        L = k_idx.shape[1]
+        paged = block_table is not None
+        if paged:
+            if L is None or block_size <= 0:
+                raise ValueError("paged caches need L and block_size")
+        else:
+            L = k_idx.shape[1]
         if D_v is None:
             D_v = kv_v.shape[-1] if kv_v is not None else (512 if D_qk == 576 else D_qk)
         dev = q.device
@@ -135,17 +144,26 @@ class DsaCall:
         a.n_valid = ptr(n_valid)
         a.q_idx, a.q_idx_sf, a.w = ptr(q_idx), ptr(q_idx_sf), ptr(w)
         a.k_idx, a.k_idx_sf = ptr(k_idx), ptr(k_idx_sf)
-        a.k_seq_stride, a.k_sf_seq_stride = _seq_stride(k_idx), _seq_stride(k_idx_sf)
         a.q, a.kv, a.kv_v, a.kv_scale = ptr(q), ptr(kv), ptr(kv_v), ptr(kv_scale)
-        a.kv_row_stride = kv.stride(1) * kv.element_size()
-        a.kv_seq_stride = _seq_stride(kv)
-        a.v_row_stride = 0 if kv_v is None else kv_v.stride(1) * kv_v.element_size()
-        a.v_seq_stride = _seq_stride(kv_v)
+        if paged:
+            a.k_seq_stride = a.k_sf_seq_stride = a.kv_seq_stride = a.v_seq_stride = 0
+            a.kv_row_stride = kv.stride(0) * kv.element_size()
+            a.v_row_stride = 0 if kv_v is None else kv_v.stride(0) * kv_v.element_size()
+            a.block_table = ptr(block_table)
+            a.block_size = int(block_size)
+            a.max_blocks = block_table.shape[1]
+            a.num_blocks = k_idx.shape[0] // int(block_size)
+        else:
+            a.k_seq_stride, a.k_sf_seq_stride = _seq_stride(k_idx), _seq_stride(k_idx_sf)
+            a.kv_row_stride = kv.stride(1) * kv.element_size()
+            a.kv_seq_stride = _seq_stride(kv)
+            a.v_row_stride = 0 if kv_v is None else kv_v.stride(1) * kv_v.element_size()
+            a.v_seq_stride = _seq_stride(kv_v)
+            a.block_table = None
         a.out, a.lse, a.idx_out = ptr(self.out), ptr(self.lse), ptr(self.idx)
-        a.block_table = None
         self.args = a
         # keep every tensor the struct points at alive as long as the call object
-        self._keep = (q_idx, w, k_idx, q, kv, q_idx_sf, k_idx_sf, kv_scale, kv_v, n_valid)
+        self._keep = (q_idx, w, k_idx, q, kv, q_idx_sf, k_idx_sf, kv_scale, kv_v, n_valid, block_table)
         need = dsa_workspace_size(a, self.prefill)
         if ws is None:
             ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)

@@ -133,6 +133,17 @@ dsa_status check_sparse_attn(const void* q, const void* kv, const void* kv_v, co
 // ------------------------------------------------------------------------------------------
 // launches of the three steps for queries [t_off, t_off + T)
 
+PagedCache pages_of(const dsa_args& a) {
+  PagedCache pc = {};
+  if (a.block_table) {
+    pc.table = a.block_table;
+    pc.block_size = a.block_size;
+    pc.max_blocks = a.max_blocks;
+    pc.num_blocks = a.num_blocks;
+  }
+  return pc;
+}
+
 cudaError_t run_index_score(const dsa_args& a, int t_off, int T, float* scores, int64_t ld,
                             uint32_t* hist, bool* hist_filled, cudaStream_t st, bool pdl) {
   const int64_t row_bytes = (int64_t)a.d_idx * (a.idx_dtype == DSA_BF16 ? 2 : 1);
@@ -153,6 +164,7 @@ cudaError_t run_index_score(const dsa_args& a, int t_off, int T, float* scores, 
   p.tiles = (a.L + 127) / 128;
   p.err = device_error_ptr();
   p.hist = hist;
+  p.pages = pages_of(a);
   const uint8_t* qi = reinterpret_cast<const uint8_t*>(a.q_idx) + (int64_t)t_off * a.H_idx * row_bytes;
   return launch_index_score(qi, a.k_idx, a.k_seq_stride, a.T / a.q_per_seq, a.d_idx,
                             a.idx_dtype == DSA_MXFP8_E4M3, p, st, pdl, hist_filled);
@@ -182,6 +194,7 @@ cudaError_t run_topk(const dsa_args& a, int t_off, int T, const float* scores, i
   p.v_row_stride = a.v_row_stride;
   p.v_seq_stride = a.v_seq_stride;
   p.v_bytes = a.D_v * 2;
+  p.pages = pages_of(a);
   return launch_topk(p, ws, st, pdl);
 }
 
@@ -212,6 +225,7 @@ cudaError_t run_sparse_attn(const dsa_args& a, int t_off, int T, const int32_t* 
   p.valid_prefix = valid_prefix;
   p.q_pos0 = a.q_pos0;
   p.n_valid = a.n_valid;
+  p.pages = pages_of(a);
   return launch_sparse_attn(p, a.D_qk, a.D_v, a.kv_dtype == DSA_FP8_E4M3, a.kv_v != nullptr, ws, st, pdl);
 }
 
@@ -255,18 +269,29 @@ Layout layout_of(const dsa_args& a, int prefill) {
 
 dsa_status check_args(const dsa_args* a, int prefill) {
   if (!a) return DSA_ERR_INVALID_ARG;
-  if (a->block_table) return DSA_ERR_UNSUPPORTED;
+  if (a->block_table) {
+    if (a->block_size <= 0 || a->block_size % 64 != 0 || a->num_blocks <= 0) return DSA_ERR_INVALID_ARG;
+    if ((int64_t)a->max_blocks * a->block_size < a->L) return DSA_ERR_INVALID_ARG;
+    if ((int64_t)a->num_blocks * a->block_size >= (1ll << 31)) return DSA_ERR_UNSUPPORTED;
+  }
   if (prefill ? a->q_pos0 < 0 : a->q_pos0 >= 0) return DSA_ERR_INVALID_ARG;
+  // pools have no per-sequence pitch: the checks below see the pitch of a contiguous layout
+  const int64_t L = a->L;
+  const int64_t k_seq = a->block_table ? (L * a->d_idx * (a->idx_dtype == DSA_BF16 ? 2 : 1) + 15) / 16 * 16
+                                       : a->k_seq_stride;
+  const int64_t k_sf_seq = a->block_table ? (L * (a->d_idx / 32) + 3) / 4 * 4 : a->k_sf_seq_stride;
+  const int64_t kv_seq = a->block_table ? L * a->kv_row_stride : a->kv_seq_stride;
+  const int64_t v_seq = a->block_table ? L * a->v_row_stride : a->v_seq_stride;
   dsa_status s = check_index_score(a->q_idx, a->q_idx_sf, a->w, a->k_idx, a->k_idx_sf,
-                                   a->k_seq_stride, a->k_sf_seq_stride, a->T, a->q_per_seq,
+                                   k_seq, k_sf_seq, a->T, a->q_per_seq,
                                    a->q_pos0, a->n_valid, a->L, a->H_idx, a->d_idx, a->idx_dtype,
                                    reinterpret_cast<const float*>(16), ld_for(a->L));
   if (s != DSA_OK) return s;
   s = check_topk(reinterpret_cast<const float*>(16), ld_for(a->L), a->T, a->q_per_seq, a->q_pos0,
                  a->n_valid, a->L, a->K, reinterpret_cast<const int32_t*>(16));
   if (s != DSA_OK) return s;
-  return check_sparse_attn(a->q, a->kv, a->kv_v, a->kv_scale, a->kv_row_stride, a->kv_seq_stride,
-                           a->v_row_stride, a->v_seq_stride, reinterpret_cast<const int32_t*>(16),
+  return check_sparse_attn(a->q, a->kv, a->kv_v, a->kv_scale, a->kv_row_stride, kv_seq,
+                           a->v_row_stride, v_seq, reinterpret_cast<const int32_t*>(16),
                            a->T, a->q_per_seq, a->L, a->K, a->H, a->D_qk, a->D_v, a->kv_dtype,
                            a->out);
 }

@@ -33,6 +33,18 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+// Paged caches: position s of sequence q lives in pool row
+// table[q * max_blocks + s / block_size] * block_size + s % block_size (table null: contiguous).
+struct PagedCache {
+  const int32_t* table;
+  int block_size, max_blocks, num_blocks;
+};
+
+__device__ __forceinline__ int64_t page_row(const PagedCache& pc, int64_t seq, int pos) {
+  const int32_t b = __ldg(pc.table + seq * pc.max_blocks + pos / pc.block_size);
+  return (int64_t)b * pc.block_size + pos % pc.block_size;
+}
+
 // ---------------------------------------------------------------------------------------------
 // step 1: indexer scores
 
@@ -50,6 +62,7 @@ struct IndexScoreParams {
   int* err;                // device error word
   uint32_t* hist;          // [T][4096] histograms of the top 12 key bits of the scores (added
                            // to; zero on entry), or null
+  PagedCache pages;        // k_idx / k_sf pools (table null: contiguous per sequence)
 };
 
 constexpr int kHistBins = 4096;
@@ -87,6 +100,7 @@ struct TopkParams {
   const uint8_t* kv_v;     // separate V rows, or null
   int64_t v_row_stride, v_seq_stride;
   int v_bytes;
+  PagedCache pages;        // kv / kv_v pools for the prefetch (table null: contiguous)
 };
 
 // allow_wide: long rows may be split over independent CTAs (workspace from topk_ws_bytes);
@@ -122,6 +136,7 @@ struct SparseAttnParams {
   bool valid_prefix;
   int q_pos0;
   const int32_t* n_valid;
+  PagedCache pages;        // kv / kv_v / kv_scale pools (table null: contiguous per sequence)
 };
 
 int sparse_attn_splits(int T, int H, int K);

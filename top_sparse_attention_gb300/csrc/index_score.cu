@@ -259,7 +259,34 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     int it = 0, qn = -1, cur_t0 = -1;
     bool ok = true;
     UnitWalk<G> w(p, share);
+    // paged caches: a tile is two 64-row halves, each inside one block; lane i holds the pool
+    // rows of the halves of the i-th of the next 32 units (looked up 32 units at a time, one
+    // memory round trip), or kNoRow for a half past the group's longest visible row
+    constexpr uint32_t kNoRow = 0xFFFFFFFFu;
+    const bool paged = p.pages.table != nullptr;
+    UnitWalk<G> look(p, share);
+    uint32_t pr0 = kNoRow, pr1 = kNoRow;
+    int nb = 32;
     while (ok && w.next(p)) {
+      uint32_t row0 = 0, row1 = kNoRow;
+      if (paged) {
+        if (nb == 32) {
+          UnitWalk<G> c = look;
+          bool have = true;
+          for (int q = 0; q <= lane && have; ++q) have = c.next(p);
+          pr0 = pr1 = kNoRow;
+          if (have) {
+            const int pos = c.tile * kTileM;
+            pr0 = (uint32_t)page_row(p.pages, c.seq, pos);
+            if (pos + 64 < c.n_max) pr1 = (uint32_t)page_row(p.pages, c.seq, pos + 64);
+          }
+          for (int q = 0; q < 32; ++q) look.next(p);  // every lane moves the same 32 units on
+          nb = 0;
+        }
+        row0 = __shfl_sync(0xffffffffu, pr0, nb);
+        row1 = __shfl_sync(0xffffffffu, pr1, nb);
+        ++nb;
+      }
       if (w.t0() != cur_t0) {
         cur_t0 = w.t0();
         ++qn;
@@ -301,11 +328,24 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&full[s], C::A_BYTES);
+        if (!paged) {
+          mbar_arrive_expect_tx(&full[s], C::A_BYTES);
 #pragma unroll
-        for (int b = 0; b < C::BOXES; ++b)
-          tma_load_3d_hint(a_s + s * C::A_BYTES + b * (kTileM * 128), &tm_k, &full[s], b * C::BOX_COLS,
-                           w.tile * kTileM, w.seq, evict_first);
+          for (int b = 0; b < C::BOXES; ++b)
+            tma_load_3d_hint(a_s + s * C::A_BYTES + b * (kTileM * 128), &tm_k, &full[s], b * C::BOX_COLS,
+                             w.tile * kTileM, w.seq, evict_first);
+        } else {
+          // a half past the visible rows is not loaded: its MMA rows hold stale data and are
+          // never scored (every accumulator row depends on its own A row only)
+          const int halves = row1 == kNoRow ? 1 : 2;
+          mbar_arrive_expect_tx(&full[s], (uint32_t)(halves * C::A_BYTES / 2));
+#pragma unroll
+          for (int b = 0; b < C::BOXES; ++b) {
+            uint8_t* dst = a_s + s * C::A_BYTES + b * (kTileM * 128);
+            tma_load_2d_hint(dst, &tm_k, &full[s], b * C::BOX_COLS, (int)row0, evict_first);
+            if (halves == 2) tma_load_2d_hint(dst + 64 * 128, &tm_k, &full[s], b * C::BOX_COLS, (int)row1, evict_first);
+          }
+        }
       }
       __syncwarp();
       ++it;
@@ -390,6 +430,8 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     auto sf_load_a = [&]() -> uint32_t {
       const int pos = sfw.tile * kTileM + row;
       if (pos >= sfw.n_max) return 0x7F7F7F7Fu;  // a row that is not scored: any finite scale
+      if (p.pages.table)
+        return __ldg(reinterpret_cast<const uint32_t*>(p.k_sf + page_row(p.pages, sfw.seq, pos) * 4));
       return __ldg(reinterpret_cast<const uint32_t*>(p.k_sf + (int64_t)sfw.seq * p.k_sf_seq_stride + (int64_t)pos * 4));
     };
     auto q_word = [&](int t, int h) -> uint32_t {
@@ -502,13 +544,22 @@ cudaError_t launch_cfg(const void* q_idx, const void* k_idx, int64_t k_seq_strid
                        const IndexScoreParams& p, cudaStream_t stream, bool pdl) {
   using C = Cfg<MX, D, G, NPAD>;
   CUtensorMap tm;
-  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.L, (cuuint64_t)n_seq};
-  const cuuint64_t seq_stride = n_seq > 1 ? (cuuint64_t)k_seq_stride : (cuuint64_t)p.L * C::ROW_BYTES;
-  const cuuint64_t strides[2] = {(cuuint64_t)C::ROW_BYTES, seq_stride};
-  const cuuint32_t box[3] = {(cuuint32_t)C::BOX_COLS, (cuuint32_t)kTileM, 1};
-  CUresult r = encode_tensor_map(&tm, MX ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                                 3, const_cast<void*>(k_idx), dims, strides, box,
-                                 CU_TENSOR_MAP_SWIZZLE_128B);
+  CUresult r;
+  if (!p.pages.table) {
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.L, (cuuint64_t)n_seq};
+    const cuuint64_t seq_stride = n_seq > 1 ? (cuuint64_t)k_seq_stride : (cuuint64_t)p.L * C::ROW_BYTES;
+    const cuuint64_t strides[2] = {(cuuint64_t)C::ROW_BYTES, seq_stride};
+    const cuuint32_t box[3] = {(cuuint32_t)C::BOX_COLS, (cuuint32_t)kTileM, 1};
+    r = encode_tensor_map(&tm, MX ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                          const_cast<void*>(k_idx), dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    // one pool of num_blocks * block_size rows; boxes of 64 rows (half a tile, inside one block)
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)p.pages.num_blocks * p.pages.block_size};
+    const cuuint64_t strides[1] = {(cuuint64_t)C::ROW_BYTES};
+    const cuuint32_t box[2] = {(cuuint32_t)C::BOX_COLS, (cuuint32_t)(kTileM / 2)};
+    r = encode_tensor_map(&tm, MX ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                          const_cast<void*>(k_idx), dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   // q_idx rows by TMA when the box of N rows fits inside the T * H_idx rows of the tensor
   CUtensorMap tq;

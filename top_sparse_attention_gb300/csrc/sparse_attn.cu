@@ -119,9 +119,11 @@ sparse_attn_kernel(const SparseAttnParams p) {
   float* red_max = reinterpret_cast<float*>(smem + C::OFF_RED) + g * 2 * 4 * kHeads;
   float* red_sum = red_max + 4 * kHeads;
 
-  const uint8_t* kv_base = p.kv + (int64_t)seq * p.kv_seq_stride;
-  const uint8_t* v_base = SEPV ? p.kv_v + (int64_t)seq * p.v_seq_stride : nullptr;
-  const float* scale_base = FP8 ? p.kv_scale + (int64_t)seq * p.L : nullptr;
+  // paged caches: rows are pool rows found through the page table (no per-sequence base)
+  const bool paged = p.pages.table != nullptr;
+  const uint8_t* kv_base = p.kv + (paged ? 0 : (int64_t)seq * p.kv_seq_stride);
+  const uint8_t* v_base = SEPV ? p.kv_v + (paged ? 0 : (int64_t)seq * p.v_seq_stride) : nullptr;
+  const float* scale_base = FP8 ? p.kv_scale + (paged ? 0 : (int64_t)seq * p.L) : nullptr;
 
   if (tid == 0) {
     mbar_init(&bars[0], 1);
@@ -145,7 +147,7 @@ sparse_attn_kernel(const SparseAttnParams p) {
   if (tid == 0) mbar_arrive(&bars[2]);
   pdl_wait();  // the index rows come from the previous kernel in the stream
 
-  // this CTA's index rows (and FP8 row scales), checked against [-1, L)
+  // this CTA's index rows (and FP8 row scales), checked against [-1, L); kept as cache rows
   for (int j = tid; j < nblk * kRows; j += C::THREADS) {
     int i = -1;
     if (j < nrows) {
@@ -154,6 +156,7 @@ sparse_attn_kernel(const SparseAttnParams p) {
         record_error(p.err, DSA_DEVERR_INDEX_RANGE);
         i = -1;
       }
+      if (i >= 0 && paged) i = (int)page_row(p.pages, seq, i);
     }
     idx_s[j] = i;
     if (FP8) scale_s[j] = (i >= 0) ? scale_base[i] : 0.f;

@@ -226,11 +226,13 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkParams
 
   // L2 prefetch of a selected row of the attention cache (chain only)
   const int64_t seq = (t + p.t_off) / p.q_per_seq;
-  const uint8_t* pf_kv = p.kv ? p.kv + seq * p.kv_seq_stride : nullptr;
-  const uint8_t* pf_v = p.kv_v ? p.kv_v + seq * p.v_seq_stride : nullptr;
+  const bool paged = p.pages.table != nullptr;
+  const uint8_t* pf_kv = p.kv ? p.kv + (paged ? 0 : seq * p.kv_seq_stride) : nullptr;
+  const uint8_t* pf_v = p.kv_v ? p.kv_v + (paged ? 0 : seq * p.v_seq_stride) : nullptr;
   auto prefetch_row = [&](uint32_t pos) {
-    prefetch_l2(pf_kv + (int64_t)pos * p.kv_row_stride, (uint32_t)p.kv_bytes);
-    if (pf_v) prefetch_l2(pf_v + (int64_t)pos * p.v_row_stride, (uint32_t)p.v_bytes);
+    const int64_t row = paged ? page_row(p.pages, seq, (int)pos) : (int64_t)pos;
+    prefetch_l2(pf_kv + row * p.kv_row_stride, (uint32_t)p.kv_bytes);
+    if (pf_v) prefetch_l2(pf_v + row * p.v_row_stride, (uint32_t)p.v_bytes);
   };
 
   if (n <= p.K) {  // the whole cluster leaves here together (n is the same for all its CTAs)
@@ -865,12 +867,14 @@ __global__ void __launch_bounds__(kThreads) topk_wide_emit_kernel(const TopkPara
   const int n = visible_len(t + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid);
   int32_t* out = p.idx + (int64_t)t * p.K;
   const int64_t seq = (t + p.t_off) / p.q_per_seq;
-  const uint8_t* pf_kv = p.kv ? p.kv + seq * p.kv_seq_stride : nullptr;
-  const uint8_t* pf_v = p.kv_v ? p.kv_v + seq * p.v_seq_stride : nullptr;
+  const bool paged = p.pages.table != nullptr;
+  const uint8_t* pf_kv = p.kv ? p.kv + (paged ? 0 : seq * p.kv_seq_stride) : nullptr;
+  const uint8_t* pf_v = p.kv_v ? p.kv_v + (paged ? 0 : seq * p.v_seq_stride) : nullptr;
   auto prefetch_row = [&](uint32_t pos) {
     if (!pf_kv) return;
-    prefetch_l2(pf_kv + (int64_t)pos * p.kv_row_stride, (uint32_t)p.kv_bytes);
-    if (pf_v) prefetch_l2(pf_v + (int64_t)pos * p.v_row_stride, (uint32_t)p.v_bytes);
+    const int64_t row = paged ? page_row(p.pages, seq, (int)pos) : (int64_t)pos;
+    prefetch_l2(pf_kv + row * p.kv_row_stride, (uint32_t)p.kv_bytes);
+    if (pf_v) prefetch_l2(pf_v + row * p.v_row_stride, (uint32_t)p.v_bytes);
   };
   const ChunkKeys ck(p, t, c, n);
   if (n <= p.K) {  // every visible position, in order, then -1
