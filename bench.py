@@ -59,7 +59,8 @@ def bytes_per_query(wl, n_visible=None):
     if wl.separate_v:
         kv = rows * (wl.D_qk + wl.D_v) * kv_e
     else:
-        kv = rows * wl.D_qk * kv_e + (rows * 4 if wl.kv_dtype == "fp8" else 0)
+        n_scales = {"fp8": 1, "fp8_t128": -(-wl.D_qk // 128)}.get(wl.kv_dtype, 0)
+        kv = rows * wl.D_qk * kv_e + rows * 4 * n_scales
     q_out = wl.H * wl.D_qk * 2 + wl.H * wl.D_v * 2
     return k_idx + q_side + kv + q_out
 

@@ -36,7 +36,7 @@ import numpy as np
 
 __all__ = [
     "bf16_bits_to_f64", "e4m3_to_f64", "e8m0_to_f64", "dequant_mxfp8", "dequant_fp8_rows",
-    "e4m3_encode", "quantize_mxfp8", "quantize_fp8_rows",
+    "e4m3_encode", "quantize_mxfp8", "quantize_fp8_rows", "dequant_fp8_tiles", "quantize_fp8_tiles",
     "index_scores", "topk_positions", "sparse_attention", "visible_length", "query_sequence",
     "Chain", "chain_query",
 ]
@@ -91,6 +91,17 @@ def dequant_mxfp8(codes, sf, group: int = 32) -> np.ndarray:
 def dequant_fp8_rows(codes, row_scale) -> np.ndarray:
     """FP8 E4M3 cache rows with one fp32 scale per row (token) -> fp64."""
     return e4m3_to_f64(codes) * np.asarray(row_scale, dtype=np.float64)[..., None]
+
+
+def dequant_fp8_tiles(codes, tile_scale, tile: int = 128) -> np.ndarray:
+    """FP8 E4M3 cache rows with one fp32 scale per `tile` consecutive elements of a row (the last
+    tile may be shorter) -> fp64.  tile_scale has ceil(width / tile) entries per row.
+    (Day 0 Support for New LLM Architectures, Key Optimization 2: FP8 KV cache with a scale per
+    token and 128-element tile.)"""
+    v = e4m3_to_f64(codes)
+    width = v.shape[-1]
+    sc = np.repeat(np.asarray(tile_scale, dtype=np.float64), tile, axis=-1)[..., :width]
+    return v * sc
 
 
 # ----------------------------------------------------------------------------------------------
@@ -184,6 +195,20 @@ def quantize_fp8_rows(x):
     s = np.where(amax > 0, amax / np.float32(_E4M3_MAX), np.float32(1.0)).astype(np.float32)
     q = (x32 / s[..., None]).astype(np.float32)
     return e4m3_encode(q.astype(np.float64)), s
+
+
+def quantize_fp8_tiles(x, tile: int = 128):
+    """Rows of values -> (E4M3 codes, fp32 scales [..., ceil(width / tile)]): every `tile`
+    consecutive elements of a row (the last tile may be shorter) are one quantize_fp8_rows row."""
+    x = np.asarray(x, dtype=np.float64)
+    width = x.shape[-1]
+    codes = np.empty(x.shape, dtype=np.uint8)
+    scales = []
+    for t0 in range(0, width, tile):
+        c, s = quantize_fp8_rows(x[..., t0:t0 + tile])
+        codes[..., t0:t0 + tile] = c
+        scales.append(s)
+    return codes, np.stack(scales, axis=-1).astype(np.float32)
 
 
 # ----------------------------------------------------------------------------------------------
@@ -296,6 +321,8 @@ class Chain:
         kv = self.a["kv"][seq, rows]
         if self.kv_dtype == "bf16":
             k = bf16_bits_to_f64(kv)
+        elif self.kv_dtype == "fp8_t128":
+            k = dequant_fp8_tiles(kv, self.a["kv_scale"][seq, rows])
         else:
             k = dequant_fp8_rows(kv, self.a["kv_scale"][seq, rows])
         if self.a.get("kv_v") is not None:

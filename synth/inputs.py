@@ -27,7 +27,7 @@ from typing import Dict, Optional, Sequence, Tuple
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "make_inputs", "encode_mxfp8", "encode_fp8_rows",
+__all__ = ["Workload", "WORKLOADS", "make_inputs", "encode_mxfp8", "encode_fp8_rows", "encode_fp8_tiles",
            "to_bf16", "small_workload"]
 
 
@@ -62,7 +62,7 @@ class Workload:
     H: int
     D_qk: int
     D_v: int
-    kv_dtype: str  # "bf16" | "fp8"
+    kv_dtype: str  # "bf16" | "fp8" (one scale per row) | "fp8_t128" (one scale per 128 of a row)
     separate_v: bool
     q_pos0: int
     seed: int
@@ -97,6 +97,12 @@ WORKLOADS: Dict[str, Workload] = {
     "decode_b8_l32k_mxfp8": Workload("decode_b8_l32k_mxfp8", T=8, q_per_seq=1, L=32768, H_idx=64,
                                      d_idx=128, idx_dtype="mxfp8", K=2048, H=16, D_qk=576, D_v=512,
                                      kv_dtype="fp8", separate_v=False, q_pos0=-1, seed=1002),
+    # the MXFP8 decode batch with the page's FP8 KV variant: one fp32 scale per 128-element tile
+    # of each latent row (576 = 4 x 128 + 64: five scales per row); the N1b row of the scope table.
+    "decode_b8_l32k_mxfp8_kvt128": Workload("decode_b8_l32k_mxfp8_kvt128", T=8, q_per_seq=1, L=32768,
+                                            H_idx=64, d_idx=128, idx_dtype="mxfp8", K=2048, H=16,
+                                            D_qk=576, D_v=512, kv_dtype="fp8_t128", separate_v=False,
+                                            q_pos0=-1, seed=1006),
     # batch 1 at L=1,048,576, MXFP8 indexer, FP8 latent cache.
     "decode_b1_l1m_mxfp8": Workload("decode_b1_l1m_mxfp8", T=1, q_per_seq=1, L=1 << 20, H_idx=64,
                                     d_idx=128, idx_dtype="mxfp8", K=2048, H=16, D_qk=576, D_v=512,
@@ -185,6 +191,16 @@ def encode_fp8_rows(x: torch.Tensor):
     return codes.contiguous(), scale.contiguous()
 
 
+def encode_fp8_tiles(x: torch.Tensor, tile: int = 128):
+    """E4M3 encoding with one fp32 scale per `tile` consecutive elements of a row (the last tile
+    may be shorter): each tile is encoded as encode_fp8_rows encodes a row.  Returns (codes u8,
+    scales [..., ceil(width / tile)] fp32)."""
+    parts = [encode_fp8_rows(x[..., t0:t0 + tile]) for t0 in range(0, x.shape[-1], tile)]
+    codes = torch.cat([c for c, _ in parts], dim=-1)
+    scales = torch.stack([sc for _, sc in parts], dim=-1)
+    return codes.contiguous(), scales.contiguous()
+
+
 # ----------------------------------------------------------------------------------------------
 # workload inputs
 
@@ -207,6 +223,8 @@ def _cache_rows(n_seq: int, L: int, width: int, seed: int, tid: int, fmt: str, w
                 c, sf = encode_mxfp8(x)
             elif fmt == "fp8":
                 c, sf = encode_fp8_rows(x)
+            elif fmt == "fp8_t128":
+                c, sf = encode_fp8_tiles(x, 128)
             else:
                 raise ValueError(fmt)
             if out_codes is None:
@@ -243,7 +261,7 @@ def make_inputs(wl: Workload, seed_offset: int = 0, n_valid: Optional[Sequence[i
     out["k_idx"], out["k_idx_sf"] = _cache_rows(S, wl.L, wl.d_idx, seed, 3, wl.idx_dtype)
 
     out["q"] = to_bf16(_randn((T, wl.H, wl.D_qk), seed, 4))
-    kv_fmt = "bf16" if wl.kv_dtype == "bf16" else "fp8"
+    kv_fmt = wl.kv_dtype
     out["kv"], out["kv_scale"] = _cache_rows(S, wl.L, wl.D_qk, seed, 5, kv_fmt)
     if wl.separate_v:
         assert wl.kv_dtype == "bf16"

@@ -9,10 +9,10 @@ import oracle
 import synth
 
 # Attention max-abs tolerances on outputs (bf16 path / FP8 KV path)
-ATTN_TOL = {"bf16": 2e-2, "fp8": 6e-2}
+ATTN_TOL = {"bf16": 2e-2, "fp8": 6e-2, "fp8_t128": 6e-2}
 # Tighter regression guard for the same comparison over distinct random rows, where the bf16
 # rounding of the softmax weights averages out (observed errors sit near 1e-3)
-ATTN_GUARD = {"bf16": 4e-3, "fp8": 4e-3}
+ATTN_GUARD = {"bf16": 4e-3, "fp8": 4e-3, "fp8_t128": 4e-3}
 LSE_TOL = 2e-3
 
 

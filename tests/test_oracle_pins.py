@@ -195,6 +195,31 @@ def test_quantize_fp8_rows_matches_torch_fp32():
     assert s[7] == 1.0 and np.all(codes[7] == 0)
 
 
+def test_fp8_tiles_reduce_to_rows_and_match_torch():
+    rng = np.random.default_rng(10)
+    x = torch.from_numpy(rng.standard_normal((40, 576)) * np.ldexp(1.0, rng.integers(-8, 8, (40, 5))).repeat(128, 1)[:, :576])
+    x = x.to(torch.bfloat16).to(torch.float32)
+    x[3, 128:256] = 0.0  # an all-zero tile
+    codes, s = oracle.quantize_fp8_tiles(x.double().numpy())
+    assert s.shape == (40, 5) and s[3, 1] == 1.0 and np.all(codes[3, 128:256] == 0)
+    # torch restatement, tile by tile (the last tile is 64 wide)
+    for t0 in range(0, 576, 128):
+        xt = x[:, t0:t0 + 128]
+        amax = xt.abs().amax(-1)
+        ts = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+        tq = (xt / ts[:, None]).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+        np.testing.assert_array_equal(s[:, t0 // 128], ts.numpy())
+        np.testing.assert_array_equal(codes[:, t0:t0 + 128], tq.numpy())
+    # one scale repeated over all tiles of a row is the per-row format
+    row_s = np.abs(rng.standard_normal(40)).astype(np.float32) + 0.5
+    np.testing.assert_array_equal(oracle.dequant_fp8_tiles(codes, np.repeat(row_s[:, None], 5, 1)),
+                                  oracle.dequant_fp8_rows(codes, row_s))
+    # dequantised error within E4M3 rounding (1/16 of the tile's max) or saturation
+    back = oracle.dequant_fp8_tiles(codes, s)
+    tmax = np.repeat(np.maximum.reduceat(np.abs(x.double().numpy()), np.arange(0, 576, 128), axis=1), 128, 1)[:, :576]
+    assert np.all(np.abs(back - x.double().numpy()) <= tmax / 16 + 1e-300)
+
+
 # ------------------------------------------------------------------------------------------------
 # indexer scores
 
