@@ -51,7 +51,10 @@ typedef enum dsa_status {
 typedef enum dsa_dtype {
   DSA_BF16 = 0,       /* bfloat16 elements */
   DSA_FP8_E4M3 = 1,   /* E4M3 ("fn") codes with one fp32 scale per cache row (KV cache) */
-  DSA_MXFP8_E4M3 = 2  /* E4M3 codes with one E8M0 exponent byte per 32 elements (indexer) */
+  DSA_MXFP8_E4M3 = 2, /* E4M3 codes with one E8M0 exponent byte per 32 elements (indexer) */
+  DSA_FP8_E4M3_T128 = 3 /* E4M3 codes with one fp32 scale per 128-element tile of a row (KV
+                           cache, the 576/512 latent row: 5 scales per row, the last tile 64
+                           wide); kv_scale holds ceil(D_qk / 128) floats per row */
 } dsa_dtype;
 
 /* Device error codes recorded by kernels (read with dsa_get_device_error). */
@@ -158,15 +161,17 @@ dsa_status dsa_topk_noalloc(const float* scores, int64_t ld_scores, int T, int q
  *   logit[r] = sm_scale * sum_j q[t,h,j] * Kv[r, j]                 (j < D_qk)
  *   out[t,h,:] = sum_r softmax(logit)[r] * V[r, :D_v]               (bf16 result)
  *   lse[t,h]   = ln sum_r exp(logit[r])                             (fp32; -inf if R is empty)
- * where Kv[r] = kv row r of sequence seq(t) (times kv_scale[r] for DSA_FP8_E4M3) and V[r] =
+ * where Kv[r] = kv row r of sequence seq(t) (times kv_scale[r] for DSA_FP8_E4M3, element j times
+ * the scale of its tile j / 128 for DSA_FP8_E4M3_T128) and V[r] =
  * the first D_v columns of that same row when kv_v is NULL (latent cache), else row r of kv_v.
  * An out-of-range entry (< -1 or >= L) is skipped and recorded as DSA_DEVERR_INDEX_RANGE.
  *   q         device bf16 [T, H, D_qk]
  *   kv        device: row r of sequence q at kv + q*kv_seq_stride + r*kv_row_stride (bytes);
  *             bf16 or E4M3 codes per kv_dtype
  *   kv_v      device bf16 rows (row pitch v_row_stride, sequence pitch v_seq_stride) or NULL
- *   kv_scale  device fp32, DSA_FP8_E4M3 only: scale of row r of sequence q at
- *             kv_scale[q*L + r]; else NULL
+ *   kv_scale  device fp32: DSA_FP8_E4M3: scale of row r of sequence q at kv_scale[q*L + r];
+ *             DSA_FP8_E4M3_T128: the ceil(D_qk/128) tile scales of that row at
+ *             kv_scale[(q*L + r) * ceil(D_qk/128) ...]; NULL for bf16
  *   idx       device int32 [T, K]
  *   out       device bf16 [T, H, D_v];  lse  device fp32 [T, H] or NULL
  *   ws        device workspace of at least dsa_sparse_attn_workspace_size(T, H, K, D_v)
@@ -214,6 +219,14 @@ dsa_status dsa_quantize_fp8_rows(const void* x, int64_t x_row_stride, int rows, 
                                  uint8_t* codes, int64_t code_row_stride, float* scales,
                                  const int64_t* dst_rows, void* stream);
 
+/* dsa_quantize_fp8_tiles: dsa_quantize_fp8_rows applied to every `tile` consecutive elements of
+ * a row (the last tile may be shorter; 1 <= tile <= 1024), one fp32 scale per tile: destination
+ * row q's scales at scales + q * ceil(width / tile) (the page's per-token 128-element tiles for
+ * DSA_FP8_E4M3_T128 caches, "Day 0 Support for New LLM Architectures", Key Optimization 2). */
+dsa_status dsa_quantize_fp8_tiles(const void* x, int64_t x_row_stride, int rows, int width, int tile,
+                                  uint8_t* codes, int64_t code_row_stride, float* scales,
+                                  const int64_t* dst_rows, void* stream);
+
 /* --------------------------------------------------------------------------------------------
  * Fused chain: dsa_decode / dsa_prefill run steps 1-3 back to back on `stream` (the indexer's
  * "score-weight-TopK" chain followed by the sparse gather kernel, Day 0 Support for New LLM
@@ -253,6 +266,7 @@ typedef struct dsa_args {
    * sequence as described above.  Otherwise each cache is one pool of num_blocks * block_size
    * rows shared by all sequences: k_idx rows packed (row pitch d_idx * element size), k_idx_sf
    * rows of d_idx/32 bytes, kv / kv_v rows at kv_row_stride / v_row_stride, kv_scale one fp32
+   * (DSA_FP8_E4M3_T128: ceil(D_qk/128) fp32)
    * per row; the *_seq_stride fields are ignored.  Position s of sequence q (= query t /
    * q_per_seq) lives in pool row block_table[q * max_blocks + s / block_size] * block_size +
    * s % block_size.  Entries for every position a query sees (s < n_t) must hold block ids in

@@ -80,6 +80,7 @@ CASES = [
     ("tiny_separate_v_b64", "tiny_decode_l2k", dict(), None, 64),
     ("prefill_grouped_b64", "prefill_t4096_l128k_bf16", dict(T=8, q_per_seq=8, L=700, K=128, q_pos0=400), None, 64),
     ("long_row_split_b256", "decode_b1_l1m_mxfp8", dict(L=300000), None, 256),
+    ("fp8_tiles_b64", "decode_b8_l32k_mxfp8_kvt128", dict(T=2, L=1500, K=300), [1500, 640], 64),
 ]
 
 

@@ -236,10 +236,10 @@ def _random_idx(T, K, L, seed, pad=0):
     return idx
 
 
-@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv", ["bf16", "fp8", "fp8_t128"])
 @pytest.mark.parametrize("K,pad", [(2048, 0), (2048, 37), (100, 0), (64, 64)])
 def test_sparse_attn_mla(dsa, kv, K, pad):
-    base = "decode_b8_l32k_bf16" if kv == "bf16" else "decode_b8_l32k_mxfp8"
+    base = {"bf16": "decode_b8_l32k_bf16", "fp8": "decode_b8_l32k_mxfp8", "fp8_t128": "decode_b8_l32k_mxfp8_kvt128"}[kv]
     wl = synth.small_workload(base, T=3, L=4000, K=K)
     _attn_case(dsa, wl, _random_idx(3, K, 4000, K + pad, pad), kv)
 
@@ -287,7 +287,7 @@ _check_chain = check_chain
 
 
 @pytest.mark.parametrize("name", ["tiny_decode_l2k", "decode_b8_l32k_bf16", "decode_b8_l32k_mxfp8",
-                                  "decode_b8_varlen_bf16"])
+                                  "decode_b8_varlen_bf16", "decode_b8_l32k_mxfp8_kvt128"])
 def test_chain_full_decode_workloads(dsa, name):
     wl = synth.WORKLOADS[name]
     _check_chain(dsa, wl, synth.make_inputs(wl))

@@ -70,6 +70,15 @@ def test_quantize_fp8_rows_bit_exact(dsa, width):
     np.testing.assert_array_equal(codes.cpu().numpy(), want_codes)
 
 
+@pytest.mark.parametrize("width,tile", [(576, 128), (100, 32), (576, 1024), (130, 64)])
+def test_quantize_fp8_tiles_bit_exact(dsa, width, tile):
+    x = _rows(3 + width + tile, 211, width)
+    codes, s = dsa.dsa_quantize_fp8_tiles(x.cuda(), tile=tile)
+    want_codes, want_s = oracle.quantize_fp8_tiles(_f64(x), tile)
+    np.testing.assert_array_equal(s.cpu().numpy(), want_s)
+    np.testing.assert_array_equal(codes.cpu().numpy(), want_codes)
+
+
 def test_cache_append_writes_only_its_rows(dsa):
     # new tokens of 3 sequences appended at their next positions of [3][L] caches
     L, d, W = 50, 128, 576

@@ -13,13 +13,13 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libdsa.so")
 
 DSA_OK = 0
-DSA_BF16, DSA_FP8_E4M3, DSA_MXFP8_E4M3 = 0, 1, 2
+DSA_BF16, DSA_FP8_E4M3, DSA_MXFP8_E4M3, DSA_FP8_E4M3_T128 = 0, 1, 2, 3
 DEVERR = {0: "none", 1: "index out of range", 2: "wait timeout"}
 
 EXPORTS = (
     "dsa_status_string", "dsa_abi_version", "dsa_get_device_error", "dsa_index_score",
     "dsa_topk", "dsa_topk_workspace_size", "dsa_sparse_attn", "dsa_sparse_attn_workspace_size",
-    "dsa_quantize_mxfp8", "dsa_quantize_fp8_rows",
+    "dsa_quantize_mxfp8", "dsa_quantize_fp8_rows", "dsa_quantize_fp8_tiles",
     "dsa_workspace_size", "dsa_launch_count", "dsa_decode", "dsa_prefill", "dsa_topk_noalloc",
     "dsa_selftest_wait_timeout",
 )
@@ -74,6 +74,7 @@ def _load():
         "dsa_sparse_attn_workspace_size": (SZ, [I, I, I, I]),
         "dsa_quantize_mxfp8": (I, [P, I64, I, I, P, P, P, P]),
         "dsa_quantize_fp8_rows": (I, [P, I64, I, I, P, I64, P, P, P]),
+        "dsa_quantize_fp8_tiles": (I, [P, I64, I, I, I, P, I64, P, P, P]),
         "dsa_workspace_size": (I, [ctypes.POINTER(DsaArgs), I, ctypes.POINTER(SZ)]),
         "dsa_launch_count": (I, [ctypes.POINTER(DsaArgs), I, ctypes.POINTER(ctypes.c_int)]),
         "dsa_decode": (I, [ctypes.POINTER(DsaArgs), P, SZ, P]),

@@ -14,7 +14,7 @@ from . import _native as N
 
 __all__ = ["dsa_index_score", "dsa_topk", "dsa_sparse_attn", "DsaCall", "dsa_decode", "dsa_prefill",
            "dsa_workspace_size", "dsa_launch_count", "dsa_get_device_error", "ld_scores_for",
-           "dsa_quantize_mxfp8", "dsa_quantize_fp8_rows"]
+           "dsa_quantize_mxfp8", "dsa_quantize_fp8_rows", "dsa_quantize_fp8_tiles"]
 
 
 def _p(t: Optional[torch.Tensor]):
@@ -34,10 +34,14 @@ def _idx_dtype(t: torch.Tensor) -> int:
     raise TypeError(f"indexer tensors must be bfloat16 or uint8 (E4M3 codes), got {t.dtype}")
 
 
-def _kv_dtype(t: torch.Tensor) -> int:
+def _kv_dtype(t: torch.Tensor, scale: Optional[torch.Tensor] = None) -> int:
+    """bf16 rows; E4M3 rows with one scale per row (kv_scale without a last tile axis), or with
+    one scale per 128-element tile (kv_scale [..., ceil(D_qk / 128)] beside the rows' axes)."""
     if t.dtype == torch.bfloat16:
         return N.DSA_BF16
     if t.dtype == torch.uint8:
+        if scale is not None and scale.dim() == t.dim():
+            return N.DSA_FP8_E4M3_T128
         return N.DSA_FP8_E4M3
     raise TypeError(f"kv must be bfloat16 or uint8 (E4M3 codes), got {t.dtype}")
 
@@ -101,7 +105,7 @@ def dsa_sparse_attn(q, kv, idx, *, sm_scale, kv_v=None, kv_scale=None, D_v=None,
         ws = torch.zeros(need, dtype=torch.uint8, device=q.device)
     st = N.lib.dsa_sparse_attn(_p(q), _p(kv), _p(kv_v), _p(kv_scale), kv.stride(1) * kv.element_size(),
                                _seq_stride(kv), 0 if kv_v is None else kv_v.stride(1) * 2, _seq_stride(kv_v),
-                               _p(idx), T, q_per_seq, L, K, H, D_qk, D_v, float(sm_scale), _kv_dtype(kv),
+                               _p(idx), T, q_per_seq, L, K, H, D_qk, D_v, float(sm_scale), _kv_dtype(kv, kv_scale),
                                _p(out), _p(lse), _p(ws), 0 if ws is None else ws.numel(), _stream(stream))
     N.check(st, "dsa_sparse_attn")
     return out, lse
@@ -139,7 +143,7 @@ class DsaCall:
         a.T, a.q_per_seq, a.q_pos0, a.L, a.K = T, q_per_seq, q_pos0, L, K
         a.H_idx, a.d_idx, a.H, a.D_qk, a.D_v = H_idx, d_idx, H, D_qk, D_v
         a.sm_scale = float(sm_scale)
-        a.idx_dtype, a.kv_dtype = _idx_dtype(q_idx), _kv_dtype(kv)
+        a.idx_dtype, a.kv_dtype = _idx_dtype(q_idx), _kv_dtype(kv, kv_scale)
         ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
         a.n_valid = ptr(n_valid)
         a.q_idx, a.q_idx_sf, a.w = ptr(q_idx), ptr(q_idx_sf), ptr(w)
@@ -211,6 +215,20 @@ def dsa_quantize_fp8_rows(x, *, codes=None, scales=None, dst_rows=None, stream=N
     N.check(N.lib.dsa_quantize_fp8_rows(_p(x), x.stride(0), rows, width, _p(codes), codes.stride(0),
                                         _p(scales), _p(dst_rows), _stream(stream)),
             "dsa_quantize_fp8_rows")
+    return codes, scales
+
+
+def dsa_quantize_fp8_tiles(x, *, tile=128, codes=None, scales=None, dst_rows=None, stream=None):
+    """bf16 rows x [rows, width] -> (E4M3 codes, fp32 scales [rows, ceil(width / tile)]): one
+    scale per `tile` consecutive elements of a row; `dst_rows` as in dsa_quantize_mxfp8."""
+    rows, width = x.shape
+    nt = -(-width // tile)
+    if codes is None:
+        codes = torch.empty(rows, width, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(rows, nt, dtype=torch.float32, device=x.device)
+    N.check(N.lib.dsa_quantize_fp8_tiles(_p(x), x.stride(0), rows, width, tile, _p(codes), codes.stride(0),
+                                         _p(scales), _p(dst_rows), _stream(stream)), "dsa_quantize_fp8_tiles")
     return codes, scales
 
 

@@ -109,7 +109,8 @@ dsa_status check_sparse_attn(const void* q, const void* kv, const void* kv_v, co
                              int K, int H, int D_qk, int D_v, dsa_dtype kv_dtype, const void* out) {
   if (T < 0 || L < 0 || q_per_seq < 1 || T % q_per_seq != 0 || K < 1 || H < 1)
     return DSA_ERR_INVALID_ARG;
-  if (kv_dtype != DSA_BF16 && kv_dtype != DSA_FP8_E4M3) return DSA_ERR_UNSUPPORTED;
+  if (kv_dtype != DSA_BF16 && kv_dtype != DSA_FP8_E4M3 && kv_dtype != DSA_FP8_E4M3_T128)
+    return DSA_ERR_UNSUPPORTED;
   const bool mla = D_qk == 576 && D_v == 512 && !kv_v;
   const bool small = D_qk == 64 && D_v == 64 && !(kv_v && kv_dtype != DSA_BF16);
   if (!mla && !small) return DSA_ERR_UNSUPPORTED;
@@ -121,7 +122,8 @@ dsa_status check_sparse_attn(const void* q, const void* kv, const void* kv_v, co
   if (kv_row_stride % 16 != 0 || kv_row_stride < D_qk * elem) return DSA_ERR_INVALID_ARG;
   if (T / q_per_seq > 1 && (kv_seq_stride % 16 != 0 || kv_seq_stride < (int64_t)L * kv_row_stride))
     return DSA_ERR_INVALID_ARG;
-  if (kv_dtype == DSA_FP8_E4M3 && !kv_scale) return DSA_ERR_INVALID_ARG;
+  if (kv_dtype != DSA_BF16 && !kv_scale) return DSA_ERR_INVALID_ARG;
+  if (kv_dtype == DSA_FP8_E4M3_T128 && !mla) return DSA_ERR_UNSUPPORTED;
   if (kv_v) {
     if (!aligned16(kv_v) || v_row_stride % 16 != 0 || v_row_stride < D_v * 2) return DSA_ERR_INVALID_ARG;
     if (T / q_per_seq > 1 && (v_seq_stride % 16 != 0 || v_seq_stride < (int64_t)L * v_row_stride))
@@ -189,7 +191,7 @@ cudaError_t run_topk(const dsa_args& a, int t_off, int T, const float* scores, i
   p.kv = reinterpret_cast<const uint8_t*>(a.kv);
   p.kv_row_stride = a.kv_row_stride;
   p.kv_seq_stride = a.kv_seq_stride;
-  p.kv_bytes = a.D_qk * (a.kv_dtype == DSA_BF16 ? 2 : 1);
+  p.kv_bytes = a.D_qk * (a.kv_dtype == DSA_BF16 ? 2 : 1);  // (E4M3 rows: one byte per element)
   p.kv_v = reinterpret_cast<const uint8_t*>(a.kv_v);
   p.v_row_stride = a.v_row_stride;
   p.v_seq_stride = a.v_seq_stride;
@@ -226,7 +228,8 @@ cudaError_t run_sparse_attn(const dsa_args& a, int t_off, int T, const int32_t* 
   p.q_pos0 = a.q_pos0;
   p.n_valid = a.n_valid;
   p.pages = pages_of(a);
-  return launch_sparse_attn(p, a.D_qk, a.D_v, a.kv_dtype == DSA_FP8_E4M3, a.kv_v != nullptr, ws, st, pdl);
+  return launch_sparse_attn(p, a.D_qk, a.D_v, a.kv_dtype != DSA_BF16, a.kv_v != nullptr, ws, st, pdl,
+                            a.kv_dtype == DSA_FP8_E4M3_T128);
 }
 
 // ------------------------------------------------------------------------------------------

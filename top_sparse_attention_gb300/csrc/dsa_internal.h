@@ -141,8 +141,9 @@ struct SparseAttnParams {
 
 int sparse_attn_splits(int T, int H, int K);
 size_t sparse_attn_ws_bytes(int T, int H, int K, int D_v);
+// tiled: FP8 rows with one scale per 128-element tile (kv_scale [rows][ceil(D_qk / 128)])
 cudaError_t launch_sparse_attn(SparseAttnParams p, int D_qk, int D_v, bool fp8, bool sepv,
-                               void* ws, cudaStream_t stream, bool pdl);
+                               void* ws, cudaStream_t stream, bool pdl, bool tiled);
 
 // Argument checks and device facts shared with entry points defined outside dsa_api.cu.
 dsa_status check_topk_args(const float* scores, int64_t ld_scores, int T, int q_per_seq, int q_pos0,

@@ -234,6 +234,29 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) fp8_rows_quant_v8_kernel(
   if (lane == 0) scales[dst] = s;
 }
 
+// Tiles: one warp per (row, tile); the tile is quantised as a row of fp8_rows_quant_kernel.
+__global__ void __launch_bounds__(32 * kRowsPerCta) fp8_tiles_quant_kernel(
+    const __nv_bfloat16* __restrict__ x, int64_t x_row_stride, int rows, int width, int tile,
+    uint8_t* __restrict__ codes, int64_t code_row_stride, float* __restrict__ scales,
+    const int64_t* __restrict__ dst_rows) {
+  const int lane = threadIdx.x & 31;
+  const int ntile = (width + tile - 1) / tile;
+  const int64_t w = (int64_t)blockIdx.x * kRowsPerCta + (threadIdx.x >> 5);  // (row, tile) index
+  if (w >= (int64_t)rows * ntile) return;
+  const int r = (int)(w / ntile), c = (int)(w % ntile);
+  const int64_t dst = dst_rows ? dst_rows[r] : r;
+  if (dst < 0) return;
+  const int lo = c * tile, n = min(tile, width - lo);
+  const __nv_bfloat16* src = x + (int64_t)r * x_row_stride + lo;
+  float a = 0.f;
+  for (int j = lane; j < n; j += 32) a = fmaxf(a, fabsf(__bfloat162float(src[j])));
+  const float amax = warp_amax(a);
+  const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+  uint8_t* out = codes + dst * code_row_stride + lo;
+  for (int j = lane; j < n; j += 32) out[j] = to_e4m3(__fdiv_rn(__bfloat162float(src[j]), s));
+  if (lane == 0) scales[dst * ntile + c] = s;
+}
+
 bool aligned2(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1u) == 0; }
 bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
 
@@ -284,6 +307,24 @@ dsa_status dsa_quantize_fp8_rows(const void* x, int64_t x_row_stride, int rows, 
                         ? fp8_rows_quant_vec_kernel : fp8_rows_quant_kernel;
   kern<<<grid, 32 * kRowsPerCta, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
       reinterpret_cast<const __nv_bfloat16*>(x), x_row_stride, rows, width, codes, code_row_stride,
+      scales, dst_rows);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+dsa_status dsa_quantize_fp8_tiles(const void* x, int64_t x_row_stride, int rows, int width, int tile,
+                                  uint8_t* codes, int64_t code_row_stride, float* scales,
+                                  const int64_t* dst_rows, void* stream) {
+  if (rows < 0 || width <= 0 || tile < 1 || tile > 1024 || x_row_stride < width || code_row_stride < width)
+    return DSA_ERR_INVALID_ARG;
+  if (rows == 0) return DSA_OK;
+  if (!x || !codes || !scales || !aligned2(x)) return DSA_ERR_INVALID_ARG;
+  dsa_status s = check_device_arch();
+  if (s != DSA_OK) return s;
+  const int64_t items = (int64_t)rows * ((width + tile - 1) / tile);
+  const int64_t grid = (items + kRowsPerCta - 1) / kRowsPerCta;
+  if (grid >= (1ll << 31)) return DSA_ERR_UNSUPPORTED;
+  fp8_tiles_quant_kernel<<<(unsigned)grid, 32 * kRowsPerCta, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const __nv_bfloat16*>(x), x_row_stride, rows, width, tile, codes, code_row_stride,
       scales, dst_rows);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }

@@ -35,8 +35,11 @@ __device__ __forceinline__ uint32_t swz(int r, int c, int chunks) {
   return (uint32_t)((r * chunks + (c ^ (r & 7))) * 16);
 }
 
-template <int DQK, int DV, bool FP8, bool SEPV>
+// TILED (FP8 only): one fp32 scale per 128-element tile of a row instead of one per row.
+template <int DQK, int DV, bool FP8, bool SEPV, bool TILED>
 struct Cfg {
+  static constexpr int NSC = TILED ? (DQK + 127) / 128 : (FP8 ? 1 : 0);  // scales per row
+  static constexpr int PCOPIES = TILED ? DV / 128 : 1;  // P scaled per value tile (one per warp)
   static constexpr int GROUPS = FP8 ? 1 : 2;             // warp groups of 4 warps
   static constexpr int THREADS = 128 * GROUPS;
   static constexpr int ROW = DQK * 2 + 16;               // padded bf16 row (bytes)
@@ -49,10 +52,11 @@ struct Cfg {
   static constexpr int OFF_SLOT = OFF_Q + kHeads * ROW;
   static constexpr int OFF_CBUF = OFF_SLOT + 2 * SLOT;
   static constexpr int OFF_P = OFF_CBUF + CBUF;                      // per group
-  static constexpr int OFF_RED = OFF_P + GROUPS * kHeads * kRows * 2;  // per group: max, sum
+  static constexpr int OFF_RED = OFF_P + GROUPS * PCOPIES * kHeads * kRows * 2;  // per group: max, sum
   static constexpr int OFF_BAR = OFF_RED + GROUPS * 2 * 4 * kHeads * 4;
   static constexpr int OFF_IDX = OFF_BAR + 64;
-  static int bytes(int rows) { return OFF_IDX + rows * 4 * (FP8 ? 2 : 1); }
+  static int bytes(int rows) { return OFF_IDX + rows * 4 * (1 + NSC); }
+  static_assert(!TILED || (FP8 && DV == 512 && DQK % 16 == 0), "tiled scales: the 576/512 latent row");
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -86,10 +90,10 @@ __device__ __forceinline__ void group_sync(int g) {
   asm volatile("bar.sync %0, 128;" ::"r"(g + 1) : "memory");
 }
 
-template <int DQK, int DV, bool FP8, bool SEPV>
-__global__ void __launch_bounds__(Cfg<DQK, DV, FP8, SEPV>::THREADS, 1)
+template <int DQK, int DV, bool FP8, bool SEPV, bool TILED>
+__global__ void __launch_bounds__(Cfg<DQK, DV, FP8, SEPV, TILED>::THREADS, 1)
 sparse_attn_kernel(const SparseAttnParams p) {
-  using C = Cfg<DQK, DV, FP8, SEPV>;
+  using C = Cfg<DQK, DV, FP8, SEPV, TILED>;
   extern __shared__ __align__(128) uint8_t smem[];
   pdl_launch_dependents();  // the combine kernel may launch now; it waits for this grid's results
 
@@ -115,7 +119,7 @@ sparse_attn_kernel(const SparseAttnParams p) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);  // [0,1] slots, [2] q
   int* idx_s = reinterpret_cast<int*>(smem + C::OFF_IDX);
   float* scale_s = reinterpret_cast<float*>(smem + C::OFF_IDX + p.rows_per_split * 4);
-  uint8_t* p_s = smem + C::OFF_P + g * kHeads * kRows * 2;
+  uint8_t* p_s = smem + C::OFF_P + g * C::PCOPIES * kHeads * kRows * 2;
   float* red_max = reinterpret_cast<float*>(smem + C::OFF_RED) + g * 2 * 4 * kHeads;
   float* red_sum = red_max + 4 * kHeads;
 
@@ -123,7 +127,7 @@ sparse_attn_kernel(const SparseAttnParams p) {
   const bool paged = p.pages.table != nullptr;
   const uint8_t* kv_base = p.kv + (paged ? 0 : (int64_t)seq * p.kv_seq_stride);
   const uint8_t* v_base = SEPV ? p.kv_v + (paged ? 0 : (int64_t)seq * p.v_seq_stride) : nullptr;
-  const float* scale_base = FP8 ? p.kv_scale + (paged ? 0 : (int64_t)seq * p.L) : nullptr;
+  const float* scale_base = FP8 ? p.kv_scale + (paged ? 0 : (int64_t)seq * p.L * C::NSC) : nullptr;
 
   if (tid == 0) {
     mbar_init(&bars[0], 1);
@@ -159,7 +163,8 @@ sparse_attn_kernel(const SparseAttnParams p) {
       if (i >= 0 && paged) i = (int)page_row(p.pages, seq, i);
     }
     idx_s[j] = i;
-    if (FP8) scale_s[j] = (i >= 0) ? scale_base[i] : 0.f;
+#pragma unroll
+    for (int c = 0; c < C::NSC; ++c) scale_s[j * C::NSC + c] = (i >= 0) ? scale_base[(int64_t)i * C::NSC + c] : 0.f;
   }
   __syncthreads();
 
@@ -217,7 +222,7 @@ sparse_attn_kernel(const SparseAttnParams p) {
     const int slot_i = b & 1;
     ok = ok && mbar_wait(&bars[slot_i], (uint32_t)((C::GROUPS == 2 ? use : (use >> 1)) & 1), p.err);
     const int* ib = idx_s + b * kRows;
-    const float* sb = scale_s + b * kRows;
+    const float* sb = scale_s + b * kRows * C::NSC;  // C::NSC scales per row
     uint8_t* slot = smem + C::OFF_SLOT + slot_i * C::SLOT;
     uint8_t* kv_s = FP8 ? smem + C::OFF_CBUF : slot;
     uint8_t* v_s = SEPV ? slot + kRows * C::ROW : kv_s;
@@ -242,13 +247,37 @@ sparse_attn_kernel(const SparseAttnParams p) {
       const int mat = lane >> 3, rr = lane & 7;
       const uint32_t qa = smem_u32(q_s) + (rr + (mat & 1) * 8) * C::ROW + (mat >> 1) * 16;
       const uint32_t kb = smem_u32(kv_s) + (gw * 16 + rr + (mat >> 1) * 8) * C::ROW + (mat & 1) * 16;
+      if constexpr (TILED) {
+        // tile c of a row covers k-steps [8c, 8c + 8): each tile accumulates alone and is added
+        // with the tile's scale of each of this thread's four positions
+        for (int c = 0; c < C::NSC; ++c) {
+          float a_[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+          const int k1 = min(DQK / 16, 8 * c + 8);
 #pragma unroll 4
-      for (int ks = 0; ks < DQK / 16; ++ks) {
-        uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-        ldsm_x4(qa + ks * 32, a0, a1, a2, a3);
-        ldsm_x4(kb + ks * 32, b0, b1, b2, b3);
-        mma_bf16_16816(s[0], a0, a1, a2, a3, b0, b1);
-        mma_bf16_16816(s[1], a0, a1, a2, a3, b2, b3);
+          for (int ks = 8 * c; ks < k1; ++ks) {
+            uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+            ldsm_x4(qa + ks * 32, a0, a1, a2, a3);
+            ldsm_x4(kb + ks * 32, b0, b1, b2, b3);
+            mma_bf16_16816(a_[0], a0, a1, a2, a3, b0, b1);
+            mma_bf16_16816(a_[1], a0, a1, a2, a3, b2, b3);
+          }
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int pos = gw * 16 + j * 8 + (lane & 3) * 2 + (e & 1);
+              s[j][e] = fmaf(sb[pos * C::NSC + c], a_[j][e], s[j][e]);
+            }
+        }
+      } else {
+#pragma unroll 4
+        for (int ks = 0; ks < DQK / 16; ++ks) {
+          uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+          ldsm_x4(qa + ks * 32, a0, a1, a2, a3);
+          ldsm_x4(kb + ks * 32, b0, b1, b2, b3);
+          mma_bf16_16816(s[0], a0, a1, a2, a3, b0, b1);
+          mma_bf16_16816(s[1], a0, a1, a2, a3, b2, b3);
+        }
       }
     }
 
@@ -260,7 +289,7 @@ sparse_attn_kernel(const SparseAttnParams p) {
       for (int e = 0; e < 4; ++e) {
         const int pos = gw * 16 + j * 8 + (lane & 3) * 2 + (e & 1);
         float x = s[j][e] * p.scale_log2;
-        if (FP8) x *= sb[pos];
+        if (FP8 && !TILED) x *= sb[pos];  // the row's scale (tiles: applied per tile above)
         if (ib[pos] < 0) x = -INFINITY;
         s[j][e] = x;
         mx[e >> 1] = fmaxf(mx[e >> 1], x);
@@ -296,12 +325,23 @@ sparse_attn_kernel(const SparseAttnParams p) {
       for (int e = 0; e < 4; ++e) {
         pv[e] = exp2f(s[j][e] - m_use[e >> 1]);
         psum[e >> 1] += pv[e];
-        if (FP8) pv[e] *= sb[pos0 + (e & 1)];  // V rows carry the same per-row scale
+        if (FP8 && !TILED) pv[e] *= sb[pos0 + (e & 1)];  // V rows carry the same per-row scale
       }
-      // P is stored [head][position], swizzled in 16-byte chunks of 8 positions
+      // P is stored [head][position], swizzled in 16-byte chunks of 8 positions; with tiled
+      // scales one copy per value tile (warp gw's columns are tile gw), scaled by that tile
       const int c = pos0 >> 3, within = (pos0 & 7) * 2;
-      *reinterpret_cast<uint32_t*>(p_s + swz(r0, c, C::P_CHUNKS) + within) = pack_bf16(pv[0], pv[1]);
-      *reinterpret_cast<uint32_t*>(p_s + swz(r1, c, C::P_CHUNKS) + within) = pack_bf16(pv[2], pv[3]);
+      if constexpr (TILED) {
+#pragma unroll
+        for (int vt = 0; vt < C::PCOPIES; ++vt) {
+          uint8_t* pc = p_s + vt * (kHeads * kRows * 2);
+          const float s0 = sb[pos0 * C::NSC + vt], s1 = sb[(pos0 + 1) * C::NSC + vt];
+          *reinterpret_cast<uint32_t*>(pc + swz(r0, c, C::P_CHUNKS) + within) = pack_bf16(pv[0] * s0, pv[1] * s1);
+          *reinterpret_cast<uint32_t*>(pc + swz(r1, c, C::P_CHUNKS) + within) = pack_bf16(pv[2] * s0, pv[3] * s1);
+        }
+      } else {
+        *reinterpret_cast<uint32_t*>(p_s + swz(r0, c, C::P_CHUNKS) + within) = pack_bf16(pv[0], pv[1]);
+        *reinterpret_cast<uint32_t*>(p_s + swz(r1, c, C::P_CHUNKS) + within) = pack_bf16(pv[2], pv[3]);
+      }
     }
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
@@ -330,7 +370,7 @@ sparse_attn_kernel(const SparseAttnParams p) {
     // ---- O += P . V : warp gw owns value columns [gw*DV/4, (gw+1)*DV/4)
     {
       const int mat = lane >> 3, rr = lane & 7;
-      const uint32_t p_base = smem_u32(p_s);
+      const uint32_t p_base = smem_u32(p_s) + (TILED ? gw * (kHeads * kRows * 2) : 0);
       const uint32_t vb = smem_u32(v_s) + (rr + (mat & 1) * 8) * VR + (gw * (DV / 4) + (mat >> 1) * 8) * 2;
 #pragma unroll
       for (int kk = 0; kk < kRows / 16; ++kk) {
@@ -458,10 +498,10 @@ __global__ void __launch_bounds__(DV / 4) lse_combine_kernel(const SparseAttnPar
     p.lse[(int64_t)t * p.H + h] = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
 }
 
-template <int DQK, int DV, bool FP8, bool SEPV>
+template <int DQK, int DV, bool FP8, bool SEPV, bool TILED = false>
 cudaError_t launch_variant(const SparseAttnParams& p, cudaStream_t stream, bool pdl) {
-  using C = Cfg<DQK, DV, FP8, SEPV>;
-  auto kern = sparse_attn_kernel<DQK, DV, FP8, SEPV>;
+  using C = Cfg<DQK, DV, FP8, SEPV, TILED>;
+  auto kern = sparse_attn_kernel<DQK, DV, FP8, SEPV, TILED>;
   const int smem = C::bytes(p.rows_per_split);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -503,7 +543,7 @@ size_t sparse_attn_ws_bytes(int T, int H, int K, int D_v) {
 }
 
 cudaError_t launch_sparse_attn(SparseAttnParams p, int D_qk, int D_v, bool fp8, bool sepv, void* ws,
-                               cudaStream_t stream, bool pdl) {
+                               cudaStream_t stream, bool pdl, bool tiled) {
   p.splits = sparse_attn_splits(p.T, p.H, p.K);
   p.rows_per_split = rows_per_split(p.K, p.splits);
   if (p.rows_per_split > kMaxRows) return cudaErrorNotSupported;
@@ -512,6 +552,10 @@ cudaError_t launch_sparse_attn(SparseAttnParams p, int D_qk, int D_v, bool fp8, 
     const size_t rows = (size_t)p.T * p.H * p.splits;
     p.part_o = reinterpret_cast<float*>(ws);
     p.part_ml = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + align_up(rows * D_v * sizeof(float), 256));
+  }
+  if (tiled) {  // FP8 with one scale per 128-element tile: the 576/512 latent row only
+    if (!fp8 || D_qk != 576 || D_v != 512 || sepv) return cudaErrorNotSupported;
+    return launch_variant<576, 512, true, false, true>(p, stream, pdl);
   }
   if (D_qk == 576 && D_v == 512 && !sepv) {
     return fp8 ? launch_variant<576, 512, true, false>(p, stream, pdl)
