@@ -13,9 +13,10 @@
 // blocks (running max / sum, log2 domain).
 //
 // bf16 rows: two groups of 4 warps work on the two slots at the same time and merge their
-// (m, l, o) in shared memory at the end.  E4M3 rows (one group): the raw block is widened to bf16
-// in registers (exact: every E4M3 value is a bf16 value) into a compute buffer; the per-row scale
-// is folded into the logit and into the probability that multiplies V.
+// (m, l, o) in shared memory at the end.  E4M3 rows (one group of 8 warps for the 576/512 row):
+// the raw block is widened to bf16 in registers (exact: every E4M3 value is a bf16 value) into a
+// compute buffer; the per-row scale is folded into the logit and into the probability that
+// multiplies V.
 //
 // When K is split over S > 1 CTAs (so a small batch still covers every SM), each CTA writes its
 // partial (o, m, l) and a second kernel merges them with a log-sum-exp combine.
@@ -39,12 +40,21 @@ __device__ __forceinline__ uint32_t swz(int r, int c, int chunks) {
 template <int DQK, int DV, bool FP8, bool SEPV, bool TILED>
 struct Cfg {
   static constexpr int NSC = TILED ? (DQK + 127) / 128 : (FP8 ? 1 : 0);  // scales per row
-  static constexpr int PCOPIES = TILED ? DV / 128 : 1;  // P scaled per value tile (one per warp)
-  static constexpr int GROUPS = FP8 ? 1 : 2;             // warp groups of 4 warps
-  static constexpr int THREADS = 128 * GROUPS;
+  static constexpr int PCOPIES = TILED ? DV / 128 : 1;  // P scaled per value tile
+  // bf16: two independent groups of 4 warps, one block each.  E4M3 (576/512 row): one group of
+  // 8 warps on each block, so the widening is spread over twice the threads and two warps per
+  // scheduler hide each other's latencies; the compute buffer stays single.
+  static constexpr int GROUPS = FP8 ? 1 : 2;
+  static constexpr int GW = (FP8 && DV >= 128) ? 8 : 4;  // warps per group
+  static constexpr int GT = 32 * GW;                     // threads per group
+  static constexpr int THREADS = GT * GROUPS;
+  static constexpr int RPW = kRows / GW;                 // S rows per warp (n-tiles of 8: RPW / 8)
+  static constexpr int CPW = DV / GW;                    // value columns per warp
+  static_assert(RPW == 8 || RPW == 16, "S warp tile");
+  static_assert(CPW % 16 == 0 && (!TILED || 128 % CPW == 0), "P.V warp tile");
   static constexpr int ROW = DQK * 2 + 16;               // padded bf16 row (bytes)
   static constexpr int VROW = SEPV ? DV * 2 + 16 : 0;    // padded bf16 V row
-  static constexpr int RAWROW = FP8 ? DQK + 16 : 0;      // padded E4M3 row
+  static constexpr int RAWROW = FP8 ? DQK : 0;           // E4M3 row (read by 16-byte loads only)
   static constexpr int SLOT = FP8 ? kRows * RAWROW : kRows * (ROW + VROW);  // one load slot
   static constexpr int CBUF = FP8 ? kRows * ROW : 0;     // bf16 compute buffer (FP8)
   static constexpr int P_CHUNKS = kRows / 8;
@@ -53,7 +63,7 @@ struct Cfg {
   static constexpr int OFF_CBUF = OFF_SLOT + 2 * SLOT;
   static constexpr int OFF_P = OFF_CBUF + CBUF;                      // per group
   static constexpr int OFF_RED = OFF_P + GROUPS * PCOPIES * kHeads * kRows * 2;  // per group: max, sum
-  static constexpr int OFF_BAR = OFF_RED + GROUPS * 2 * 4 * kHeads * 4;
+  static constexpr int OFF_BAR = OFF_RED + GROUPS * 2 * GW * kHeads * 4;
   static constexpr int OFF_IDX = OFF_BAR + 64;
   static int bytes(int rows) { return OFF_IDX + rows * 4 * (1 + NSC); }
   static_assert(!TILED || (FP8 && DV == 512 && DQK % 16 == 0), "tiled scales: the 576/512 latent row");
@@ -64,13 +74,26 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// 4 E4M3 codes (one 32-bit word) -> 4 bf16 values (two 32-bit words), exact.
+// 4 E4M3 codes (one 32-bit word, code j in byte j) -> 4 bf16 values (x: codes 0, 1; y: codes 2,
+// 3), exact, on the integer and packed-bf16 pipes instead of the conversion unit.  A code
+// s eeee mmm placed as bf16 bits s 0000 eeee mmm 0000 is its E4M3 value times 2^-120: a normal
+// code's exponent e sits in the bf16 exponent field with bias 127 instead of 7, and a subnormal
+// code (e = 0, 0.mmm x 2^-6) becomes the bf16 subnormal 0.mmm x 2^-126.  One bf16 multiply by
+// 2^120 (exact: every product is an E4M3 value, representable in bf16) gives the value.  The
+// two NaN codes (0x7F, 0xFF) are not cache contents (the quantisers saturate); they read as
+// +-480.
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
 __device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
-  __half2_raw h0 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFFu), __NV_E4M3);
-  __half2_raw h1 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
-  float2 f0 = __half22float2(*reinterpret_cast<__half2*>(&h0));
-  float2 f1 = __half22float2(*reinterpret_cast<__half2*>(&h1));
-  return make_uint2(pack_bf16(f0.x, f0.y), pack_bf16(f1.x, f1.y));
+  constexpr uint32_t kTwo120 = 0x7B807B80u;  // bf16 2^120 in both halves (exponent field 247)
+  const uint32_t mag = w & 0x7F7F7F7Fu, sgn = w & 0x80808080u;
+  // magnitude byte j -> low byte of half j (times 16: bits 4..10); sign byte j -> high byte
+  const uint32_t lo = __byte_perm(mag, 0u, 0x5140) * 16u + __byte_perm(sgn, 0u, 0x1404);
+  const uint32_t hi = __byte_perm(mag, 0u, 0x7362) * 16u + __byte_perm(sgn, 0u, 0x3424);
+  return make_uint2(bf16x2_mul(lo, kTwo120), bf16x2_mul(hi, kTwo120));
 }
 
 // Bulk copy of `bytes` (a multiple of 16) from global to shared memory on the TMA engine.
@@ -86,8 +109,9 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
+template <int NTHREADS>
 __device__ __forceinline__ void group_sync(int g) {
-  asm volatile("bar.sync %0, 128;" ::"r"(g + 1) : "memory");
+  asm volatile("bar.sync %0, %1;" ::"r"(g + 1), "n"(NTHREADS) : "memory");
 }
 
 template <int DQK, int DV, bool FP8, bool SEPV, bool TILED>
@@ -99,9 +123,9 @@ sparse_attn_kernel(const SparseAttnParams p) {
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
-  const int g = tid >> 7;          // warp group
-  const int gw = (tid >> 5) & 3;   // warp within the group
-  const int gt = tid & 127;        // thread within the group
+  const int g = tid / C::GT;              // warp group
+  const int gw = (tid >> 5) % C::GW;      // warp within the group
+  const int gt = tid % C::GT;             // thread within the group
   const int split = blockIdx.x;
   const int t = blockIdx.y;
   const int h0 = blockIdx.z * kHeads;
@@ -120,8 +144,8 @@ sparse_attn_kernel(const SparseAttnParams p) {
   int* idx_s = reinterpret_cast<int*>(smem + C::OFF_IDX);
   float* scale_s = reinterpret_cast<float*>(smem + C::OFF_IDX + p.rows_per_split * 4);
   uint8_t* p_s = smem + C::OFF_P + g * C::PCOPIES * kHeads * kRows * 2;
-  float* red_max = reinterpret_cast<float*>(smem + C::OFF_RED) + g * 2 * 4 * kHeads;
-  float* red_sum = red_max + 4 * kHeads;
+  float* red_max = reinterpret_cast<float*>(smem + C::OFF_RED) + g * 2 * C::GW * kHeads;
+  float* red_sum = red_max + C::GW * kHeads;
 
   // paged caches: rows are pool rows found through the page table (no per-sequence base)
   const bool paged = p.pages.table != nullptr;
@@ -151,7 +175,7 @@ sparse_attn_kernel(const SparseAttnParams p) {
   if (tid == 0) mbar_arrive(&bars[2]);
   pdl_wait();  // the index rows come from the previous kernel in the stream
 
-  // this CTA's index rows (and FP8 row scales), checked against [-1, L); kept as cache rows
+  // this CTA's index rows, checked against [-1, L); kept as cache rows
   for (int j = tid; j < nblk * kRows; j += C::THREADS) {
     int i = -1;
     if (j < nrows) {
@@ -163,8 +187,6 @@ sparse_attn_kernel(const SparseAttnParams p) {
       if (i >= 0 && paged) i = (int)page_row(p.pages, seq, i);
     }
     idx_s[j] = i;
-#pragma unroll
-    for (int c = 0; c < C::NSC; ++c) scale_s[j * C::NSC + c] = (i >= 0) ? scale_base[(int64_t)i * C::NSC + c] : 0.f;
   }
   __syncthreads();
 
@@ -173,7 +195,7 @@ sparse_attn_kernel(const SparseAttnParams p) {
     uint8_t* slot = smem + C::OFF_SLOT + (b & 1) * C::SLOT;
     uint64_t* bar = &bars[b & 1];
     fence_proxy_async_smem();  // earlier generic reads / zero-fills of this slot come first
-    for (int r = gt; r < kRows; r += 128) {
+    for (int r = gt; r < kRows; r += C::GT) {
       const int i = idx_s[b * kRows + r];
       if (FP8) {
         uint8_t* dst = slot + r * C::RAWROW;
@@ -197,7 +219,7 @@ sparse_attn_kernel(const SparseAttnParams p) {
         }
       }
     }
-    group_sync(g);  // every expect_tx of the block precedes the arrival that opens the phase
+    group_sync<C::GT>(g);  // every expect_tx of the block precedes the arrival that opens the phase
     if (gt == 0) mbar_arrive(bar);
   };
   if (C::GROUPS == 2) {
@@ -206,13 +228,25 @@ sparse_attn_kernel(const SparseAttnParams p) {
     if (nblk > 0) issue(0);
     if (nblk > 1) issue(1);
   }
+  // E4M3 scales of the rows, fetched while the first blocks are on their way; the first block's
+  // widening barrier (every thread of the CTA) orders them before any use
+  if constexpr (C::NSC > 0) {
+    for (int j = tid; j < nblk * kRows; j += C::THREADS) {  // one row's scales per thread, all in flight
+      const int i = idx_s[j];
+      float v[C::NSC];
+#pragma unroll
+      for (int c = 0; c < C::NSC; ++c) v[c] = i >= 0 ? scale_base[(int64_t)i * C::NSC + c] : 0.f;
+#pragma unroll
+      for (int c = 0; c < C::NSC; ++c) scale_s[j * C::NSC + c] = v[c];
+    }
+  }
   bool ok = mbar_wait(&bars[2], 0, p.err);  // q is in shared memory
 
   // per-thread softmax state for heads r0 = lane/4 and r1 = lane/4 + 8
   const int r0 = lane >> 2, r1 = r0 + 8;
   float m_run[2] = {-INFINITY, -INFINITY};
   float l_run[2] = {0.f, 0.f};
-  constexpr int NT = DV / 32;  // n-tiles of 8 columns per warp in P.V
+  constexpr int NT = C::CPW / 8;  // n-tiles of 8 columns per warp in P.V
   float acc[NT][4];
 #pragma unroll
   for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
@@ -228,66 +262,93 @@ sparse_attn_kernel(const SparseAttnParams p) {
     uint8_t* v_s = SEPV ? slot + kRows * C::ROW : kv_s;
     constexpr int VR = SEPV ? C::VROW : C::ROW;
     if (FP8) {
-      constexpr int PIECES = DQK / 16;
-      for (int id = gt; id < kRows * PIECES; id += 128) {
-        const int r = id / PIECES, c = id % PIECES;
+      constexpr int PIECES = DQK / 16;  // 16 codes each
+      auto widen = [&](int r, int c) {
         const uint4 w = *reinterpret_cast<const uint4*>(slot + r * C::RAWROW + c * 16);
         const uint2 a = e4m3x4_to_bf16x4(w.x), bb = e4m3x4_to_bf16x4(w.y);
         const uint2 cc = e4m3x4_to_bf16x4(w.z), d = e4m3x4_to_bf16x4(w.w);
         *reinterpret_cast<uint4*>(kv_s + r * C::ROW + 32 * c) = make_uint4(a.x, a.y, bb.x, bb.y);
         *reinterpret_cast<uint4*>(kv_s + r * C::ROW + 32 * c + 16) = make_uint4(cc.x, cc.y, d.x, d.y);
+      };
+      if constexpr (C::GT == 4 * kRows && PIECES % 4 == 0) {
+        // thread -> (row gt / 4, quarter gt % 4 of it): consecutive pieces, no index division;
+        // the 8 threads of a quarter-warp load from and store to distinct bank groups
+        const int r = gt >> 2, c0 = (gt & 3) * (PIECES / 4);
+#pragma unroll 3
+        for (int c = c0; c < c0 + PIECES / 4; ++c) widen(r, c);
+      } else {
+        for (int id = gt; id < kRows * PIECES; id += C::GT) widen(id / PIECES, id % PIECES);
       }
-      group_sync(g);
+      group_sync<C::GT>(g);
       if (ok && b + 2 < nblk) issue(b + 2);  // the raw slot of block b is free again
     }
 
-    // ---- S = q . K^T : warp gw owns block rows [16gw, 16gw+16) as two n-tiles of 8
-    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // ---- S = q . K^T : warp gw owns block rows [RPW gw, RPW gw + RPW) as NJ n-tiles of 8
+    constexpr int NJ = C::RPW / 8;
+    float s[NJ][4];
     {
       const int mat = lane >> 3, rr = lane & 7;
       const uint32_t qa = smem_u32(q_s) + (rr + (mat & 1) * 8) * C::ROW + (mat >> 1) * 16;
-      const uint32_t kb = smem_u32(kv_s) + (gw * 16 + rr + (mat >> 1) * 8) * C::ROW + (mat & 1) * 16;
-      if constexpr (TILED) {
-        // tile c of a row covers k-steps [8c, 8c + 8): each tile accumulates alone and is added
-        // with the tile's scale of each of this thread's four positions
-        for (int c = 0; c < C::NSC; ++c) {
-          float a_[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-          const int k1 = min(DQK / 16, 8 * c + 8);
+      // NJ = 2: the four 8x8 matrices of one k-step are (rows 0-7 | 8-15) x (k 0-7 | 8-15);
+      // NJ = 1: rows 0-7 x the four 8-wide k groups of two k-steps
+      const uint32_t kb = NJ == 2 ? smem_u32(kv_s) + (gw * 16 + rr + (mat >> 1) * 8) * C::ROW + (mat & 1) * 16
+                                  : smem_u32(kv_s) + (gw * 8 + rr) * C::ROW + mat * 16;
+      // o = the partial logits over k-steps [k0, k1) (both even when NJ = 1)
+      auto s_range = [&](int k0, int k1, float (&o)[NJ][4]) {
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+        if constexpr (NJ == 2) {
 #pragma unroll 4
-          for (int ks = 8 * c; ks < k1; ++ks) {
+          for (int ks = k0; ks < k1; ++ks) {
             uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
             ldsm_x4(qa + ks * 32, a0, a1, a2, a3);
             ldsm_x4(kb + ks * 32, b0, b1, b2, b3);
-            mma_bf16_16816(a_[0], a0, a1, a2, a3, b0, b1);
-            mma_bf16_16816(a_[1], a0, a1, a2, a3, b2, b3);
+            mma_bf16_16816(o[0], a0, a1, a2, a3, b0, b1);
+            mma_bf16_16816(o[NJ - 1], a0, a1, a2, a3, b2, b3);
+          }
+        } else {
+          float odd[4] = {0.f, 0.f, 0.f, 0.f};  // a second chain halves the MMA dependency depth
+#pragma unroll 2
+          for (int ks = k0; ks < k1; ks += 2) {
+            uint32_t a0, a1, a2, a3, c0, c1, c2, c3, b0, b1, b2, b3;
+            ldsm_x4(kb + ks * 32, b0, b1, b2, b3);
+            ldsm_x4(qa + ks * 32, a0, a1, a2, a3);
+            ldsm_x4(qa + ks * 32 + 32, c0, c1, c2, c3);
+            mma_bf16_16816(o[0], a0, a1, a2, a3, b0, b1);
+            mma_bf16_16816(odd, c0, c1, c2, c3, b2, b3);
           }
 #pragma unroll
-          for (int j = 0; j < 2; ++j)
+          for (int e = 0; e < 4; ++e) o[0][e] += odd[e];
+        }
+      };
+      if constexpr (TILED) {
+        // tile c of a row covers k-steps [8c, 8c + 8): each tile accumulates alone and is added
+        // with the tile's scale of each of this thread's positions
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+        for (int c = 0; c < C::NSC; ++c) {
+          float a_[NJ][4];
+          s_range(8 * c, min(DQK / 16, 8 * c + 8), a_);
+#pragma unroll
+          for (int j = 0; j < NJ; ++j)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int pos = gw * 16 + j * 8 + (lane & 3) * 2 + (e & 1);
+              const int pos = gw * C::RPW + j * 8 + (lane & 3) * 2 + (e & 1);
               s[j][e] = fmaf(sb[pos * C::NSC + c], a_[j][e], s[j][e]);
             }
         }
       } else {
-#pragma unroll 4
-        for (int ks = 0; ks < DQK / 16; ++ks) {
-          uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-          ldsm_x4(qa + ks * 32, a0, a1, a2, a3);
-          ldsm_x4(kb + ks * 32, b0, b1, b2, b3);
-          mma_bf16_16816(s[0], a0, a1, a2, a3, b0, b1);
-          mma_bf16_16816(s[1], a0, a1, a2, a3, b2, b3);
-        }
+        s_range(0, DQK / 16, s);
       }
     }
 
     // ---- block softmax statistics (log2 domain)
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
+    for (int j = 0; j < NJ; ++j) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int pos = gw * 16 + j * 8 + (lane & 3) * 2 + (e & 1);
+        const int pos = gw * C::RPW + j * 8 + (lane & 3) * 2 + (e & 1);
         float x = s[j][e] * p.scale_log2;
         if (FP8 && !TILED) x *= sb[pos];  // the row's scale (tiles: applied per tile above)
         if (ib[pos] < 0) x = -INFINITY;
@@ -304,13 +365,14 @@ sparse_attn_kernel(const SparseAttnParams p) {
       red_max[gw * kHeads + r0] = mx[0];
       red_max[gw * kHeads + r1] = mx[1];
     }
-    group_sync(g);
+    group_sync<C::GT>(g);
     float m_use[2], alpha[2];
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const int h = hh ? r1 : r0;
-      const float mb = fmaxf(fmaxf(red_max[h], red_max[kHeads + h]),
-                             fmaxf(red_max[2 * kHeads + h], red_max[3 * kHeads + h]));
+      float mb = red_max[h];
+#pragma unroll
+      for (int w = 1; w < C::GW; ++w) mb = fmaxf(mb, red_max[w * kHeads + h]);
       const float m_new = fmaxf(m_run[hh], mb);
       m_use[hh] = (m_new == -INFINITY) ? 0.f : m_new;
       alpha[hh] = exp2f(m_run[hh] - m_use[hh]);
@@ -318,8 +380,8 @@ sparse_attn_kernel(const SparseAttnParams p) {
     }
     float psum[2] = {0.f, 0.f};
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int pos0 = gw * 16 + j * 8 + (lane & 3) * 2;
+    for (int j = 0; j < NJ; ++j) {
+      const int pos0 = gw * C::RPW + j * 8 + (lane & 3) * 2;
       float pv[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -328,7 +390,7 @@ sparse_attn_kernel(const SparseAttnParams p) {
         if (FP8 && !TILED) pv[e] *= sb[pos0 + (e & 1)];  // V rows carry the same per-row scale
       }
       // P is stored [head][position], swizzled in 16-byte chunks of 8 positions; with tiled
-      // scales one copy per value tile (warp gw's columns are tile gw), scaled by that tile
+      // scales one copy per value tile, scaled by that tile
       const int c = pos0 >> 3, within = (pos0 & 7) * 2;
       if constexpr (TILED) {
 #pragma unroll
@@ -359,19 +421,21 @@ sparse_attn_kernel(const SparseAttnParams p) {
       acc[i][2] *= alpha[1];
       acc[i][3] *= alpha[1];
     }
-    group_sync(g);
+    group_sync<C::GT>(g);
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const int h = hh ? r1 : r0;
-      const float sum = red_sum[h] + red_sum[kHeads + h] + red_sum[2 * kHeads + h] + red_sum[3 * kHeads + h];
+      float sum = red_sum[h];
+#pragma unroll
+      for (int w = 1; w < C::GW; ++w) sum += red_sum[w * kHeads + h];
       l_run[hh] = l_run[hh] * alpha[hh] + sum;
     }
 
-    // ---- O += P . V : warp gw owns value columns [gw*DV/4, (gw+1)*DV/4)
+    // ---- O += P . V : warp gw owns value columns [CPW gw, CPW gw + CPW), inside one value tile
     {
       const int mat = lane >> 3, rr = lane & 7;
-      const uint32_t p_base = smem_u32(p_s) + (TILED ? gw * (kHeads * kRows * 2) : 0);
-      const uint32_t vb = smem_u32(v_s) + (rr + (mat & 1) * 8) * VR + (gw * (DV / 4) + (mat >> 1) * 8) * 2;
+      const uint32_t p_base = smem_u32(p_s) + (TILED ? (gw * C::CPW / 128) * (kHeads * kRows * 2) : 0);
+      const uint32_t vb = smem_u32(v_s) + (rr + (mat & 1) * 8) * VR + (gw * C::CPW + (mat >> 1) * 8) * 2;
 #pragma unroll
       for (int kk = 0; kk < kRows / 16; ++kk) {
         uint32_t a0, a1, a2, a3;
@@ -385,7 +449,7 @@ sparse_attn_kernel(const SparseAttnParams p) {
         }
       }
     }
-    group_sync(g);  // the slot and P are rewritten next
+    group_sync<C::GT>(g);  // the slot and P are rewritten next
     if (!FP8 && ok && b + 2 < nblk) issue(b + 2);
   }
   // ---- merge the second group into the first (bf16 only)
@@ -397,7 +461,7 @@ sparse_attn_kernel(const SparseAttnParams p) {
       // element i of thread gt at [i][gt]: consecutive lanes hit consecutive 16-byte words
       float4* st = reinterpret_cast<float4*>(stage) + gt;
 #pragma unroll
-      for (int i = 0; i < NT; ++i) st[i * 128] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      for (int i = 0; i < NT; ++i) st[i * C::GT] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
       if (gw == 0 && (lane & 3) == 0) {
         ml[r0] = make_float2(m_run[0], l_run[0]);
         ml[r1] = make_float2(m_run[1], l_run[1]);
@@ -416,14 +480,14 @@ sparse_attn_kernel(const SparseAttnParams p) {
       m_run[hh] = m_new;
 #pragma unroll
       for (int i = 0; i < NT; ++i) {
-        const float4 v = st[i * 128];
+        const float4 v = st[i * C::GT];
         acc[i][2 * hh] = acc[i][2 * hh] * a0 + (hh ? v.z : v.x) * a1;
         acc[i][2 * hh + 1] = acc[i][2 * hh + 1] * a0 + (hh ? v.w : v.y) * a1;
       }
     }
   }
 
-  const int col0 = gw * (DV / 4) + (lane & 3) * 2;
+  const int col0 = gw * C::CPW + (lane & 3) * 2;
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
     const int h = h0 + (hh ? r1 : r0);
