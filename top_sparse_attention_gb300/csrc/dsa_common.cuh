@@ -437,6 +437,11 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
+// Prefetch of the cache line holding `p` into L2 (no alignment requirement).
+__device__ __forceinline__ void prefetch_line_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
+
 // ------------------------------------------------------------------------------------------
 // Programmatic dependent launch (no-ops when the launch did not opt in)
 

@@ -347,6 +347,19 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
           }
         }
       }
+      if constexpr (MX) {
+        // the tile's key-scale words (4 bytes per row; 32 rows per lane, inside one cache block)
+        // into L2 now: the epilogue loads them a stage ring later, and an L2 hit keeps that
+        // load off its per-tile path
+        const int pos = w.tile * kTileM + 32 * lane;
+        if (lane < kTileM / 32 && pos < w.n_max) {
+          const uint8_t* a = paged ? p.k_sf + page_row(p.pages, w.seq, pos) * 4
+                                   : p.k_sf + (int64_t)w.seq * p.k_sf_seq_stride + (int64_t)pos * 4;
+          const int last = min(32, w.n_max - pos) * 4 - 4;
+          prefetch_line_l2(a);
+          prefetch_line_l2(a + last);
+        }
+      }
       __syncwarp();
       ++it;
     }
