@@ -728,7 +728,7 @@ def end_to_end(dsa, wl, cpu_sets, dev_sets, stream, steps, inflight=1):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--inflight", type=int, default=4,
+    ap.add_argument("--inflight", type=int, default=6,
                     help="independent batches in flight (consecutive steps on different streams)")
     ap.add_argument("--steps", type=int, default=20000)  # ~1 s of decode steps: clock samples
     ap.add_argument("--warmup", type=int, default=20)
