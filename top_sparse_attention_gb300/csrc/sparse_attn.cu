@@ -13,10 +13,12 @@
 // blocks (running max / sum, log2 domain).
 //
 // bf16 rows: two groups of 4 warps work on the two slots at the same time and merge their
-// (m, l, o) in shared memory at the end.  E4M3 rows (one group of 8 warps for the 576/512 row):
-// the raw block is widened to bf16 in registers (exact: every E4M3 value is a bf16 value) into a
-// compute buffer; the per-row scale is folded into the logit and into the probability that
-// multiplies V.
+// (m, l, o) in shared memory at the end.  E4M3 rows stay raw in shared memory: the tensor cores
+// turn them into the bf16 operands of the same MMAs.  An E4M3 MMA of 16 raw rows with a 0/1
+// selection matrix yields, in fp32 and exactly, the values in the register layout of a bf16 B
+// fragment (the K side of q.K^T with the selection on the right, the V side of P.V with the
+// selection on the left); the upper halves of those fp32 are the bf16 values.  The per-row scale
+// is folded into the logit and into the probability that multiplies V.
 //
 // When K is split over S > 1 CTAs (so a small batch still covers every SM), each CTA writes its
 // partial (o, m, l) and a second kernel merges them with a log-sum-exp combine.
@@ -41,27 +43,23 @@ template <int DQK, int DV, bool FP8, bool SEPV, bool TILED>
 struct Cfg {
   static constexpr int NSC = TILED ? (DQK + 127) / 128 : (FP8 ? 1 : 0);  // scales per row
   static constexpr int PCOPIES = TILED ? DV / 128 : 1;  // P scaled per value tile
-  // bf16: two independent groups of 4 warps, one block each.  E4M3 (576/512 row): one group of
-  // 8 warps on each block, so the widening is spread over twice the threads and two warps per
-  // scheduler hide each other's latencies; the compute buffer stays single.
-  static constexpr int GROUPS = FP8 ? 1 : 2;
-  static constexpr int GW = (FP8 && DV >= 128) ? 8 : 4;  // warps per group
+  // two independent groups of 4 warps, one block each (E4M3 rows too: the MMAs read them raw)
+  static constexpr int GROUPS = 2;
+  static constexpr int GW = 4;                           // warps per group
   static constexpr int GT = 32 * GW;                     // threads per group
   static constexpr int THREADS = GT * GROUPS;
-  static constexpr int RPW = kRows / GW;                 // S rows per warp (n-tiles of 8: RPW / 8)
+  static constexpr int RPW = kRows / GW;                 // S rows per warp: two n-tiles of 8
   static constexpr int CPW = DV / GW;                    // value columns per warp
-  static_assert(RPW == 8 || RPW == 16, "S warp tile");
-  static_assert(CPW % 16 == 0 && (!TILED || 128 % CPW == 0), "P.V warp tile");
+  static_assert(RPW == 16, "S warp tile");
+  static_assert(CPW % 16 == 0 && (!TILED || CPW == 128), "P.V warp tile");
   static constexpr int ROW = DQK * 2 + 16;               // padded bf16 row (bytes)
   static constexpr int VROW = SEPV ? DV * 2 + 16 : 0;    // padded bf16 V row
-  static constexpr int RAWROW = FP8 ? DQK : 0;           // E4M3 row (read by 16-byte loads only)
+  static constexpr int RAWROW = FP8 ? DQK + 16 : 0;      // padded E4M3 row
   static constexpr int SLOT = FP8 ? kRows * RAWROW : kRows * (ROW + VROW);  // one load slot
-  static constexpr int CBUF = FP8 ? kRows * ROW : 0;     // bf16 compute buffer (FP8)
   static constexpr int P_CHUNKS = kRows / 8;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_SLOT = OFF_Q + kHeads * ROW;
-  static constexpr int OFF_CBUF = OFF_SLOT + 2 * SLOT;
-  static constexpr int OFF_P = OFF_CBUF + CBUF;                      // per group
+  static constexpr int OFF_P = OFF_SLOT + 2 * SLOT;                  // per group
   static constexpr int OFF_RED = OFF_P + GROUPS * PCOPIES * kHeads * kRows * 2;  // per group: max, sum
   static constexpr int OFF_BAR = OFF_RED + GROUPS * 2 * GW * kHeads * 4;
   static constexpr int OFF_IDX = OFF_BAR + 64;
@@ -74,26 +72,21 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// 4 E4M3 codes (one 32-bit word, code j in byte j) -> 4 bf16 values (x: codes 0, 1; y: codes 2,
-// 3), exact, on the integer and packed-bf16 pipes instead of the conversion unit.  A code
-// s eeee mmm placed as bf16 bits s 0000 eeee mmm 0000 is its E4M3 value times 2^-120: a normal
-// code's exponent e sits in the bf16 exponent field with bias 127 instead of 7, and a subnormal
-// code (e = 0, 0.mmm x 2^-6) becomes the bf16 subnormal 0.mmm x 2^-126.  One bf16 multiply by
-// 2^120 (exact: every product is an E4M3 value, representable in bf16) gives the value.  The
-// two NaN codes (0x7F, 0xFF) are not cache contents (the quantisers saturate); they read as
-// +-480.
-__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
+// D = A B for a 16x32 E4M3 A (row-major fragments) and a 32x8 E4M3 B (column-major fragments),
+// fp32 result (m16n8k32).  With a 0/1 selection matrix on one side it copies E4M3 values into an
+// fp32 fragment exactly: one product of an E4M3 value with 1, all others zero.
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%10, %10, %10, %10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
-__device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
-  constexpr uint32_t kTwo120 = 0x7B807B80u;  // bf16 2^120 in both halves (exponent field 247)
-  const uint32_t mag = w & 0x7F7F7F7Fu, sgn = w & 0x80808080u;
-  // magnitude byte j -> low byte of half j (times 16: bits 4..10); sign byte j -> high byte
-  const uint32_t lo = __byte_perm(mag, 0u, 0x5140) * 16u + __byte_perm(sgn, 0u, 0x1404);
-  const uint32_t hi = __byte_perm(mag, 0u, 0x7362) * 16u + __byte_perm(sgn, 0u, 0x3424);
-  return make_uint2(bf16x2_mul(lo, kTwo120), bf16x2_mul(hi, kTwo120));
+
+// bf16 pair (lo, hi) of two fp32 that hold E4M3 values: such an fp32 has at most 4 significant
+// bits, so its upper half is the bf16 of the same value.
+__device__ __forceinline__ uint32_t bf16x2_of_e4m3_f32(float lo, float hi) {
+  return __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);
 }
 
 // Bulk copy of `bytes` (a multiple of 16) from global to shared memory on the TMA engine.
@@ -228,8 +221,7 @@ sparse_attn_kernel(const SparseAttnParams p) {
     if (nblk > 0) issue(0);
     if (nblk > 1) issue(1);
   }
-  // E4M3 scales of the rows, fetched while the first blocks are on their way; the first block's
-  // widening barrier (every thread of the CTA) orders them before any use
+  // E4M3 scales of the rows, fetched while the first blocks are on their way
   if constexpr (C::NSC > 0) {
     for (int j = tid; j < nblk * kRows; j += C::THREADS) {  // one row's scales per thread, all in flight
       const int i = idx_s[j];
@@ -239,6 +231,16 @@ sparse_attn_kernel(const SparseAttnParams p) {
 #pragma unroll
       for (int c = 0; c < C::NSC; ++c) scale_s[j * C::NSC + c] = v[c];
     }
+    __syncthreads();
+  }
+  // selection columns for the E4M3 expansions: byte i of a B fragment register of this lane holds
+  // row 4 (lane % 4) + i of column lane / 4; E4M3 1.0 = 0x38 where that row is the column (sel0)
+  // or the column + 8 (sel8)
+  uint32_t sel0 = 0, sel8 = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    sel0 |= (4 * (lane & 3) + i == (lane >> 2) ? 0x38u : 0u) << (8 * i);
+    sel8 |= (4 * (lane & 3) + i == (lane >> 2) + 8 ? 0x38u : 0u) << (8 * i);
   }
   bool ok = mbar_wait(&bars[2], 0, p.err);  // q is in shared memory
 
@@ -258,77 +260,63 @@ sparse_attn_kernel(const SparseAttnParams p) {
     const int* ib = idx_s + b * kRows;
     const float* sb = scale_s + b * kRows * C::NSC;  // C::NSC scales per row
     uint8_t* slot = smem + C::OFF_SLOT + slot_i * C::SLOT;
-    uint8_t* kv_s = FP8 ? smem + C::OFF_CBUF : slot;
+    uint8_t* kv_s = slot;
     uint8_t* v_s = SEPV ? slot + kRows * C::ROW : kv_s;
     constexpr int VR = SEPV ? C::VROW : C::ROW;
-    if (FP8) {
-      constexpr int PIECES = DQK / 16;  // 16 codes each
-      auto widen = [&](int r, int c) {
-        const uint4 w = *reinterpret_cast<const uint4*>(slot + r * C::RAWROW + c * 16);
-        const uint2 a = e4m3x4_to_bf16x4(w.x), bb = e4m3x4_to_bf16x4(w.y);
-        const uint2 cc = e4m3x4_to_bf16x4(w.z), d = e4m3x4_to_bf16x4(w.w);
-        *reinterpret_cast<uint4*>(kv_s + r * C::ROW + 32 * c) = make_uint4(a.x, a.y, bb.x, bb.y);
-        *reinterpret_cast<uint4*>(kv_s + r * C::ROW + 32 * c + 16) = make_uint4(cc.x, cc.y, d.x, d.y);
-      };
-      if constexpr (C::GT == 4 * kRows && PIECES % 4 == 0) {
-        // thread -> (row gt / 4, quarter gt % 4 of it): consecutive pieces, no index division;
-        // the 8 threads of a quarter-warp load from and store to distinct bank groups
-        const int r = gt >> 2, c0 = (gt & 3) * (PIECES / 4);
-#pragma unroll 3
-        for (int c = c0; c < c0 + PIECES / 4; ++c) widen(r, c);
-      } else {
-        for (int id = gt; id < kRows * PIECES; id += C::GT) widen(id / PIECES, id % PIECES);
-      }
-      group_sync<C::GT>(g);
-      if (ok && b + 2 < nblk) issue(b + 2);  // the raw slot of block b is free again
-    }
 
-    // ---- S = q . K^T : warp gw owns block rows [RPW gw, RPW gw + RPW) as NJ n-tiles of 8
-    constexpr int NJ = C::RPW / 8;
+    // ---- S = q . K^T : warp gw owns block rows [16 gw, 16 gw + 16) as two n-tiles of 8
+    constexpr int NJ = 2;
     float s[NJ][4];
     {
       const int mat = lane >> 3, rr = lane & 7;
       const uint32_t qa = smem_u32(q_s) + (rr + (mat & 1) * 8) * C::ROW + (mat >> 1) * 16;
-      // NJ = 2: the four 8x8 matrices of one k-step are (rows 0-7 | 8-15) x (k 0-7 | 8-15);
-      // NJ = 1: rows 0-7 x the four 8-wide k groups of two k-steps
-      const uint32_t kb = NJ == 2 ? smem_u32(kv_s) + (gw * 16 + rr + (mat >> 1) * 8) * C::ROW + (mat & 1) * 16
-                                  : smem_u32(kv_s) + (gw * 8 + rr) * C::ROW + mat * 16;
-      // o = the partial logits over k-steps [k0, k1) (both even when NJ = 1)
-      auto s_range = [&](int k0, int k1, float (&o)[NJ][4]) {
+      // o = the partial logits over the 32-column chunks [c0, c1) of the rows
+      auto s_range = [&](int c0, int c1, float (&o)[NJ][4]) {
 #pragma unroll
         for (int j = 0; j < NJ; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-        if constexpr (NJ == 2) {
+        if constexpr (FP8) {
+          // the warp's 16 raw rows x 32 columns as E4M3 A fragments (matrices: rows 0-7 | 8-15 x
+          // bytes 0-15 | 16-31); the selections at column offsets 0, 8, 16, 24 give the B
+          // fragments of the chunk's two k-steps for both n-tiles
+          const uint32_t ka = smem_u32(kv_s) + (gw * 16 + rr + (mat & 1) * 8) * C::RAWROW + (mat >> 1) * 16;
+#pragma unroll 2
+          for (int cc = c0; cc < c1; ++cc) {
+            uint32_t a0, a1, a2, a3, q0, q1, q2, q3;
+            ldsm_x4(ka + cc * 32, a0, a1, a2, a3);
+            float e0[4], e8[4], e16[4], e24[4];
+            mma_e4m3_16832(e0, a0, a1, a2, a3, sel0, 0u);
+            mma_e4m3_16832(e8, a0, a1, a2, a3, sel8, 0u);
+            mma_e4m3_16832(e16, a0, a1, a2, a3, 0u, sel0);
+            mma_e4m3_16832(e24, a0, a1, a2, a3, 0u, sel8);
+            ldsm_x4(qa + (2 * cc) * 32, q0, q1, q2, q3);
+            mma_bf16_16816(o[0], q0, q1, q2, q3, bf16x2_of_e4m3_f32(e0[0], e0[1]), bf16x2_of_e4m3_f32(e8[0], e8[1]));
+            mma_bf16_16816(o[1], q0, q1, q2, q3, bf16x2_of_e4m3_f32(e0[2], e0[3]), bf16x2_of_e4m3_f32(e8[2], e8[3]));
+            ldsm_x4(qa + (2 * cc + 1) * 32, q0, q1, q2, q3);
+            mma_bf16_16816(o[0], q0, q1, q2, q3, bf16x2_of_e4m3_f32(e16[0], e16[1]), bf16x2_of_e4m3_f32(e24[0], e24[1]));
+            mma_bf16_16816(o[1], q0, q1, q2, q3, bf16x2_of_e4m3_f32(e16[2], e16[3]), bf16x2_of_e4m3_f32(e24[2], e24[3]));
+          }
+        } else {
+          // matrices of one k-step: (rows 0-7 | 8-15) x (k 0-7 | 8-15)
+          const uint32_t kb = smem_u32(kv_s) + (gw * 16 + rr + (mat >> 1) * 8) * C::ROW + (mat & 1) * 16;
 #pragma unroll 4
-          for (int ks = k0; ks < k1; ++ks) {
+          for (int ks = 2 * c0; ks < 2 * c1; ++ks) {
             uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
             ldsm_x4(qa + ks * 32, a0, a1, a2, a3);
             ldsm_x4(kb + ks * 32, b0, b1, b2, b3);
             mma_bf16_16816(o[0], a0, a1, a2, a3, b0, b1);
-            mma_bf16_16816(o[NJ - 1], a0, a1, a2, a3, b2, b3);
+            mma_bf16_16816(o[1], a0, a1, a2, a3, b2, b3);
           }
-        } else {
-          float odd[4] = {0.f, 0.f, 0.f, 0.f};  // a second chain halves the MMA dependency depth
-#pragma unroll 2
-          for (int ks = k0; ks < k1; ks += 2) {
-            uint32_t a0, a1, a2, a3, c0, c1, c2, c3, b0, b1, b2, b3;
-            ldsm_x4(kb + ks * 32, b0, b1, b2, b3);
-            ldsm_x4(qa + ks * 32, a0, a1, a2, a3);
-            ldsm_x4(qa + ks * 32 + 32, c0, c1, c2, c3);
-            mma_bf16_16816(o[0], a0, a1, a2, a3, b0, b1);
-            mma_bf16_16816(odd, c0, c1, c2, c3, b2, b3);
-          }
-#pragma unroll
-          for (int e = 0; e < 4; ++e) o[0][e] += odd[e];
         }
       };
+      static_assert(DQK % 32 == 0, "rows are read in 32-column chunks");
       if constexpr (TILED) {
-        // tile c of a row covers k-steps [8c, 8c + 8): each tile accumulates alone and is added
+        // tile c of a row covers chunks [4c, 4c + 4): each tile accumulates alone and is added
         // with the tile's scale of each of this thread's positions
 #pragma unroll
         for (int j = 0; j < NJ; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
         for (int c = 0; c < C::NSC; ++c) {
           float a_[NJ][4];
-          s_range(8 * c, min(DQK / 16, 8 * c + 8), a_);
+          s_range(4 * c, min(DQK / 32, 4 * c + 4), a_);
 #pragma unroll
           for (int j = 0; j < NJ; ++j)
 #pragma unroll
@@ -338,7 +326,7 @@ sparse_attn_kernel(const SparseAttnParams p) {
             }
         }
       } else {
-        s_range(0, DQK / 16, s);
+        s_range(0, DQK / 32, s);
       }
     }
 
@@ -435,22 +423,48 @@ sparse_attn_kernel(const SparseAttnParams p) {
     {
       const int mat = lane >> 3, rr = lane & 7;
       const uint32_t p_base = smem_u32(p_s) + (TILED ? (gw * C::CPW / 128) * (kHeads * kRows * 2) : 0);
-      const uint32_t vb = smem_u32(v_s) + (rr + (mat & 1) * 8) * VR + (gw * C::CPW + (mat >> 1) * 8) * 2;
-#pragma unroll
+#pragma unroll(FP8 ? 1 : kRows / 16)
       for (int kk = 0; kk < kRows / 16; ++kk) {
         uint32_t a0, a1, a2, a3;
         ldsm_x4(p_base + swz(rr + (mat & 1) * 8, 2 * kk + (mat >> 1), C::P_CHUNKS), a0, a1, a2, a3);
+        if constexpr (FP8) {
+          // raw rows 16kk .. 16kk+15 x 32 value columns as E4M3 B fragments (matrices: rows 0-7 |
+          // 8-15 x bytes 0-15 | 16-31); the selections on the left (value columns 0-15 or 16-31
+          // of the chunk) give the V fragments of four n-tiles, rows 0-7 and 8-15 in turn
+          const uint32_t vb = smem_u32(kv_s) + (16 * kk + rr + (mat >> 1) * 8) * C::RAWROW + (mat & 1) * 16;
+          constexpr int CH = C::CPW >= 32 ? C::CPW / 32 : 1;  // chunks of the warp's columns
 #pragma unroll
-        for (int nt = 0; nt < NT; nt += 2) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(vb + kk * 16 * VR + nt * 16, b0, b1, b2, b3);
-          mma_bf16_16816(acc[nt], a0, a1, a2, a3, b0, b1);
-          mma_bf16_16816(acc[nt + 1], a0, a1, a2, a3, b2, b3);
+          for (int ch = 0; ch < CH; ++ch) {
+            const int col = gw * C::CPW + 32 * ch;  // first value column (16-column warps: may be mid-chunk)
+            uint32_t v0, v1, v2, v3;
+            ldsm_x4(vb + (col & ~31), v0, v1, v2, v3);
+#pragma unroll
+            for (int half = 0; half < (C::CPW >= 32 ? 2 : 1); ++half) {
+              const bool upper = C::CPW >= 32 ? half == 1 : (col & 16) != 0;
+              const uint32_t l0 = upper ? 0u : sel0, l8 = upper ? 0u : sel8;
+              const uint32_t u0 = upper ? sel0 : 0u, u8 = upper ? sel8 : 0u;
+              float f0[4], f8[4];  // value rows 0-7 and 8-15 of the k-step
+              mma_e4m3_16832(f0, l0, l8, u0, u8, v0, v1);
+              mma_e4m3_16832(f8, l0, l8, u0, u8, v2, v3);
+              const int nt = (C::CPW >= 32 ? 4 * ch : 0) + 2 * half;
+              mma_bf16_16816(acc[nt], a0, a1, a2, a3, bf16x2_of_e4m3_f32(f0[0], f0[1]), bf16x2_of_e4m3_f32(f8[0], f8[1]));
+              mma_bf16_16816(acc[nt + 1], a0, a1, a2, a3, bf16x2_of_e4m3_f32(f0[2], f0[3]), bf16x2_of_e4m3_f32(f8[2], f8[3]));
+            }
+          }
+        } else {
+          const uint32_t vb = smem_u32(v_s) + (rr + (mat & 1) * 8) * VR + (gw * C::CPW + (mat >> 1) * 8) * 2;
+#pragma unroll
+          for (int nt = 0; nt < NT; nt += 2) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(vb + kk * 16 * VR + nt * 16, b0, b1, b2, b3);
+            mma_bf16_16816(acc[nt], a0, a1, a2, a3, b0, b1);
+            mma_bf16_16816(acc[nt + 1], a0, a1, a2, a3, b2, b3);
+          }
         }
       }
     }
     group_sync<C::GT>(g);  // the slot and P are rewritten next
-    if (!FP8 && ok && b + 2 < nblk) issue(b + 2);
+    if (ok && b + 2 < nblk) issue(b + 2);
   }
   // ---- merge the second group into the first (bf16 only)
   if (C::GROUPS == 2) {
