@@ -45,6 +45,7 @@ struct Cfg {
   static constexpr int PCOPIES = TILED ? DV / 128 : 1;  // P scaled per value tile
   // two independent groups of 4 warps, one block each (E4M3 rows too: the MMAs read them raw)
   static constexpr int GROUPS = 2;
+  static_assert(GROUPS == 2, "block b goes to group b % 2 through slot b % 2");
   static constexpr int GW = 4;                           // warps per group
   static constexpr int GT = 32 * GW;                     // threads per group
   static constexpr int THREADS = GT * GROUPS;
@@ -215,12 +216,7 @@ sparse_attn_kernel(const SparseAttnParams p) {
     group_sync<C::GT>(g);  // every expect_tx of the block precedes the arrival that opens the phase
     if (gt == 0) mbar_arrive(bar);
   };
-  if (C::GROUPS == 2) {
-    if (g < nblk) issue(g);
-  } else {
-    if (nblk > 0) issue(0);
-    if (nblk > 1) issue(1);
-  }
+  if (g < nblk) issue(g);  // group g takes blocks g, g + 2, ... through slot g
   // E4M3 scales of the rows, fetched while the first blocks are on their way
   if constexpr (C::NSC > 0) {
     for (int j = tid; j < nblk * kRows; j += C::THREADS) {  // one row's scales per thread, all in flight
@@ -254,9 +250,9 @@ sparse_attn_kernel(const SparseAttnParams p) {
   for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
   int use = 0;  // how many blocks this group has consumed (mbarrier phase of its slots)
-  for (int b = (C::GROUPS == 2 ? g : 0); b < nblk; b += C::GROUPS, ++use) {
+  for (int b = g; b < nblk; b += C::GROUPS, ++use) {
     const int slot_i = b & 1;
-    ok = ok && mbar_wait(&bars[slot_i], (uint32_t)((C::GROUPS == 2 ? use : (use >> 1)) & 1), p.err);
+    ok = ok && mbar_wait(&bars[slot_i], (uint32_t)(use & 1), p.err);
     const int* ib = idx_s + b * kRows;
     const float* sb = scale_s + b * kRows * C::NSC;  // C::NSC scales per row
     uint8_t* slot = smem + C::OFF_SLOT + slot_i * C::SLOT;
@@ -466,8 +462,8 @@ sparse_attn_kernel(const SparseAttnParams p) {
     group_sync<C::GT>(g);  // the slot and P are rewritten next
     if (ok && b + 2 < nblk) issue(b + 2);
   }
-  // ---- merge the second group into the first (bf16 only)
-  if (C::GROUPS == 2) {
+  // ---- merge the second group into the first
+  {
     __syncthreads();  // all slots are idle: reuse slot 1 as staging
     float* stage = reinterpret_cast<float*>(smem + C::OFF_SLOT + C::SLOT);
     float2* ml = reinterpret_cast<float2*>(smem + C::OFF_P);  // P of group 0 is idle as well
