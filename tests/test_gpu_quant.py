@@ -79,6 +79,44 @@ def test_quantize_fp8_tiles_bit_exact(dsa, width, tile):
     np.testing.assert_array_equal(codes.cpu().numpy(), want_codes)
 
 
+def _all_bf16_up_to_448():
+    b = np.arange(0, 1 << 16, dtype=np.uint32)
+    v = (b << 16).view(np.float32)
+    # magnitudes below 2^-100 are left out so that scaling by 2^-20 stays exact in bf16 (they are
+    # far below E4M3's smallest midpoint, 2^-10)
+    keep = np.isfinite(v) & (np.abs(v) <= 448) & ((np.abs(v) >= 2.0**-100) | (v == 0))
+    return v[keep].astype(np.float64)
+
+
+@pytest.mark.parametrize("k", [-20, 0, 13])
+def test_quantize_fp8_rows_exact_ties_at_every_midpoint(dsa, k):
+    # rows whose amax is 448 * 2^k have s = 2^k exactly, so x / s is the bf16 value itself: the rows
+    # carry every bf16 value of magnitude <= 448, among them every midpoint of two E4M3 values
+    # (an exact tie, resolved to even) and the values around it
+    W = 576
+    vals = _all_bf16_up_to_448()
+    n = -(-vals.size // (W - 1))
+    body = np.resize(vals, n * (W - 1)).reshape(n, W - 1)
+    x = np.concatenate([np.full((n, 1), 448.0), body], axis=1) * 2.0**k
+    t = torch.from_numpy(x).to(torch.bfloat16)
+    assert np.array_equal(t.to(torch.float64).numpy(), x)  # every value is a bf16
+    codes, s = dsa.dsa_quantize_fp8_rows(t.cuda())
+    want_codes, want_s = oracle.quantize_fp8_rows(x)
+    np.testing.assert_array_equal(s.cpu().numpy(), want_s)
+    np.testing.assert_array_equal(codes.cpu().numpy(), want_codes)
+
+
+def test_quantize_fp8_rows_large_random_batch(dsa):
+    # 4096 latent rows with per-row magnitudes spread over 2^-40 .. 2^40
+    rng = np.random.default_rng(77)
+    x = rng.standard_normal((4096, 576)) * np.ldexp(1.0, rng.integers(-40, 40, (4096, 1)))
+    t = torch.from_numpy(x).to(torch.bfloat16)
+    codes, s = dsa.dsa_quantize_fp8_rows(t.cuda())
+    want_codes, want_s = oracle.quantize_fp8_rows(_f64(t))
+    np.testing.assert_array_equal(s.cpu().numpy(), want_s)
+    np.testing.assert_array_equal(codes.cpu().numpy(), want_codes)
+
+
 def test_cache_append_writes_only_its_rows(dsa):
     # new tokens of 3 sequences appended at their next positions of [3][L] caches
     L, d, W = 50, 128, 576

@@ -32,6 +32,28 @@ __device__ __forceinline__ float warp_amax(float a) {
   return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(a))));
 }
 
+// The E4M3 code of the IEEE quotient x / s (fp32, round to nearest), without a division per
+// element.  Per row: r = 1/s correctly rounded, usable when s and r are normal floats.  Per element:
+// q0 = x * r lies within 2.5 fp32 ulps of x / s rounded, and E4M3 rounding is monotone, so the two
+// give the same code unless an E4M3 rounding midpoint lies that close to q0.  A midpoint of two
+// normal E4M3 values (those two a binade apart included) has fp32 mantissa bit 19 set and bits
+// 18..0 clear, so a q0 whose low 20 bits are within 4 of 0x80000 takes the division, and so does
+// a q0 in E4M3's subnormal range (below 2^-6), whose midpoints sit elsewhere.
+struct Quotient {
+  float s, r;
+  bool fast;
+  __device__ explicit Quotient(float s_) : s(s_) {
+    r = __frcp_rn(s_);
+    fast = s_ >= 0x1p-126f && r >= 0x1p-126f && r <= 0x1p126f;
+  }
+  __device__ __forceinline__ float operator()(float x) const {
+    const float q0 = x * r;
+    const uint32_t low = __float_as_uint(q0) & 0xFFFFFu;
+    const bool near = low - 0x7FFFCu <= 8u || fabsf(q0) < 0x1p-6f;
+    return (fast && !near) ? q0 : __fdiv_rn(x, s);
+  }
+};
+
 __global__ void __launch_bounds__(32 * kRowsPerCta) mxfp8_quant_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t x_row_stride, int rows, int d,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, const int64_t* __restrict__ dst_rows) {
@@ -68,7 +90,8 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) fp8_rows_quant_kernel(
   const float amax = warp_amax(a);
   const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
   uint8_t* out = codes + dst * code_row_stride;
-  for (int j = lane; j < width; j += 32) out[j] = to_e4m3(__fdiv_rn(__bfloat162float(src[j]), s));
+  const Quotient div(s);
+  for (int j = lane; j < width; j += 32) out[j] = to_e4m3(div(__bfloat162float(src[j])));
   if (lane == 0) scales[dst] = s;
 }
 
@@ -133,12 +156,12 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) fp8_rows_quant_vec_kernel(
   const float amax = warp_amax(a);
   const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
   uint8_t* out = codes + dst * code_row_stride;
+  const Quotient div(s);
   for (int j = 4 * lane; j < width; j += 128) {
     float v[4];
     load4(src + j, v);
-    *reinterpret_cast<uint32_t*>(out + j) =
-        pack4(to_e4m3(__fdiv_rn(v[0], s)), to_e4m3(__fdiv_rn(v[1], s)), to_e4m3(__fdiv_rn(v[2], s)),
-              to_e4m3(__fdiv_rn(v[3], s)));
+    *reinterpret_cast<uint32_t*>(out + j) = pack4(to_e4m3(div(v[0])), to_e4m3(div(v[1])), to_e4m3(div(v[2])),
+                                                  to_e4m3(div(v[3])));
   }
   if (lane == 0) scales[dst] = s;
 }
@@ -221,13 +244,14 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) fp8_rows_quant_v8_kernel(
   const float amax = warp_amax(a);
   const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
   uint8_t* out = codes + dst * code_row_stride;
+  const Quotient div(s);
 #pragma unroll
   for (int j = 0; j < kMaxChunks8; ++j) {
     const int c = lane + 32 * j;
     if (c < nch) {
       uint8_t q[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) q[i] = to_e4m3(__fdiv_rn(v[j][i], s));
+      for (int i = 0; i < 8; ++i) q[i] = to_e4m3(div(v[j][i]));
       *reinterpret_cast<uint2*>(out + 8 * c) = make_uint2(pack4(q[0], q[1], q[2], q[3]), pack4(q[4], q[5], q[6], q[7]));
     }
   }
@@ -253,7 +277,8 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) fp8_tiles_quant_kernel(
   const float amax = warp_amax(a);
   const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
   uint8_t* out = codes + dst * code_row_stride + lo;
-  for (int j = lane; j < n; j += 32) out[j] = to_e4m3(__fdiv_rn(__bfloat162float(src[j]), s));
+  const Quotient div(s);
+  for (int j = lane; j < n; j += 32) out[j] = to_e4m3(div(__bfloat162float(src[j])));
   if (lane == 0) scales[dst * ntile + c] = s;
 }
 
