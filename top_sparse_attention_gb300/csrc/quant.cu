@@ -46,11 +46,17 @@ struct Quotient {
     r = __frcp_rn(s_);
     fast = s_ >= 0x1p-126f && r >= 0x1p-126f && r <= 0x1p126f;
   }
-  __device__ __forceinline__ float operator()(float x) const {
+  // q0, and whether it gives the code of the IEEE quotient
+  __device__ __forceinline__ float fast_part(float x, bool* exact) const {
     const float q0 = x * r;
     const uint32_t low = __float_as_uint(q0) & 0xFFFFFu;
-    const bool near = low - 0x7FFFCu <= 8u || fabsf(q0) < 0x1p-6f;
-    return (fast && !near) ? q0 : __fdiv_rn(x, s);
+    *exact = fast && !(low - 0x7FFFCu <= 8u || fabsf(q0) < 0x1p-6f);
+    return q0;
+  }
+  __device__ __forceinline__ float operator()(float x) const {
+    bool exact;
+    const float q0 = fast_part(x, &exact);
+    return exact ? q0 : __fdiv_rn(x, s);
   }
 };
 
@@ -170,8 +176,8 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) fp8_rows_quant_vec_kernel(
 //  * MXFP8: a warp takes kRowsPerWarp8 consecutive rows as one flat run of 8-element chunks; four
 //    consecutive lanes hold a group of 32 (d is a multiple of 32, so groups never straddle rows)
 //    and its max takes two shuffles.
-//  * FP8 rows (width a multiple of 8, at most 32 * 8 * kMaxChunks8): the row stays in registers,
-//    so it is read once.
+//  * FP8 rows (width a multiple of 8, at most 32 * 8 * kMaxChunks8): two passes, the second
+//    re-reading the row from L2.
 
 constexpr int kRowsPerWarp8 = 8;
 constexpr int kMaxChunks8 = 4;
@@ -230,30 +236,31 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) fp8_rows_quant_v8_kernel(
   if (dst < 0) return;
   const __nv_bfloat16* src = x + (int64_t)r * x_row_stride;
   const int nch = width / 8;
-  float v[kMaxChunks8][8];
+  // two passes over the row: the first (from HBM) keeps only the running max, the second re-reads
+  // the row from L2; few registers per thread keep many rows in flight per SM
   float a = 0.f;
 #pragma unroll
   for (int j = 0; j < kMaxChunks8; ++j) {
     const int c = lane + 32 * j;
     if (c < nch) {
-      load8(src + 8 * c, v[j]);
+      float v[8];
+      load8(src + 8 * c, v);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[j][i]));
+      for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[i]));
     }
   }
   const float amax = warp_amax(a);
   const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
   uint8_t* out = codes + dst * code_row_stride;
   const Quotient div(s);
+#pragma unroll 1
+  for (int c = lane; c < nch; c += 32) {
+    float v[8];
+    load8(src + 8 * c, v);
+    uint8_t q[8];
 #pragma unroll
-  for (int j = 0; j < kMaxChunks8; ++j) {
-    const int c = lane + 32 * j;
-    if (c < nch) {
-      uint8_t q[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) q[i] = to_e4m3(div(v[j][i]));
-      *reinterpret_cast<uint2*>(out + 8 * c) = make_uint2(pack4(q[0], q[1], q[2], q[3]), pack4(q[4], q[5], q[6], q[7]));
-    }
+    for (int i = 0; i < 8; ++i) q[i] = to_e4m3(div(v[i]));
+    *reinterpret_cast<uint2*>(out + 8 * c) = make_uint2(pack4(q[0], q[1], q[2], q[3]), pack4(q[4], q[5], q[6], q[7]));
   }
   if (lane == 0) scales[dst] = s;
 }
