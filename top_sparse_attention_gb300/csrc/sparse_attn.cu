@@ -12,8 +12,8 @@
 // so every gathered row is read from HBM once and used by all heads; softmax is online across
 // blocks (running max / sum, log2 domain).
 //
-// bf16 rows: two groups of 4 warps work on the two slots at the same time and merge their
-// (m, l, o) in shared memory at the end.  E4M3 rows stay raw in shared memory: the tensor cores
+// Two groups of 4 warps work on the two slots at the same time and merge their (m, l, o) in
+// shared memory at the end, for bf16 and E4M3 rows alike.  E4M3 rows stay raw in shared memory: the tensor cores
 // turn them into the bf16 operands of the same MMAs.  An E4M3 MMA of 16 raw rows with a 0/1
 // selection matrix yields, in fp32 and exactly, the values in the register layout of a bf16 B
 // fragment (the K side of q.K^T with the selection on the right, the V side of P.V with the
@@ -229,9 +229,10 @@ sparse_attn_kernel(const SparseAttnParams p) {
     }
     __syncthreads();
   }
-  // selection columns for the E4M3 expansions: byte i of a B fragment register of this lane holds
-  // row 4 (lane % 4) + i of column lane / 4; E4M3 1.0 = 0x38 where that row is the column (sel0)
-  // or the column + 8 (sel8)
+  // selection matrices for the E4M3 expansions.  Byte i of this lane's register is element
+  // (4 (lane % 4) + i, lane / 4) of a B fragment (k, n) and element (lane / 4, 4 (lane % 4) + i)
+  // of an A fragment (m, k); it holds E4M3 1.0 = 0x38 where the k index equals the other index
+  // (sel0) or the other index + 8 (sel8), zero elsewhere
   uint32_t sel0 = 0, sel8 = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
