@@ -12,13 +12,13 @@
 // so every gathered row is read from HBM once and used by all heads; softmax is online across
 // blocks (running max / sum, log2 domain).
 //
-// Two groups of 4 warps work on the two slots at the same time and merge their (m, l, o) in
-// shared memory at the end, for bf16 and E4M3 rows alike.  E4M3 rows stay raw in shared memory: the tensor cores
-// turn them into the bf16 operands of the same MMAs.  An E4M3 MMA of 16 raw rows with a 0/1
+// Two groups of 4 warps work on the two slots at the same time and merge their (m, l, o) in shared
+// memory at the end, for bf16 and E4M3 rows alike.  E4M3 rows stay raw in shared memory: the tensor
+// cores turn them into the bf16 operands of the same MMAs.  An E4M3 MMA of 16 raw rows with a 0/1
 // selection matrix yields, in fp32 and exactly, the values in the register layout of a bf16 B
 // fragment (the K side of q.K^T with the selection on the right, the V side of P.V with the
-// selection on the left); the upper halves of those fp32 are the bf16 values.  The per-row scale
-// is folded into the logit and into the probability that multiplies V.
+// selection on the left); the upper halves of those fp32 are the bf16 values.  The per-row scale is
+// folded into the logit and into the probability that multiplies V.
 //
 // When K is split over S > 1 CTAs (so a small batch still covers every SM), each CTA writes its
 // partial (o, m, l) and a second kernel merges them with a log-sum-exp combine.
