@@ -115,6 +115,34 @@ def test_validation_rejects_before_any_launch(native):
     assert lib.dsa_sparse_attn(*bad) == 1
 
 
+def test_quantiser_and_tiled_kv_validation(native):
+    # every case returns from the host checks, which run before the device query (without a
+    # device that query would answer DSA_ERR_CUDA = 4)
+    lib = native.lib
+    mx = lib.dsa_quantize_mxfp8  # (x, x_row_stride, rows, d, codes, sf, dst_rows, stream)
+    assert mx(F, 100, 4, 100, F, F, None, None) == 1    # d not a multiple of 32
+    assert mx(F, 64, 4, 128, F, F, None, None) == 1     # row pitch below d
+    assert mx(F, 128, -1, 128, F, F, None, None) == 1   # negative row count
+    assert mx(None, 128, 4, 128, F, F, None, None) == 1
+    assert mx(F + 1, 128, 4, 128, F, F, None, None) == 1  # bf16 source not 2-byte aligned
+    assert mx(F, 128, 0, 128, None, None, None, None) == 0  # no rows: nothing to do
+    rows = lib.dsa_quantize_fp8_rows  # (x, x_row_stride, rows, width, codes, code_stride, scales, dst, stream)
+    assert rows(F, 576, 4, 576, F, 500, F, None, None) == 1  # code pitch below the width
+    assert rows(F, 576, 4, 576, F, 576, None, None, None) == 1  # no scale buffer
+    tiles = lib.dsa_quantize_fp8_tiles  # (x, x_row_stride, rows, width, tile, codes, stride, scales, dst, stream)
+    assert tiles(F, 576, 4, 576, 0, F, 576, F, None, None) == 1
+    assert tiles(F, 576, 4, 576, 2048, F, 576, F, None, None) == 1  # tile above 1024
+    # 128-element KV scale tiles: the 576 / 512 latent row only; a valid call passes validation and
+    # stops at the missing workspace (3)
+    sa = [F, F, None, F, 64, 64 * 64, 0, 0, F, 2, 1, 64, 16, 16, 64, 64, 0.125, 3, F, None, None, 0, None]
+    assert lib.dsa_sparse_attn(*sa) == 2
+    sa = [F, F, None, F, 576, 576 * 64, 0, 0, F, 2, 1, 64, 2048, 16, 576, 512, 0.04, 3, F, None, None, 0,
+          None]
+    assert lib.dsa_sparse_attn(*sa) == 3
+    sa[3] = None  # tiled scales missing
+    assert lib.dsa_sparse_attn(*sa) == 1
+
+
 def test_fused_validation(native):
     a = native.DsaArgs()
     a.T, a.q_per_seq, a.q_pos0, a.L, a.K = 2, 1, -1, 64, 8
