@@ -262,29 +262,39 @@ def test_sparse_attn_repeated_rows(dsa):
     _attn_case(dsa, wl, idx, "bf16", guard=False)
 
 
-@pytest.mark.parametrize("tiled", [False, True])
-def test_sparse_attn_fp8_rows_widen_exactly_for_every_code(dsa, tiled):
+@pytest.mark.parametrize("D,D_v,tiled", [(576, 512, False), (576, 512, True), (64, 64, False)])
+def test_sparse_attn_fp8_rows_widen_exactly_for_every_code(dsa, D, D_v, tiled):
     # One selected row: its softmax weight is exactly 1, so with power-of-two scales the output is
     # each value column's E4M3 value times its scale, exactly representable in bf16.  The rows
-    # cycle through all 254 finite codes (subnormals and both zeros included) at shifted columns.
-    T, L, D = 4, 8, 576
+    # cycle through all 254 finite codes (subnormals and both zeros included) at shifted columns;
+    # with 64-wide rows the eight rows together hold every code.
+    L = 8
     finite = np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8)
-    codes = np.stack([np.resize(np.roll(finite, 37 * r), D) for r in range(L)])
+    codes = np.stack([np.resize(np.roll(finite, -37 * r), D) for r in range(L)])
+    assert len(set(codes[:, :D_v].ravel())) == 254
     rng = np.random.default_rng(3)
     shape = (1, L, (D + 127) // 128) if tiled else (1, L)
     sc = np.ldexp(1.0, rng.integers(-7, 6, shape)).astype(np.float32)
+    rows = list(range(L))
+    T = len(rows)
     q = torch.from_numpy(rng.standard_normal((T, 16, D))).to(torch.bfloat16)
-    rows = [1, 3, 6, 7]
     idx = torch.tensor([[r] for r in rows], dtype=torch.int32)
     out, lse = dsa.dsa_sparse_attn(q.cuda(), torch.from_numpy(codes).reshape(1, L, D).cuda(), idx.cuda(),
-                                   sm_scale=0.1, kv_scale=torch.from_numpy(sc).cuda(), D_v=512, q_per_seq=T)
+                                   sm_scale=0.1, kv_scale=torch.from_numpy(sc).cuda(), D_v=D_v, q_per_seq=T)
     out = out.float().cpu().numpy()
     for t, r in enumerate(rows):
-        v = oracle.e4m3_to_f64(codes[r, :512])
-        s = np.repeat(sc[0, r], 128)[:512] if tiled else sc[0, r]
-        want = np.broadcast_to(v * s, (16, 512))
+        v = oracle.e4m3_to_f64(codes[r, :D_v])
+        s = np.repeat(sc[0, r], 128)[:D_v] if tiled else sc[0, r]
+        want = np.broadcast_to(v * s, (16, D_v))
         assert np.array_equal(out[t], want), f"t={t}: {np.flatnonzero(out[t][0] != want[0])[:8]}"
     assert torch.isfinite(lse).all()
+
+
+def test_sparse_attn_small_fp8_rows(dsa):
+    # E4M3 rows of 64 with V = the same row (each warp owns 16 value columns, half a 32-column
+    # chunk of the row), against the oracle
+    wl = synth.small_workload("decode_b8_l32k_mxfp8", T=3, L=1500, K=300, H=20, D_qk=64, D_v=64)
+    _attn_case(dsa, wl, _random_idx(3, 300, 1500, 9, pad=7), "fp8", guard=False)
 
 
 def test_sparse_attn_out_of_range_index_is_skipped_and_recorded(dsa):
