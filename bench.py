@@ -6,7 +6,9 @@ A step is one call of the fused chain (dsa_decode / dsa_prefill through the C AB
 of seeded synthetic inputs already resident in HBM.  The default workload is the batch-8 decode at
 L = 32768 (bf16 indexer 64 x 128, K = 2048, 16 heads over a 576-wide latent row).  Steps rotate
 over several independent input sets whose total size is several times the 129 MB L2, so every
-step reads its caches from HBM.  Rank 0 prints one JSON line.
+step reads its caches from HBM.  By default six independent batches are in flight (consecutive
+steps on six streams, each input set always on the same stream); the same steps one batch at a time
+are reported as `serial`.  Rank 0 prints one JSON line.
 
 --impl reference times the oracle (plain fp64 CPU code) on the host cores on the same workload.
 Under torchrun every rank runs an independent replica (no data-path collective); the barrier and
