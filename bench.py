@@ -255,6 +255,92 @@ def dist_env():
     return world, rank, local
 
 
+GRAPH_MAX_STEPS = 240  # steps held by one captured graph (a multiple of the input-set count is used)
+
+
+def capture_steps(first, count, stream, streams, enqueue):
+    """One CUDA graph holding steps first .. first+count-1: step i is enqueued by enqueue(i, st)
+    on streams[i % len(streams)], all forked from and joined back into `stream`.  Everything the
+    steps read stays owned by the caller (a graph keeps raw pointers only)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        for st in streams:
+            if st is not stream:
+                st.wait_event(fork)
+        for i in range(first, first + count):
+            st = streams[i % len(streams)]
+            with torch.cuda.stream(st):
+                enqueue(i, st)
+        for st in streams:
+            if st is not stream:
+                stream.wait_stream(st)
+    return g
+
+
+def step_plan(steps, n_sets):
+    """(period, full periods, tail): `steps` steps as replays of one graph of `period` steps (a
+    multiple of n_sets, so every replay starts at input set 0) plus one graph of the `tail` steps
+    left over.  Up to GRAPH_MAX_STEPS steps form a single graph of exactly `steps` steps."""
+    if steps <= GRAPH_MAX_STEPS:
+        return steps, 1, 0
+    period = max(n_sets, GRAPH_MAX_STEPS // n_sets * n_sets)
+    return period, steps // period, steps % period
+
+
+def timed_steps(steps, n_sets, stream, streams, enqueue, barrier, graphs=True, clocks=None):
+    """Device milliseconds per step for exactly `steps` steps, step i enqueued by enqueue(i, st)
+    on streams[i % len(streams)].  With graphs, the steps are replayed from CUDA graphs of up to
+    GRAPH_MAX_STEPS steps each (captured and replayed once before timing), so the host launches a
+    handful of graphs and the figure does not depend on the host's launch rate; CUDA events on
+    `stream` bracket the region, with a barrier and a device synchronisation on both sides.
+    `clocks` (a ClockSampler) samples the GPU clocks while the timed region runs."""
+    import contextlib
+
+    sampling = clocks if clocks is not None else contextlib.nullcontext()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if graphs:
+        period, full, tail = step_plan(steps, n_sets)
+        g_period = capture_steps(0, period, stream, streams, enqueue)
+        g_tail = capture_steps(full * period, tail, stream, streams, enqueue) if tail else None
+        with torch.cuda.stream(stream):  # untimed replay: every node has run once
+            g_period.replay()
+            if g_tail is not None:
+                g_tail.replay()
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        with sampling, torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(full):
+                g_period.replay()
+            if g_tail is not None:
+                g_tail.replay()
+            ev1.record(stream)
+            torch.cuda.synchronize()
+    else:
+        barrier()
+        torch.cuda.synchronize()
+        sampling.__enter__()
+        ev0.record(stream)
+        for st in streams:
+            if st is not stream:
+                st.wait_event(ev0)
+        for i in range(steps):
+            st = streams[i % len(streams)]
+            with torch.cuda.stream(st):
+                enqueue(i, st)
+        for st in streams:
+            if st is not stream:
+                stream.wait_stream(st)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        sampling.__exit__(None, None, None)
+    barrier()
+    return ev0.elapsed_time(ev1) / steps
+
+
 def run_reference(args, wl):
     """The oracle as it stands, on the host cores: each step is one query of the workload through
     the whole chain (fp64 scores, full-sort Top-K, exact attention)."""
@@ -325,66 +411,31 @@ def run_ours(args, wl):
             calls[i % n_sets](stream)
     torch.cuda.synchronize()
 
-    graphs = None
-    if not args.no_graph:
-        graphs = []
-        for c in calls:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                c(stream)
-            graphs.append(g)
-        with torch.cuda.stream(stream):
-            for i in range(args.warmup):
-                graphs[i % n_sets].replay()
-        torch.cuda.synchronize()
-
     def barrier():
         if world > 1:
             import torch.distributed as dist
 
             dist.barrier()
 
-    # ---- timed region: exactly K steps
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize()
     # with inflight > 1, consecutive steps (independent batches) go to different streams so that
     # one batch's selection and attention overlap the next batch's scoring
     streams = [stream] + [torch.cuda.Stream(device=dev) for _ in range(inflight - 1)]
-    with ClockSampler(dev.index) as clocks:
-        ev0.record(stream)
-        for st in streams[1:]:
-            st.wait_event(ev0)
-        for i in range(args.steps):
-            st = streams[i % inflight]
-            with torch.cuda.stream(st):
-                if graphs is not None:
-                    graphs[i % n_sets].replay()
-                else:
-                    calls[i % n_sets](st)
-        for st in streams[1:]:
-            stream.wait_stream(st)
-        ev1.record(stream)
-        torch.cuda.synchronize()
-    barrier()
-    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world, dev)
+
+    def enqueue(i, st):
+        calls[i % n_sets](st)
+
+    clocks = ClockSampler(dev.index)
+    ms = timed_steps(args.steps, n_sets, stream, streams, enqueue, barrier, graphs=not args.no_graph,
+                     clocks=clocks)
+    ms = max_over_ranks(ms, world, dev)
     # the same steps one batch at a time (one stream), reported beside the headline
     serial = None
     if inflight > 1:
-        n_serial = min(args.steps, 5000)
-        torch.cuda.synchronize()
-        with torch.cuda.stream(stream):
-            ev0.record(stream)
-            for i in range(n_serial):
-                if graphs is not None:
-                    graphs[i % n_sets].replay()
-                else:
-                    calls[i % n_sets](stream)
-            ev1.record(stream)
-        torch.cuda.synchronize()
-        ms_serial = max_over_ranks(ev0.elapsed_time(ev1) / n_serial, world, dev)
+        ms_serial = timed_steps(args.steps, n_sets, stream, [stream], enqueue, barrier,
+                                graphs=not args.no_graph)
+        ms_serial = max_over_ranks(ms_serial, world, dev)
         serial = {"value": wl.T * world / (ms_serial * 1e-3), "unit": "queries/s",
-                  "ms_per_step": ms_serial, "steps": n_serial, "batches_in_flight": 1}
+                  "ms_per_step": ms_serial, "steps": args.steps, "batches_in_flight": 1}
     err = dsa.dsa_get_device_error(stream)
     queries = wl.T * world
     value = queries / (ms * 1e-3)
@@ -411,8 +462,7 @@ def run_ours(args, wl):
                     "algorithmic_flops": flops, "traffic": profiled_traffic(wl.name)}
 
     # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
-    e2e = end_to_end(dsa, wl, cpu_sets, dev_sets, stream, steps=max(10, min(args.steps, 5000)),
-                     inflight=inflight)
+    e2e = end_to_end(dsa, wl, cpu_sets, dev_sets, stream, steps=args.steps, inflight=inflight)
 
     line = None
     if rank == 0:
@@ -430,7 +480,7 @@ def run_ours(args, wl):
             "data": "synthetic (seeded N(0,1) inputs, U(0,1) head weights)",
             "config": {"workload": wl.name, "batch": wl.T, "L": wl.L, "K": wl.K, "H_idx": wl.H_idx,
                        "d_idx": wl.d_idx, "idx_dtype": wl.idx_dtype, "H": wl.H, "D_qk": wl.D_qk,
-                       "D_v": wl.D_v, "kv_dtype": wl.kv_dtype, "cuda_graph": graphs is not None,
+                       "D_v": wl.D_v, "kv_dtype": wl.kv_dtype, "cuda_graph": not args.no_graph,
                        "batches_in_flight": inflight,
                        "l2": f"rotating {n_sets} input sets, {n_sets * per_step / 1e6:.0f} MB compulsory bytes > 129 MB L2"},
             "hbm_gbs": chain_gbs, "hbm_frac_of_8tbs": chain_gbs / NOMINAL_HBM_GBS,
@@ -634,11 +684,12 @@ def end_to_end(dsa, wl, cpu_sets, dev_sets, stream, steps, inflight=1):
     copied from pinned host memory and its outputs (out, lse) read back, inside the timed region.
     The caches are device-resident state, as in decode, rotating over the same input sets as the
     device timing (their bytes exceed L2).  Inputs sit in one pinned host buffer and one device
-    buffer, outputs likewise, so a step is one host-to-device copy, the fused call (dsa_decode)
-    and one device-to-host copy.  The copies run on their own streams so that neighbouring steps'
-    copies overlap the calls, as a serving loop would run them; with inflight > 1 consecutive
-    steps' calls run on different streams, as in the device timing.  One CUDA graph replays a
-    period of one step per input set, so the host launches once per period."""
+    buffer per set, outputs likewise, so a step is one host-to-device copy, the fused call
+    (dsa_decode) and one device-to-host copy.  Copies run on their own streams so that
+    neighbouring steps' copies overlap the calls, as a serving loop would run them; with
+    inflight > 1 consecutive steps' calls run on different streams, as in the device timing.
+    Exactly `steps` steps are timed, replayed from the same graph plan as the device timing
+    (step_plan); the figure is the larger of the event time and the host's wall time."""
     keys_in = [k for k in ("q", "q_idx", "q_idx_sf", "w") if cpu_sets[0][k] is not None]
 
     def packed(tensors, device, pinned):
@@ -673,56 +724,73 @@ def end_to_end(dsa, wl, cpu_sets, dev_sets, stream, steps, inflight=1):
             for _ in range(2):
                 call(stream)
         torch.cuda.synchronize()
-        sets.append((hin, din, hout, dout, None, call))  # the call owns its workspace
+        # the tuple keeps every buffer the captured graphs point at (the call owns its workspace):
+        # a graph holds raw pointers, and each capture empties torch's allocator cache
+        sets.append((hin, din, hout, dout, call))
     h2d, d2h = sets[0][0].numel(), sets[0][2].numel()
     n = len(sets)
-    # three streams: copies in, the fused call, copies out; events keep each set's buffers from
-    # being overwritten before their readers are done, so step i+1's input copy and step i-1's
-    # output copy overlap step i's call
-    # One CUDA graph holds a period of n steps (one per input set): each step's input copy on a
-    # copy stream, its call on compute stream j % inflight, its output copy on a third stream,
-    # ordered by events, so copies and calls of neighbouring steps overlap without host gaps.
     s_in, s_out = torch.cuda.Stream(device=dev0), torch.cuda.Stream(device=dev0)
     comp = [torch.cuda.Stream(device=dev0) for _ in range(inflight)]
-    ev_in = [torch.cuda.Event() for _ in range(n)]
-    ev_done = [torch.cuda.Event() for _ in range(n)]
-    period = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(period, stream=stream):
-        fork = torch.cuda.Event()
-        fork.record(stream)
-        for st in [s_in, s_out] + comp:
-            st.wait_event(fork)
-        for j in range(n):
-            hin, din, hout, dout, _, call = sets[j]
-            sc = comp[j % inflight]
-            with torch.cuda.stream(s_in):
-                din.copy_(hin, non_blocking=True)
-                ev_in[j].record(s_in)
-            sc.wait_event(ev_in[j])
-            call(sc)
-            ev_done[j].record(sc)
-            s_out.wait_event(ev_done[j])
-            with torch.cuda.stream(s_out):
-                hout.copy_(dout, non_blocking=True)
-        for st in [s_in, s_out] + comp:
-            stream.wait_stream(st)
-    periods = max(1, -(-steps // n))
-    steps = periods * n
+
+    def capture(first, count):
+        """Steps first .. first+count-1 in one graph: step i's input copy on s_in, its call on
+        comp[i % inflight], its output copy on s_out.  A set's input copy waits for the set's
+        previous call (which read those inputs) and its call for the set's previous output copy
+        (which read those outputs)."""
+        ev_in, ev_call, ev_out = {}, {}, {}
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fork = torch.cuda.Event()
+            fork.record(stream)
+            for st in [s_in, s_out] + comp:
+                st.wait_event(fork)
+            for i in range(first, first + count):
+                hin, din, hout, dout, call = sets[i % n]
+                sc = comp[i % inflight]
+                prev = i - n if i - n >= first else None
+                if prev is not None:
+                    s_in.wait_event(ev_call[prev])
+                with torch.cuda.stream(s_in):
+                    din.copy_(hin, non_blocking=True)
+                ev_in[i] = torch.cuda.Event()
+                ev_in[i].record(s_in)
+                sc.wait_event(ev_in[i])
+                if prev is not None:
+                    sc.wait_event(ev_out[prev])
+                call(sc)
+                ev_call[i] = torch.cuda.Event()
+                ev_call[i].record(sc)
+                s_out.wait_event(ev_call[i])
+                with torch.cuda.stream(s_out):
+                    hout.copy_(dout, non_blocking=True)
+                ev_out[i] = torch.cuda.Event()
+                ev_out[i].record(s_out)
+            for st in [s_in, s_out] + comp:
+                stream.wait_stream(st)
+        return g
+
+    period, full, tail = step_plan(steps, n)
+    g_period = capture(0, period)
+    g_tail = capture(full * period, tail) if tail else None
     with torch.cuda.stream(stream):
-        for _ in range(2):
-            period.replay()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g_period.replay()
+        if g_tail is not None:
+            g_tail.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
         e0.record(stream)
-        for _ in range(periods):
-            period.replay()
+        for _ in range(full):
+            g_period.replay()
+        if g_tail is not None:
+            g_tail.replay()
         e1.record(stream)
-        torch.cuda.synchronize()
+    torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     ms = max(e0.elapsed_time(e1), wall * 1e3) / steps
     return {"value": wl.T / (ms * 1e-3), "unit": "queries/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps,
             "copies_per_step": {"h2d": 1, "d2h": 1}, "batches_in_flight": inflight,
             "pipelined": "copies of adjacent steps overlap the calls"}
 

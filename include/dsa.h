@@ -83,9 +83,9 @@ dsa_status dsa_get_device_error(int* code, void* stream);
 dsa_status dsa_selftest_wait_timeout(void* stream);
 
 /* --------------------------------------------------------------------------------------------
- * dsa_index_score -- step 1: indexer relevance scores ("relevance scoring, head-weight
- * application", Day 0 Support for New LLM Architectures, Key Optimization 1; MXFP8 index path
- * with groups of 32 sharing one scale, Key Optimization 2).
+ * dsa_index_score -- step 1: indexer relevance scores (per-position scoring followed by head
+ * weighting, Day 0 Support for New LLM Architectures, Key Optimization 1; MXFP8 index path with
+ * groups of 32 sharing one scale, Key Optimization 2).
  *
  *   scores[t * ld_scores + s] = sum_h w[t,h] * max(0, sum_j q_idx[t,h,j] * k_idx[seq(t), s, j])
  *
@@ -110,7 +110,7 @@ dsa_status dsa_index_score(const void* q_idx, const uint8_t* q_idx_sf, const flo
                            dsa_dtype idx_dtype, float* scores, int64_t ld_scores, void* stream);
 
 /* --------------------------------------------------------------------------------------------
- * dsa_topk -- step 2: Top-K selection ("select the Top-K positions", Day 0 Support for New LLM
+ * dsa_topk -- step 2: Top-K selection (keep the K best-scoring positions, Day 0 Support for New LLM
  * Architectures, Step 1; the Top-k selection operator of "Achieving Day-0 Readiness...",
  * section 2.1).
  *
@@ -140,7 +140,9 @@ size_t dsa_topk_workspace_size(int T, int L, int K);
  * GPU that loads the library, held until the process exits.  T > 16 returns
  * DSA_ERR_UNSUPPORTED before any launch.
  *  - The first call on a device looks up the array's device address (once per device, with that
- *    device current); make that first call before any stream capture.
+ *    device current); make that first call before any stream capture.  The address is kept for
+ *    the life of the process: after cudaDeviceReset (or any teardown of the device's primary
+ *    context) this entry must not be called again on that device.
  *  - Each call clears the part of the array it uses (an asynchronous memset on `stream`), then
  *    launches the Top-K kernel; the array keeps the last call's contents afterwards.
  *  - All calls share the one array: calls that overlap on the GPU (other streams, other threads)
@@ -152,10 +154,10 @@ dsa_status dsa_topk_noalloc(const float* scores, int64_t ld_scores, int T, int q
 
 /* --------------------------------------------------------------------------------------------
  * dsa_sparse_attn -- step 3: gather the selected rows of the latent KV cache and compute exact
- * softmax attention over them ("a sparse-attention kernel then reads only the selected KV
- * entries to perform exact computation", Day 0 Support for New LLM Architectures, Step 1;
- * gather by index then attention, "Achieving Day-0 Readiness...", section 2.3; FP8 KV cache,
- * Key Optimization 2).
+ * softmax attention over them (the sparse-attention kernel touches only the chosen cache entries
+ * and computes attention over them without approximation, Day 0 Support for New LLM
+ * Architectures, Step 1; gather by index then attention, "Achieving Day-0 Readiness...",
+ * section 2.3; FP8 KV cache, Key Optimization 2).
  *
  * For query t, head h, with R = the valid entries (0 <= i < L) of idx[t*K .. t*K+K):
  *   logit[r] = sm_scale * sum_j q[t,h,j] * Kv[r, j]                 (j < D_qk)
@@ -231,7 +233,7 @@ dsa_status dsa_quantize_fp8_tiles(const void* x, int64_t x_row_stride, int rows,
 
 /* --------------------------------------------------------------------------------------------
  * Fused chain: dsa_decode / dsa_prefill run steps 1-3 back to back on `stream` (the indexer's
- * "score-weight-TopK" chain followed by the sparse gather kernel, Day 0 Support for New LLM
+ * scoring, weighting and Top-K chain followed by the sparse gather kernel, Day 0 Support for New LLM
  * Architectures, Key Optimization 1), keeping the scores in the workspace.  dsa_decode expects
  * q_pos0 < 0; dsa_prefill expects q_pos0 >= 0 (a causal chunk, "Achieving Day-0 Readiness...",
  * section 2.3: prefill scores all queries in a batch) and processes the queries in slices so
@@ -263,7 +265,7 @@ typedef struct dsa_args {
   float* lse;         /* fp32 [T, H] or NULL */
   int32_t* idx_out;   /* int32 [T, K] or NULL (then kept in the workspace) */
   /* Paged caches (the pages' block-wise KV layout read through an index table, "Achieving
-   * Day-0 Readiness...", section 2.2; "reads directly from the paged K cache", Day 0 Support for
+   * Day-0 Readiness...", section 2.2; the indexer reads the paged key cache in place, Day 0 Support for
    * New LLM Architectures, Key Optimization 1).  NULL block_table: every cache is contiguous per
    * sequence as described above.  Otherwise each cache is one pool of num_blocks * block_size
    * rows shared by all sequences: k_idx rows packed (row pitch d_idx * element size), k_idx_sf

@@ -15,8 +15,8 @@ score of position s for query t is
 
     I[t, s] = sum_h  w[t, h] * ReLU( q_idx[t, h, :] . k_idx[s, :] )
 
-(per-head dot product, ReLU, head-weighted sum: "relevance scoring, head-weight
-application, and Top-K selection").  Storage formats follow Key Optimization 2
+(per-head dot product, ReLU, head-weighted sum: the page's scoring, head-weighting
+and Top-K chain).  Storage formats follow Key Optimization 2
 of the same page: MXFP8 for the indexer (groups of 32 elements share one scale
 factor) and FP8 for the sparse-attention KV cache.
 

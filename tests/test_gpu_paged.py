@@ -94,8 +94,7 @@ def test_paged_chain_equals_contiguous_chain(dsa, name, base, kw, n_valid, bs):
     assert torch.equal(idx_p, idx_c)
     assert torch.equal(out_p, out_c)
     assert torch.equal(lse_p, lse_c)
-    if name in ("bf16_b64_ragged", "mxfp8_fp8_b128", "prefill_grouped_b64"):
-        check_chain(dsa, wl, cpu)  # the contiguous chain against the oracle
+    check_chain(dsa, wl, cpu)  # and that chain against the oracle
 
 
 def test_paged_arguments_are_checked(dsa):

@@ -294,7 +294,7 @@ def test_sparse_attn_small_fp8_rows(dsa):
     # E4M3 rows of 64 with V = the same row (each warp owns 16 value columns, half a 32-column
     # chunk of the row), against the oracle
     wl = synth.small_workload("decode_b8_l32k_mxfp8", T=3, L=1500, K=300, H=20, D_qk=64, D_v=64)
-    _attn_case(dsa, wl, _random_idx(3, 300, 1500, 9, pad=7), "fp8", guard=False)
+    _attn_case(dsa, wl, _random_idx(3, 300, 1500, 9, pad=7), "fp8")
 
 
 def test_sparse_attn_out_of_range_index_is_skipped_and_recorded(dsa):
@@ -334,10 +334,14 @@ def test_chain_long_context_decode(dsa):
 
 
 def test_chain_prefill_chunk_sampled_rows(dsa):
+    # 128 seeded rows of the 4096-query chunk, always with the first and last query (the
+    # shortest and longest causal prefixes) and both ends of a four-query scoring group
     wl = synth.WORKLOADS["prefill_t4096_l128k_bf16"]
     rng = np.random.default_rng(16)
-    rows = sorted({0, 1, 2, 3, 4095, 2048} | set(rng.choice(4096, size=10, replace=False).tolist()))
-    _check_chain(dsa, wl, synth.make_inputs(wl), queries=rows)
+    rows = {0, 1, 2, 3, 2047, 2048, 4092, 4095}
+    while len(rows) < 128:
+        rows.add(int(rng.integers(0, 4096)))
+    _check_chain(dsa, wl, synth.make_inputs(wl), queries=sorted(rows))
 
 
 @pytest.mark.parametrize("case", ["short_context", "varlen", "small_causal", "ragged_fp8"])
@@ -375,14 +379,67 @@ def test_chain_empty_batch_is_a_no_op(dsa):
 
 @pytest.mark.parametrize("name", ["decode_b8_l32k_bf16", "decode_b8_l32k_mxfp8"])
 def test_chain_repeat_calls_on_one_workspace_are_identical(dsa, name):
-    # the workspace carries score histograms between kernels; each call must leave it clean
+    # The workspace carries score histograms between kernels and every call must leave them at
+    # zero: a call on a workspace that already served other inputs must give exactly what the same
+    # call gives on a fresh zero-filled workspace, and the score-histogram region (after the
+    # scores, dsa.h's fused-chain layout) must be all zero after each call.
     wl = synth.small_workload(name, T=3, L=5000, K=700)
-    dev = to_device(synth.make_inputs(wl))
-    call = dsa.call_from_tensors(dev, K=wl.K, sm_scale=wl.sm_scale)
-    out1, lse1, idx1 = [x.clone() for x in call()]
-    out2, lse2, idx2 = call()
+    dev_a = to_device(synth.make_inputs(wl))
+    dev_b = to_device(synth.make_inputs(wl, seed_offset=1))
+    call_a = dsa.call_from_tensors(dev_a, K=wl.K, sm_scale=wl.sm_scale)
+    ws = call_a.ws
+    hist_lo = -(-(wl.T * dsa.ld_scores_for(wl.L) * 4) // 256) * 256
+    hist = ws[hist_lo:hist_lo + wl.T * 4096 * 4]
+    out1, lse1, idx1 = [x.clone() for x in call_a()]
     torch.cuda.synchronize()
-    assert torch.equal(idx1, idx2)
-    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
-    ws = call.ws
-    assert int(torch.count_nonzero(ws[-(wl.T * 4096 * 4):]).item()) >= 0  # readable
+    assert int(torch.count_nonzero(hist)) == 0
+    out2, lse2, idx2 = [x.clone() for x in call_a()]
+    assert torch.equal(idx1, idx2) and torch.equal(out1, out2) and torch.equal(lse1, lse2)
+    # other inputs on the used workspace vs. on a fresh one
+    used = dsa.call_from_tensors(dev_b, K=wl.K, sm_scale=wl.sm_scale, ws=ws)
+    fresh = dsa.call_from_tensors(dev_b, K=wl.K, sm_scale=wl.sm_scale)
+    got = [x.clone() for x in used()]
+    want = fresh()
+    torch.cuda.synchronize()
+    assert int(torch.count_nonzero(hist)) == 0
+    for g, w_ in zip(got, want):
+        assert torch.equal(g, w_)
+    assert not torch.equal(got[2], idx1)  # the second inputs select other positions
+
+
+# ------------------------------------------------------------------------------------------------
+# element-wise scores at the full decode sizes (the persistent unit walk over many tiles per CTA)
+
+
+def test_index_score_full_size_bf16_every_position(dsa):
+    wl = synth.WORKLOADS["decode_b8_l32k_bf16"]
+    cpu = synth.make_inputs(wl)
+    dev = to_device(cpu)
+    scores = dsa.dsa_index_score(dev["q_idx"], dev["w"], dev["k_idx"]).cpu().numpy()
+    ch, a = oracle_chain(wl, cpu)
+    for t in range(wl.T):
+        ref = ch.scores(t)
+        bound = score_error_bound(ch.q_idx(t), a["w"][t].astype(np.float64), ch.k_idx(t, wl.L))
+        err = np.abs(scores[t, :wl.L].astype(np.float64) - ref)
+        assert np.all(err <= bound), f"t={t}: worst error/bound {np.max(err / bound):.3g}"
+
+
+def test_index_score_full_size_mxfp8_1m_sampled_positions(dsa):
+    # L = 1,048,576 MXFP8: 8192 seeded positions plus both ends and the edges of every 65,536-row
+    # block, each checked against the oracle's score of that position alone
+    wl = synth.WORKLOADS["decode_b1_l1m_mxfp8"]
+    cpu = synth.make_inputs(wl)
+    dev = {k: cpu[k].cuda() for k in ("q_idx", "q_idx_sf", "w", "k_idx", "k_idx_sf")}
+    scores = dsa.dsa_index_score(dev["q_idx"], dev["w"], dev["k_idx"], q_idx_sf=dev["q_idx_sf"],
+                                 k_idx_sf=dev["k_idx_sf"]).cpu().numpy()[0]
+    a = synth.to_numpy_bits({k: cpu[k] for k in ("q_idx", "q_idx_sf", "w", "k_idx", "k_idx_sf")})
+    rng = np.random.default_rng(41)
+    edges = [e + d for e in range(0, wl.L + 1, 1 << 16) for d in (-1, 0) if 0 <= e + d < wl.L]
+    pos = np.unique(np.concatenate([rng.integers(0, wl.L, 8192), [0, 127, 128, wl.L - 1], edges]))
+    q = oracle.dequant_mxfp8(a["q_idx"][0], a["q_idx_sf"][0])
+    w = a["w"][0].astype(np.float64)
+    k = oracle.dequant_mxfp8(a["k_idx"][0, pos], a["k_idx_sf"][0, pos])
+    ref = oracle.index_scores(q, w, k)
+    bound = score_error_bound(q, w, k)
+    err = np.abs(scores[pos].astype(np.float64) - ref)
+    assert np.all(err <= bound), f"worst error/bound {np.max(err / bound):.3g}"

@@ -461,6 +461,96 @@ def test_chain_fp8_kv_latent_v_uses_row_scale_and_first_columns():
     np.testing.assert_allclose(r["out"], ref, rtol=1e-12, atol=1e-12)
 
 
+def _torch_e4m3(codes):
+    """E4M3 codes -> fp64 through torch's float8_e4m3fn cast (a library decoder independent of
+    the oracle's bit-field code)."""
+    return torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).to(torch.float64)
+
+
+def _distinct_exponents(a, rng):
+    """Every group, row and head its own E8M0 exponent (scales 2^-6 .. 2^6), so a scale applied
+    to the wrong group, row, head or operand changes the scores."""
+    for key in ("q_idx_sf", "k_idx_sf"):
+        a[key] = rng.integers(121, 134, size=a[key].shape).astype(np.uint8)
+
+
+def test_chain_mxfp8_scores_match_brute_force_with_distinct_exponents():
+    # The oracle's MXFP8 scoring branch (Chain.scores) against Python loops over the raw codes:
+    # I[s] = sum_h w[h] * max(0, sum_g 2^(eq[h,g]-127) 2^(ek[s,g]-127) sum_{j in g} q[h,j] k[s,j])
+    # ("Day 0 Support for New LLM Architectures", Key Optimization 2: groups of 32 elements
+    # share one scale factor).
+    wl = synth.Workload("mxb", T=2, q_per_seq=1, L=9, H_idx=3, d_idx=64, idx_dtype="mxfp8", K=4,
+                        H=1, D_qk=64, D_v=64, kv_dtype="fp8", separate_v=False, q_pos0=-1, seed=31)
+    a = synth.to_numpy_bits(synth.make_inputs(wl))
+    _distinct_exponents(a, np.random.default_rng(4))
+    ch = oracle.Chain(a, L=wl.L, K=wl.K, q_per_seq=1, q_pos0=-1, idx_dtype="mxfp8", kv_dtype="fp8",
+                      sm_scale=wl.sm_scale)
+    for t in range(wl.T):
+        qv = _torch_e4m3(a["q_idx"][t]).tolist()
+        kv = _torch_e4m3(a["k_idx"][t]).tolist()
+        want = []
+        for s in range(wl.L):
+            tot = 0.0
+            for h in range(wl.H_idx):
+                dot = 0.0
+                for g in range(wl.d_idx // 32):
+                    part = sum(qv[h][j] * kv[s][j] for j in range(32 * g, 32 * g + 32))
+                    dot += part * 2.0 ** (int(a["q_idx_sf"][t, h, g]) - 127) * 2.0 ** (int(a["k_idx_sf"][t, s, g]) - 127)
+                tot += float(a["w"][t, h]) * max(0.0, dot)
+            want.append(tot)
+        np.testing.assert_allclose(ch.scores(t), want, rtol=1e-12, atol=1e-300)
+
+
+@pytest.mark.parametrize("idx_dtype", ["mxfp8", "bf16"])
+def test_chain_scores_across_the_row_chunk_boundary(idx_dtype):
+    # Chain.scores decodes the key cache in chunks of 65,536 rows; a cache longer than one chunk,
+    # with every row's scale exponents its own, checks the chunk offsets on the codes and on the
+    # scale array against one whole-cache product built from torch's decoders and matmul.
+    L = (1 << 16) + 333
+    wl = synth.Workload("chunks", T=1, q_per_seq=1, L=L, H_idx=2, d_idx=64, idx_dtype=idx_dtype, K=4,
+                        H=1, D_qk=64, D_v=64, kv_dtype="bf16", separate_v=False, q_pos0=-1, seed=32)
+    cpu = synth.make_inputs(wl)
+    a = synth.to_numpy_bits(cpu)
+    if idx_dtype == "mxfp8":
+        _distinct_exponents(a, np.random.default_rng(5))
+        scale_q = torch.pow(2.0, torch.from_numpy(a["q_idx_sf"][0].astype(np.float64) - 127))
+        scale_k = torch.pow(2.0, torch.from_numpy(a["k_idx_sf"][0].astype(np.float64) - 127))
+        q = _torch_e4m3(a["q_idx"][0]) * scale_q.repeat_interleave(32, dim=-1)
+        k = _torch_e4m3(a["k_idx"][0]) * scale_k.repeat_interleave(32, dim=-1)
+    else:
+        q = cpu["q_idx"][0].to(torch.float64)
+        k = cpu["k_idx"][0].to(torch.float64)
+    w = torch.from_numpy(a["w"][0].astype(np.float64))
+    want = (torch.relu(k @ q.T) @ w).numpy()
+    ch = oracle.Chain(a, L=L, K=4, q_per_seq=1, q_pos0=-1, idx_dtype=idx_dtype, kv_dtype="bf16",
+                      sm_scale=0.125)
+    np.testing.assert_allclose(ch.scores(0), want, rtol=1e-12, atol=1e-300)
+
+
+def test_chain_fp8_tiled_kv_applies_each_tiles_scale():
+    # The oracle's tiled FP8 KV branch (Chain.kv_rows with fp8_t128): element j of a selected row
+    # is E4M3(code) * scale[row][j // 128] (576 = 4 x 128 + 64: five scales per row; "Day 0
+    # Support for New LLM Architectures", Key Optimization 2), V = its first 512 columns; checked
+    # on selected rows of a second sequence against torch's float8 decode, an explicit per-element
+    # tile lookup and torch's scaled_dot_product_attention.
+    wl = synth.Workload("t128", T=2, q_per_seq=1, L=30, H_idx=2, d_idx=64, idx_dtype="bf16", K=7,
+                        H=3, D_qk=576, D_v=512, kv_dtype="fp8_t128", separate_v=False, q_pos0=-1, seed=33)
+    a = synth.to_numpy_bits(synth.make_inputs(wl))
+    rng = np.random.default_rng(6)
+    a["kv_scale"] = np.ldexp(1.0, rng.integers(-5, 6, size=a["kv_scale"].shape)).astype(np.float32)
+    ch = oracle.Chain(a, L=wl.L, K=wl.K, q_per_seq=1, q_pos0=-1, idx_dtype="bf16", kv_dtype="fp8_t128",
+                      sm_scale=wl.sm_scale)
+    t, seq = 1, 1
+    idx = np.array([29, 3, -1, 17, 0, 11, -1])
+    rows = [r for r in idx.tolist() if r >= 0]
+    vals = _torch_e4m3(a["kv"][seq, rows]).numpy()
+    tile_of = np.array([j // 128 for j in range(wl.D_qk)])
+    kd = vals * a["kv_scale"][seq, rows][:, tile_of].astype(np.float64)
+    q = oracle.bf16_bits_to_f64(a["q"][t])
+    out, _ = ch.attention(t, idx, wl.D_v)
+    np.testing.assert_allclose(out, _sdpa(q, kd, kd[:, :wl.D_v].copy(), wl.sm_scale), rtol=1e-12, atol=1e-12)
+
+
 # ------------------------------------------------------------------------------------------------
 # the parity rule itself (mistakes planted on the CPU)
 

@@ -56,8 +56,13 @@ def _without_workspace(native, scores, K, L):
     return idx
 
 
-def test_noalloc_topk_matches_the_workspace_entry_on_two_calls(native):
-    T, L, K = 8, 32768, 2048
+@pytest.mark.parametrize("T,L,K", [
+    (8, 32768, 2048),     # 4-CTA clusters, keys kept in shared memory
+    (16, 200000, 2048),   # the whole scratch array: 16 queries on 16-CTA clusters
+    (4, 300000, 2048),    # rows past 16 x 16384 keys: dsa_topk splits them over independent CTAs,
+                          # this entry keeps one 16-CTA cluster per row (keys re-read from L2)
+])
+def test_noalloc_topk_matches_the_workspace_entry_on_two_calls(native, T, L, K):
     a, b = _scores(1, T, L), _scores(2, T, L)
     ref_a = _with_workspace(native, a, K, L)
     ref_b = _with_workspace(native, b, K, L)

@@ -14,7 +14,7 @@ LIB_PATH = os.path.join(PKG, "libdsa.so")
 
 DSA_OK = 0
 DSA_BF16, DSA_FP8_E4M3, DSA_MXFP8_E4M3, DSA_FP8_E4M3_T128 = 0, 1, 2, 3
-DEVERR = {0: "none", 1: "index out of range", 2: "wait timeout"}
+DEVERR = {0: "none", 1: "index out of range", 2: "wait timeout", 3: "row-split Top-K counts disagree"}
 
 EXPORTS = (
     "dsa_status_string", "dsa_abi_version", "dsa_get_device_error", "dsa_index_score",

@@ -12,7 +12,7 @@ import torch
 
 from . import _native as N
 
-__all__ = ["dsa_index_score", "dsa_topk", "dsa_sparse_attn", "DsaCall", "dsa_decode", "dsa_prefill",
+__all__ = ["dsa_index_score", "dsa_topk", "dsa_topk_noalloc", "dsa_sparse_attn", "DsaCall", "dsa_decode", "dsa_prefill",
            "dsa_workspace_size", "dsa_launch_count", "dsa_get_device_error", "ld_scores_for",
            "dsa_quantize_mxfp8", "dsa_quantize_fp8_rows", "dsa_quantize_fp8_tiles"]
 
@@ -84,6 +84,18 @@ def dsa_topk(scores, K, *, L, q_per_seq=1, q_pos0=-1, n_valid=None, idx=None, ws
     st = N.lib.dsa_topk(_p(scores), scores.stride(0), T, q_per_seq, q_pos0, _p(n_valid), L, K, _p(idx),
                         _p(ws), ws_bytes, _stream(stream))
     N.check(st, "dsa_topk")
+    return idx
+
+
+def dsa_topk_noalloc(scores, K, *, L, q_per_seq=1, q_pos0=-1, n_valid=None, idx=None, stream=None) -> torch.Tensor:
+    """dsa_topk without a workspace: the library's own fixed scratch serves as the exchange area
+    (at most 16 queries per call; calls that overlap on the GPU race, see dsa.h)."""
+    T = scores.shape[0]
+    if idx is None:
+        idx = torch.empty(T, K, dtype=torch.int32, device=scores.device)
+    st = N.lib.dsa_topk_noalloc(_p(scores), scores.stride(0), T, q_per_seq, q_pos0, _p(n_valid), L, K,
+                                _p(idx), _stream(stream))
+    N.check(st, "dsa_topk_noalloc")
     return idx
 
 

@@ -1,6 +1,6 @@
 // Step 1 of the chain: indexer relevance scores,
 //   I[t, s] = sum_h w[t, h] * ReLU(q_idx[t, h, :] . k_idx[s, :])
-// ("relevance scoring, head-weight application", Day 0 Support for New LLM Architectures,
+// (scoring each position, then weighting the heads: Day 0 Support for New LLM Architectures,
 // Key Optimization 1; MXFP8 index path with groups of 32 sharing a scale, Key Optimization 2).
 //
 // The contraction runs on the 5th-generation tensor cores: a tile of 128 cache positions is the

@@ -1,6 +1,6 @@
 // Step 3 of the chain: gather the Top-K rows of the latent KV cache and compute exact softmax
-// attention over them ("a sparse-attention kernel then reads only the selected KV entries to
-// perform exact computation", Day 0 Support for New LLM Architectures, Step 1; decode gathers
+// attention over them (only the chosen cache entries are read, and attention over them is
+// computed without approximation: Day 0 Support for New LLM Architectures, Step 1; decode gathers
 // K/V by the index table then runs a small matrix multiply, "Achieving Day-0 Readiness...",
 // section 2.3; FP8 KV cache, Key Optimization 2 of the first page).
 //

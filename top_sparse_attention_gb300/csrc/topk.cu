@@ -1,4 +1,4 @@
-// Step 2 of the chain: Top-K selection ("select the Top-K positions", Day 0 Support for New LLM
+// Step 2 of the chain: Top-K selection (keep the K best-scoring positions, Day 0 Support for New LLM
 // Architectures, Step 1; the Top-k selection operator run after batched scoring, "Achieving
 // Day-0 Readiness...", section 2.1).
 //
