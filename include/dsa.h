@@ -191,6 +191,74 @@ dsa_status dsa_sparse_attn(const void* q, const void* kv, const void* kv_v, cons
 size_t dsa_sparse_attn_workspace_size(int T, int H, int K, int D_v);
 
 /* --------------------------------------------------------------------------------------------
+ * Context split over slices: the pieces of a decode whose context is cut into G position ranges
+ * (slices), each held by one device (the KV cache distributed by token with the communication
+ * overlapped by compute, "Day-0 Support for Large Model Inference: From Operator Optimization to
+ * Production Serving"; the index and attention steps of "Day 0 Support for New LLM
+ * Architectures", Step 1, applied per slice).  Every position of the global Top-K is among the
+ * Top-K of its own slice, so:
+ *   1. each slice scores its positions (dsa_index_score on its rows) and emits its Top-K as
+ *      (score, global position) pairs (dsa_topk_pairs);
+ *   2. the G x K pairs of a query are put side by side (an all-gather across devices) and
+ *      dsa_topk_merge selects the global K;
+ *   3. each slice attends over the selected positions it holds (dsa_sparse_attn_partial), giving a
+ *      normalised fp32 output and its log-sum-exp;
+ *   4. dsa_attn_combine merges the G partial outputs (after a gather across devices).
+ * The result equals the unsplit chain up to floating-point rounding of the attention; the index
+ * set is the same (exact ties resolved toward the lower position in both).
+ * ------------------------------------------------------------------------------------------ */
+
+/* dsa_topk_pairs: dsa_topk over one slice (its scores, visible lengths and L are the slice's own),
+ * writing for query t, slot k < K:  cand_pos[t*ld_cand + k] = the selected slice position plus
+ * pos_offset (the slice's first position in the whole context), -1 in empty slots, and
+ * cand_scores[t*ld_cand + k] = that position's score (0 in empty slots).  Positions come in
+ * ascending order.  ld_cand >= K (so G slices can write side by side into one [T][G*K] buffer at
+ * column offsets g*K).  ws / ws_bytes as for dsa_topk (dsa_topk_workspace_size(T, L, K)).
+ * pos_offset >= 0 and pos_offset + L < 2^31. */
+dsa_status dsa_topk_pairs(const float* scores, int64_t ld_scores, int T, int q_per_seq, int q_pos0,
+                          const int32_t* n_valid, int L, int K, int pos_offset, int32_t* cand_pos,
+                          float* cand_scores, int64_t ld_cand, void* ws, size_t ws_bytes, void* stream);
+
+/* dsa_topk_merge: each query t has parts * per_part candidates; candidate j = g * per_part + k
+ * (part g, entry k) sits at element offset g * part_stride + t * ld_cand + k of cand_scores (fp32)
+ * and of cand_pos (int32).  So one [T][parts * per_part] buffer is ld_cand = parts * per_part,
+ * part_stride = per_part, and parts gathered from devices as [parts][T][per_part] are
+ * ld_cand = per_part, part_stride = T * per_part.  Among the candidates with cand_pos >= 0, the
+ * min(K, count) with the largest scores, exact ties resolved toward the lower position, are
+ * written to idx[t*K ..] in candidate order (j ascending), then -1.  (Parts in ascending slice
+ * order, each with ascending positions as dsa_topk_pairs writes them, therefore give ascending
+ * positions.)  Positions must be distinct within a query and the layout must not make two
+ * candidates share an element (both layouts above satisfy this).  No workspace; one CTA per query.
+ * Checked: ld_cand >= per_part when T > 1, part_stride >= per_part when parts > 1.
+ * Supported: parts * per_part <= 16384, 1 <= K <= 4096. */
+dsa_status dsa_topk_merge(const float* cand_scores, const int32_t* cand_pos, int T, int parts, int per_part,
+                          int64_t ld_cand, int64_t part_stride, int K, int32_t* idx, void* stream);
+
+/* dsa_sparse_attn_partial: dsa_sparse_attn for one slice whose cache holds context positions
+ * [pos_lo, pos_lo + L): entries of idx in that range attend to cache row idx - pos_lo; every other
+ * entry (-1, or a position held by another slice) is skipped without error.  Output, fp32:
+ * o_part [T, H, D_v] = the softmax-weighted sum over this slice's attended rows (normalised over
+ * them; 0 when there are none), lse_part [T, H] = their natural log-sum-exp (-inf when none).
+ * Same arguments, layouts and support as dsa_sparse_attn otherwise; workspace
+ * dsa_sparse_attn_workspace_size(T, H, K, D_v).  o_part 16-byte aligned, lse_part required. */
+dsa_status dsa_sparse_attn_partial(const void* q, const void* kv, const void* kv_v, const float* kv_scale,
+                                   int64_t kv_row_stride, int64_t kv_seq_stride, int64_t v_row_stride,
+                                   int64_t v_seq_stride, const int32_t* idx, int T, int q_per_seq, int L,
+                                   int K, int H, int D_qk, int D_v, float sm_scale, dsa_dtype kv_dtype,
+                                   int pos_lo, float* o_part, float* lse_part, void* ws, size_t ws_bytes,
+                                   void* stream);
+
+/* dsa_attn_combine: merges G partial outputs.  Part g: o_parts + g*o_part_stride (fp32 [T, H, D_v])
+ * and lse_parts + g*lse_part_stride (fp32 [T, H]); strides in elements.  With M = max_g lse_g:
+ *   out[t,h,:] = sum_g e^(lse_g - M) o_g / sum_g e^(lse_g - M)   (bf16)
+ *   lse[t,h]   = M + ln sum_g e^(lse_g - M)                       (fp32, or NULL)
+ * Parts with lse = -inf contribute nothing; all -inf gives out = 0, lse = -inf.  D_v a multiple
+ * of 4; o_parts (and o_part_stride * 4 bytes) and out 16-byte aligned. */
+dsa_status dsa_attn_combine(const float* o_parts, const float* lse_parts, int G, int64_t o_part_stride,
+                            int64_t lse_part_stride, int T, int H, int D_v, void* out, float* lse,
+                            void* stream);
+
+/* --------------------------------------------------------------------------------------------
  * dsa_quantize_mxfp8 / dsa_quantize_fp8_rows -- online quantisation that writes the caches the
  * chain reads ("Day 0 Support for New LLM Architectures", Key Optimization 2: the indexer stores
  * MXFP8, groups of 32 elements sharing one scale factor; the sparse-attention KV cache stores

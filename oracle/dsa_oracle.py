@@ -38,7 +38,7 @@ __all__ = [
     "bf16_bits_to_f64", "e4m3_to_f64", "e8m0_to_f64", "dequant_mxfp8", "dequant_fp8_rows",
     "e4m3_encode", "quantize_mxfp8", "quantize_fp8_rows", "dequant_fp8_tiles", "quantize_fp8_tiles",
     "index_scores", "topk_positions", "sparse_attention", "visible_length", "query_sequence",
-    "Chain", "chain_query",
+    "Chain", "chain_query", "merge_candidates", "combine_partials",
 ]
 
 
@@ -261,6 +261,48 @@ def sparse_attention(q: np.ndarray, k_rows: np.ndarray, v_rows: np.ndarray, sm_s
     out = (p @ v_rows) / l
     lse = (mx + np.log(l))[:, 0]
     return out, lse
+
+
+# ----------------------------------------------------------------------------------------------
+# A context split over slices (the KV cache distributed by token: "Day-0 Support for Large Model
+# Inference: From Operator Optimization to Production Serving"; each slice runs the index and
+# attention steps of "Day 0 Support for New LLM Architectures", Step 1, on its own positions)
+
+
+def merge_candidates(scores: np.ndarray, positions: np.ndarray, K: int) -> np.ndarray:
+    """Top-K of a list of (score, position) candidates; entries with a negative position are empty.
+
+    The min(K, m) valid entries that come first in the order (score descending, position
+    ascending) are kept and returned as positions in the order of the candidate list, followed by
+    -1 in the remaining slots.
+    """
+    s = np.asarray(scores, dtype=np.float64)
+    p = np.asarray(positions, dtype=np.int64)
+    valid = np.flatnonzero(p >= 0)
+    order = np.lexsort((p[valid], -s[valid]))
+    kept = np.sort(valid[order[: min(K, valid.size)]])  # back into list order
+    out = np.full(K, -1, dtype=np.int64)
+    out[: kept.size] = p[kept]
+    return out
+
+
+def combine_partials(o_parts: np.ndarray, lse_parts: np.ndarray):
+    """Attention outputs of disjoint row sets merged into the output over their union.
+
+    o_parts [G, H, D_v] (each normalised over its own rows), lse_parts [G, H] (natural log-sum-exp
+    of its logits; -inf for an empty set) -> out [H, D_v], lse [H]:
+    lse = log sum_g exp(lse_g) and out = sum_g exp(lse_g - lse) o_g.  All parts empty: 0 and -inf.
+    """
+    o = np.asarray(o_parts, dtype=np.float64)
+    l = np.asarray(lse_parts, dtype=np.float64)
+    M = np.max(l, axis=0)
+    Mu = np.where(np.isfinite(M), M, 0.0)
+    w = np.where(np.isfinite(l), np.exp(l - Mu[None, :]), 0.0)  # [G, H]
+    tot = w.sum(axis=0)
+    safe = np.where(tot > 0, tot, 1.0)
+    out = np.einsum("gh,ghd->hd", w, np.where(np.isfinite(l)[..., None], o, 0.0)) / safe[:, None]
+    lse = np.where(tot > 0, Mu + np.log(safe), -np.inf)
+    return np.where(tot[:, None] > 0, out, 0.0), lse
 
 
 # ----------------------------------------------------------------------------------------------

@@ -552,6 +552,71 @@ def test_chain_fp8_tiled_kv_applies_each_tiles_scale():
 
 
 # ------------------------------------------------------------------------------------------------
+# a context split over slices: candidate merge and partial-output combine
+
+
+def test_merge_candidates_brute_force_tiny():
+    # every candidate list of length 6 over scores {0, 1, 2} with empty entries, against Python's
+    # sorted() on (-score, position) tuples
+    rng = np.random.default_rng(50)
+    for _ in range(300):
+        n = 6
+        s = rng.integers(0, 3, n).astype(np.float64)
+        p = rng.permutation(40)[:n]
+        p[rng.random(n) < 0.3] = -1
+        K = int(rng.integers(1, 8))
+        valid = [j for j in range(n) if p[j] >= 0]
+        best = sorted(valid, key=lambda j: (-s[j], p[j]))[:K]
+        want = [int(p[j]) for j in sorted(best)] + [-1] * (K - len(best))
+        assert oracle.merge_candidates(s, p, K).tolist() == want
+
+
+def test_merge_of_all_positions_is_topk_of_the_row():
+    rng = np.random.default_rng(51)
+    s = np.round(rng.standard_normal(3000) * 4)  # many exact ties
+    pos = rng.permutation(3000)
+    got = oracle.merge_candidates(s[pos], pos, 700)
+    assert sorted(got.tolist()) == sorted(oracle.topk_positions(s, 700).tolist())
+
+
+@pytest.mark.parametrize("G,tie", [(2, False), (5, False), (4, True)])
+def test_merge_of_slice_topks_is_the_global_topk(G, tie):
+    # the fact the split decode rests on: every global Top-K position is in its slice's Top-K, so
+    # merging the slices' selections (slices in order, ascending positions) gives the global set in
+    # ascending order; with ties across slices the lower positions still win
+    rng = np.random.default_rng(52 + G)
+    n, K = 5000, 300
+    s = np.round(rng.standard_normal(n)) if tie else rng.standard_normal(n)
+    bounds = np.linspace(0, n, G + 1).astype(int)
+    cand_s, cand_p = [], []
+    for g in range(G):
+        lo, hi = bounds[g], bounds[g + 1]
+        local = oracle.topk_positions(s[lo:hi], K)
+        local = np.concatenate([np.sort(local[local >= 0]), local[local < 0]])  # ascending, as listed
+        ok = local >= 0
+        cand_p.append(np.where(ok, local + lo, -1))
+        cand_s.append(np.where(ok, s[lo:hi][np.where(ok, local, 0)], 0.0))
+    got = oracle.merge_candidates(np.concatenate(cand_s), np.concatenate(cand_p), K)
+    want = np.sort(oracle.topk_positions(s, K))
+    np.testing.assert_array_equal(got, want)
+
+
+def test_combine_of_partials_over_a_partition_is_the_whole_attention():
+    rng = np.random.default_rng(53)
+    q, k, v = rng.standard_normal((3, 16)), rng.standard_normal((50, 16)) * 2, rng.standard_normal((50, 5))
+    full, lf = oracle.sparse_attention(q, k, v, 0.4)
+    cuts = [0, 7, 7, 31, 50]  # the second part is empty
+    parts = [oracle.sparse_attention(q, k[a:b], v[a:b], 0.4) for a, b in zip(cuts[:-1], cuts[1:])]
+    out, lse = oracle.combine_partials(np.stack([o for o, _ in parts]), np.stack([l for _, l in parts]))
+    np.testing.assert_allclose(out, full, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, lf, rtol=1e-13)
+    # against torch's scaled_dot_product_attention as well, and all-empty parts give 0 and -inf
+    np.testing.assert_allclose(out, _sdpa(q, k, v, 0.4), rtol=1e-12, atol=1e-12)
+    e_out, e_lse = oracle.combine_partials(np.zeros((2, 3, 5)), np.full((2, 3), -np.inf))
+    assert np.all(e_out == 0) and np.all(np.isneginf(e_lse))
+
+
+# ------------------------------------------------------------------------------------------------
 # the parity rule itself (mistakes planted on the CPU)
 
 

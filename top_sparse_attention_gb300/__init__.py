@@ -11,6 +11,7 @@ import importlib
 _API = ("DsaCall", "dsa_decode", "dsa_get_device_error", "dsa_index_score", "dsa_launch_count", "dsa_prefill",
         "dsa_quantize_mxfp8", "dsa_quantize_fp8_rows", "dsa_quantize_fp8_tiles",
         "dsa_selftest_wait_timeout", "dsa_sparse_attn", "dsa_topk", "dsa_topk_noalloc", "dsa_workspace_size",
+        "dsa_topk_pairs", "dsa_topk_merge", "dsa_sparse_attn_partial", "dsa_attn_combine",
         "ld_scores_for")
 _NATIVE = ("DsaError", "LIB_PATH", "EXPORTS")
 

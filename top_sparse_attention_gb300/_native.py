@@ -21,7 +21,8 @@ EXPORTS = (
     "dsa_topk", "dsa_topk_workspace_size", "dsa_sparse_attn", "dsa_sparse_attn_workspace_size",
     "dsa_quantize_mxfp8", "dsa_quantize_fp8_rows", "dsa_quantize_fp8_tiles",
     "dsa_workspace_size", "dsa_launch_count", "dsa_decode", "dsa_prefill", "dsa_topk_noalloc",
-    "dsa_selftest_wait_timeout",
+    "dsa_selftest_wait_timeout", "dsa_topk_pairs", "dsa_topk_merge", "dsa_sparse_attn_partial",
+    "dsa_attn_combine",
 )
 
 
@@ -72,6 +73,11 @@ def _load():
         "dsa_sparse_attn": (I, [P, P, P, P, I64, I64, I64, I64, P, I, I, I, I, I, I, I, F, I, P, P,
                                 P, SZ, P]),
         "dsa_sparse_attn_workspace_size": (SZ, [I, I, I, I]),
+        "dsa_topk_pairs": (I, [P, I64, I, I, I, P, I, I, I, P, P, I64, P, SZ, P]),
+        "dsa_topk_merge": (I, [P, P, I, I, I, I64, I64, I, P, P]),
+        "dsa_sparse_attn_partial": (I, [P, P, P, P, I64, I64, I64, I64, P, I, I, I, I, I, I, I, F, I, I,
+                                        P, P, P, SZ, P]),
+        "dsa_attn_combine": (I, [P, P, I, I64, I64, I, I, I, P, P, P]),
         "dsa_quantize_mxfp8": (I, [P, I64, I, I, P, P, P, P]),
         "dsa_quantize_fp8_rows": (I, [P, I64, I, I, P, I64, P, P, P]),
         "dsa_quantize_fp8_tiles": (I, [P, I64, I, I, I, P, I64, P, P, P]),

@@ -12,7 +12,8 @@ import torch
 
 from . import _native as N
 
-__all__ = ["dsa_index_score", "dsa_topk", "dsa_topk_noalloc", "dsa_sparse_attn", "DsaCall", "dsa_decode", "dsa_prefill",
+__all__ = ["dsa_index_score", "dsa_topk", "dsa_topk_noalloc", "dsa_topk_pairs", "dsa_topk_merge",
+           "dsa_sparse_attn_partial", "dsa_attn_combine", "dsa_sparse_attn", "DsaCall", "dsa_decode", "dsa_prefill",
            "dsa_workspace_size", "dsa_launch_count", "dsa_get_device_error", "ld_scores_for",
            "dsa_quantize_mxfp8", "dsa_quantize_fp8_rows", "dsa_quantize_fp8_tiles"]
 
@@ -120,6 +121,77 @@ def dsa_sparse_attn(q, kv, idx, *, sm_scale, kv_v=None, kv_scale=None, D_v=None,
                                _p(idx), T, q_per_seq, L, K, H, D_qk, D_v, float(sm_scale), _kv_dtype(kv, kv_scale),
                                _p(out), _p(lse), _p(ws), 0 if ws is None else ws.numel(), _stream(stream))
     N.check(st, "dsa_sparse_attn")
+    return out, lse
+
+
+def dsa_topk_pairs(scores, K, *, L, pos_offset, cand_pos, cand_scores, q_per_seq=1, q_pos0=-1, n_valid=None,
+                   ws=None, stream=None):
+    """One context slice's Top-K as (score, global position) pairs written into the [T, >= K]
+    views cand_pos (int32) / cand_scores (fp32), which may be column slices of a wider buffer."""
+    T = scores.shape[0]
+    ws_bytes = N.lib.dsa_topk_workspace_size(T, L, K)
+    if ws is None:
+        ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=scores.device)
+    st = N.lib.dsa_topk_pairs(_p(scores), scores.stride(0), T, q_per_seq, q_pos0, _p(n_valid), L, K,
+                              int(pos_offset), _p(cand_pos), _p(cand_scores), cand_pos.stride(0), _p(ws),
+                              ws.numel(), _stream(stream))
+    N.check(st, "dsa_topk_pairs")
+    return cand_pos, cand_scores
+
+
+def dsa_topk_merge(cand_scores, cand_pos, K, *, idx=None, stream=None) -> torch.Tensor:
+    """The K best (score, position) pairs of each query's candidates (-1 positions are empty), in
+    candidate order, -1 padded.  Candidates as [T, n] (one part per query row) or as [G, T, n]
+    (G parts, e.g. gathered from G devices), contiguous in the last axis."""
+    if cand_pos.dim() == 2:
+        T, n = cand_pos.shape
+        parts, ld, pst = 1, cand_pos.stride(0), 0
+    else:
+        parts, T, n = cand_pos.shape
+        ld, pst = cand_pos.stride(1), cand_pos.stride(0)
+    if idx is None:
+        idx = torch.empty(T, K, dtype=torch.int32, device=cand_pos.device)
+    st = N.lib.dsa_topk_merge(_p(cand_scores), _p(cand_pos), T, parts, n, ld, pst, K, _p(idx), _stream(stream))
+    N.check(st, "dsa_topk_merge")
+    return idx
+
+
+def dsa_sparse_attn_partial(q, kv, idx, *, sm_scale, pos_lo, kv_v=None, kv_scale=None, D_v=None, q_per_seq=1,
+                            o_part=None, lse_part=None, ws=None, stream=None):
+    """Attention of one context slice (cache rows = positions pos_lo .. pos_lo + L - 1) over the
+    entries of idx it holds: fp32 normalised output [T, H, D_v] and its log-sum-exp [T, H]."""
+    T, H, D_qk = q.shape
+    L = kv.shape[1]
+    K = idx.shape[1]
+    if D_v is None:
+        D_v = kv_v.shape[-1] if kv_v is not None else (512 if D_qk == 576 else D_qk)
+    if o_part is None:
+        o_part = torch.empty(T, H, D_v, dtype=torch.float32, device=q.device)
+    if lse_part is None:
+        lse_part = torch.empty(T, H, dtype=torch.float32, device=q.device)
+    need = N.lib.dsa_sparse_attn_workspace_size(T, H, K, D_v)
+    if ws is None and need:
+        ws = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    st = N.lib.dsa_sparse_attn_partial(
+        _p(q), _p(kv), _p(kv_v), _p(kv_scale), kv.stride(1) * kv.element_size(), _seq_stride(kv),
+        0 if kv_v is None else kv_v.stride(1) * 2, _seq_stride(kv_v), _p(idx), T, q_per_seq, L, K, H, D_qk, D_v,
+        float(sm_scale), _kv_dtype(kv, kv_scale), int(pos_lo), _p(o_part), _p(lse_part), _p(ws),
+        0 if ws is None else ws.numel(), _stream(stream))
+    N.check(st, "dsa_sparse_attn_partial")
+    return o_part, lse_part
+
+
+def dsa_attn_combine(o_parts, lse_parts, *, out=None, lse=None, stream=None):
+    """Merge of G partial outputs o_parts [G, T, H, D_v] fp32 / lse_parts [G, T, H] into the bf16
+    output [T, H, D_v] and its log-sum-exp [T, H]."""
+    G, T, H, D_v = o_parts.shape
+    if out is None:
+        out = torch.empty(T, H, D_v, dtype=torch.bfloat16, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty(T, H, dtype=torch.float32, device=o_parts.device)
+    st = N.lib.dsa_attn_combine(_p(o_parts), _p(lse_parts), G, o_parts.stride(0), lse_parts.stride(0), T, H, D_v,
+                                _p(out), _p(lse), _stream(stream))
+    N.check(st, "dsa_attn_combine")
     return out, lse
 
 

@@ -203,7 +203,8 @@ cudaError_t run_topk(const dsa_args& a, int t_off, int T, const float* scores, i
 // valid_prefix: idx rows hold each query's min(K, n_t) selected positions first and -1 after
 // them (the chain's own Top-K output), so the attention may stop at the last valid row.
 cudaError_t run_sparse_attn(const dsa_args& a, int t_off, int T, const int32_t* idx, void* ws,
-                            cudaStream_t st, bool pdl, bool valid_prefix) {
+                            cudaStream_t st, bool pdl, bool valid_prefix, int slice_pos_lo = -1,
+                            float* out_f32 = nullptr) {
   SparseAttnParams p = {};
   p.q = reinterpret_cast<const __nv_bfloat16*>(a.q) + (int64_t)t_off * a.H * a.D_qk;
   p.kv = reinterpret_cast<const uint8_t*>(a.kv);
@@ -228,6 +229,9 @@ cudaError_t run_sparse_attn(const dsa_args& a, int t_off, int T, const int32_t* 
   p.q_pos0 = a.q_pos0;
   p.n_valid = a.n_valid;
   p.pages = pages_of(a);
+  p.slice_rows = slice_pos_lo >= 0;
+  p.pos_lo = slice_pos_lo;
+  p.out_f32 = out_f32;
   return launch_sparse_attn(p, a.D_qk, a.D_v, a.kv_dtype != DSA_BF16, a.kv_v != nullptr, ws, st, pdl,
                             a.kv_dtype == DSA_FP8_E4M3_T128);
 }
@@ -455,6 +459,126 @@ dsa_status dsa_topk(const float* scores, int64_t ld_scores, int T, int q_per_seq
   a.L = L;
   a.K = K;
   return from_cuda(run_topk(a, 0, T, scores, ld_scores, idx, nullptr, ws, reinterpret_cast<cudaStream_t>(stream), false));
+}
+
+dsa_status dsa_topk_pairs(const float* scores, int64_t ld_scores, int T, int q_per_seq, int q_pos0,
+                          const int32_t* n_valid, int L, int K, int pos_offset, int32_t* cand_pos,
+                          float* cand_scores, int64_t ld_cand, void* ws, size_t ws_bytes, void* stream) {
+  dsa_status s = check_topk(scores, ld_scores, T, q_per_seq, q_pos0, n_valid, L, K, cand_pos);
+  if (s != DSA_OK || T == 0) return s;
+  if (!cand_scores || ld_cand < K || pos_offset < 0 || (int64_t)pos_offset + L > INT32_MAX)
+    return DSA_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < topk_ws_bytes(T, L, K) || !aligned16(ws)) return DSA_ERR_WORKSPACE;
+  if ((s = check_device()) != DSA_OK) return s;
+  TopkParams p = {};
+  p.scores = scores;
+  p.ld_scores = ld_scores;
+  p.n_valid = n_valid;
+  p.idx = cand_pos;
+  p.idx_ld = ld_cand;
+  p.T = T;
+  p.q_per_seq = q_per_seq;
+  p.q_pos0 = q_pos0;
+  p.L = L;
+  p.K = K;
+  p.err = device_error_ptr();
+  PairsParams pp = {};
+  pp.scores = scores;
+  pp.ld_scores = ld_scores;
+  pp.cand_pos = cand_pos;
+  pp.cand_scores = cand_scores;
+  pp.ld_cand = ld_cand;
+  pp.T = T;
+  pp.K = K;
+  pp.pos_offset = pos_offset;
+  return from_cuda(launch_topk_pairs(p, ws, pp, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_topk_merge(const float* cand_scores, const int32_t* cand_pos, int T, int parts, int per_part,
+                          int64_t ld_cand, int64_t part_stride, int K, int32_t* idx, void* stream) {
+  if (T < 0 || parts < 1 || per_part < 0 || K < 1) return DSA_ERR_INVALID_ARG;
+  if (K > 4096 || (int64_t)parts * per_part > topk_merge_max_candidates()) return DSA_ERR_UNSUPPORTED;
+  if (T == 0) return DSA_OK;
+  if (!idx) return DSA_ERR_INVALID_ARG;
+  if (per_part > 0) {
+    if (!cand_scores || !cand_pos) return DSA_ERR_INVALID_ARG;
+    if ((T > 1 && ld_cand < per_part) || (parts > 1 && part_stride < per_part)) return DSA_ERR_INVALID_ARG;
+  }
+  dsa_status s = check_device();
+  if (s != DSA_OK) return s;
+  MergeParams p = {};
+  p.scores = cand_scores;
+  p.pos = cand_pos;
+  p.ld = ld_cand;
+  p.part_stride = part_stride;
+  p.T = T;
+  p.parts = parts;
+  p.per_part = per_part;
+  p.K = K;
+  p.idx = idx;
+  return from_cuda(launch_topk_merge(p, reinterpret_cast<cudaStream_t>(stream), false));
+}
+
+dsa_status dsa_sparse_attn_partial(const void* q, const void* kv, const void* kv_v, const float* kv_scale,
+                                   int64_t kv_row_stride, int64_t kv_seq_stride, int64_t v_row_stride,
+                                   int64_t v_seq_stride, const int32_t* idx, int T, int q_per_seq, int L,
+                                   int K, int H, int D_qk, int D_v, float sm_scale, dsa_dtype kv_dtype,
+                                   int pos_lo, float* o_part, float* lse_part, void* ws, size_t ws_bytes,
+                                   void* stream) {
+  dsa_status s = check_sparse_attn(q, kv, kv_v, kv_scale, kv_row_stride, kv_seq_stride, v_row_stride,
+                                   v_seq_stride, idx, T, q_per_seq, L, K, H, D_qk, D_v, kv_dtype, o_part);
+  if (s != DSA_OK || T == 0) return s;
+  if (pos_lo < 0 || !lse_part) return DSA_ERR_INVALID_ARG;
+  const size_t need = sparse_attn_ws_bytes(T, H, K, D_v);
+  if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws))) return DSA_ERR_WORKSPACE;
+  if ((s = check_device()) != DSA_OK) return s;
+  dsa_args a = {};
+  a.T = T;
+  a.q_per_seq = q_per_seq;
+  a.L = L;
+  a.K = K;
+  a.H = H;
+  a.D_qk = D_qk;
+  a.D_v = D_v;
+  a.sm_scale = sm_scale;
+  a.kv_dtype = kv_dtype;
+  a.q = q;
+  a.kv = kv;
+  a.kv_v = kv_v;
+  a.kv_scale = kv_scale;
+  a.kv_row_stride = kv_row_stride;
+  a.kv_seq_stride = kv_seq_stride;
+  a.v_row_stride = v_row_stride;
+  a.v_seq_stride = v_seq_stride;
+  a.out = o_part;
+  a.lse = lse_part;
+  return from_cuda(run_sparse_attn(a, 0, T, idx, ws, reinterpret_cast<cudaStream_t>(stream), false,
+                                   /*valid_prefix=*/false, pos_lo, o_part));
+}
+
+dsa_status dsa_attn_combine(const float* o_parts, const float* lse_parts, int G, int64_t o_part_stride,
+                            int64_t lse_part_stride, int T, int H, int D_v, void* out, float* lse,
+                            void* stream) {
+  if (G < 1 || T < 0 || H < 1 || D_v < 4 || D_v % 4 != 0) return DSA_ERR_INVALID_ARG;
+  if (T == 0) return DSA_OK;
+  if (!o_parts || !lse_parts || !out || !aligned16(o_parts) || !aligned16(out)) return DSA_ERR_INVALID_ARG;
+  const int64_t rows = (int64_t)T * H;
+  if (G > 1 && (o_part_stride < rows * D_v || o_part_stride % 4 != 0 || lse_part_stride < rows))
+    return DSA_ERR_INVALID_ARG;
+  dsa_status s = check_device();
+  if (s != DSA_OK) return s;
+  SliceCombineParams p = {};
+  p.o_parts = o_parts;
+  p.lse_parts = lse_parts;
+  p.o_stride = o_part_stride;
+  p.lse_stride = lse_part_stride;
+  p.G = G;
+  p.T = T;
+  p.H = H;
+  p.D_v = D_v;
+  p.out = reinterpret_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  return from_cuda(launch_slice_combine(p, reinterpret_cast<cudaStream_t>(stream), false));
 }
 
 size_t dsa_sparse_attn_workspace_size(int T, int H, int K, int D_v) {

@@ -85,6 +85,7 @@ struct TopkParams {
   int64_t ld_scores;
   const int32_t* n_valid;
   int32_t* idx;
+  int64_t idx_ld;          // elements between index rows (0: K)
   int T, q_per_seq, q_pos0, L, K;
   int t_off;               // global index of local query 0
   int* err;                // device error word
@@ -110,6 +111,28 @@ cudaError_t launch_topk(const TopkParams& p, void* ws, cudaStream_t stream, bool
 size_t topk_cluster_ws_bytes(int T, int L);
 int topk_launches(int T, int L, bool hist_supplied);
 size_t topk_ws_bytes(int T, int L, int K);
+
+// Context split over slices: a slice's Top-K as (score, global position) pairs, and the merge of
+// the pairs of all slices into the global Top-K.
+struct PairsParams {
+  const float* scores;     // the slice's scores [T][ld_scores]
+  int64_t ld_scores;
+  int32_t* cand_pos;       // [T][ld_cand]: local positions from the slice's Top-K -> global
+  float* cand_scores;      // [T][ld_cand]
+  int64_t ld_cand;
+  int T, K, pos_offset;
+};
+struct MergeParams {
+  const float* scores;     // candidate j = g * per_part + k of query t at g * part_stride + t * ld + k
+  const int32_t* pos;      // same layout; < 0: no candidate
+  int64_t ld, part_stride; // in elements
+  int T, parts, per_part, K;
+  int32_t* idx;            // [T][K]
+};
+// p.idx = cand_pos with p.idx_ld = ld_cand; the Top-K, then the pairs kernel (PDL)
+cudaError_t launch_topk_pairs(const TopkParams& p, void* ws, const PairsParams& pp, cudaStream_t stream);
+cudaError_t launch_topk_merge(const MergeParams& p, cudaStream_t stream, bool pdl);
+int topk_merge_max_candidates();
 
 // ---------------------------------------------------------------------------------------------
 // step 3: sparse attention
@@ -137,7 +160,24 @@ struct SparseAttnParams {
   int q_pos0;
   const int32_t* n_valid;
   PagedCache pages;        // kv / kv_v / kv_scale pools (table null: contiguous per sequence)
+  // Context slice (slice_rows): the cache holds positions [pos_lo, pos_lo + L) of a longer
+  // context; index entries outside that range belong to other slices and are skipped without an
+  // error, the others address row idx - pos_lo.
+  bool slice_rows;
+  int pos_lo;
+  float* out_f32;          // when set: fp32 [T, H, D_v] output instead of the bf16 `out`
 };
+
+// Combine of G context slices' partial outputs (o_g normalised fp32, lse_g natural log).
+struct SliceCombineParams {
+  const float* o_parts;    // part g at o_parts + g * o_stride: [T, H, D_v]
+  const float* lse_parts;  // part g at lse_parts + g * lse_stride: [T, H]
+  int64_t o_stride, lse_stride;  // in elements
+  int G, T, H, D_v;
+  __nv_bfloat16* out;      // [T, H, D_v]
+  float* lse;              // [T, H] or null
+};
+cudaError_t launch_slice_combine(const SliceCombineParams& p, cudaStream_t stream, bool pdl);
 
 int sparse_attn_splits(int T, int H, int K);
 size_t sparse_attn_ws_bytes(int T, int H, int K, int D_v);

@@ -174,7 +174,10 @@ sparse_attn_kernel(const SparseAttnParams p) {
     int i = -1;
     if (j < nrows) {
       i = p.idx[(int64_t)t * p.K + row_begin + j];
-      if (i < -1 || i >= p.L) {
+      if (p.slice_rows) {  // rows of other slices of the context: not this CTA's to attend
+        i -= p.pos_lo;
+        if (i < 0 || i >= p.L) i = -1;
+      } else if (i < -1 || i >= p.L) {
         record_error(p.err, DSA_DEVERR_INDEX_RANGE);
         i = -1;
       }
@@ -505,10 +508,17 @@ sparse_attn_kernel(const SparseAttnParams p) {
     if (h >= p.H) continue;
     if (p.splits == 1) {
       const float inv = l_run[hh] > 0.f ? 1.f / l_run[hh] : 0.f;
-      __nv_bfloat16* o = p.out + ((int64_t)t * p.H + h) * DV;
+      if (p.out_f32) {
+        float* o = p.out_f32 + ((int64_t)t * p.H + h) * DV;
 #pragma unroll
-      for (int i = 0; i < NT; ++i)
-        *reinterpret_cast<uint32_t*>(o + col0 + i * 8) = pack_bf16(acc[i][2 * hh] * inv, acc[i][2 * hh + 1] * inv);
+        for (int i = 0; i < NT; ++i)
+          *reinterpret_cast<float2*>(o + col0 + i * 8) = make_float2(acc[i][2 * hh] * inv, acc[i][2 * hh + 1] * inv);
+      } else {
+        __nv_bfloat16* o = p.out + ((int64_t)t * p.H + h) * DV;
+#pragma unroll
+        for (int i = 0; i < NT; ++i)
+          *reinterpret_cast<uint32_t*>(o + col0 + i * 8) = pack_bf16(acc[i][2 * hh] * inv, acc[i][2 * hh + 1] * inv);
+      }
       if (p.lse && (lane & 3) == 0 && gw == 0)
         p.lse[(int64_t)t * p.H + h] = l_run[hh] > 0.f ? (m_run[hh] + log2f(l_run[hh])) * kLn2 : -INFINITY;
     } else {
@@ -567,8 +577,13 @@ __global__ void __launch_bounds__(DV / 4) lse_combine_kernel(const SparseAttnPar
     M = Mb;
   }
   const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-  __nv_bfloat16* out = p.out + ((int64_t)t * p.H + h) * DV + c;
-  *reinterpret_cast<uint2*>(out) = make_uint2(pack_bf16(o.x * inv, o.y * inv), pack_bf16(o.z * inv, o.w * inv));
+  if (p.out_f32) {
+    *reinterpret_cast<float4*>(p.out_f32 + ((int64_t)t * p.H + h) * DV + c) =
+        make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+  } else {
+    __nv_bfloat16* out = p.out + ((int64_t)t * p.H + h) * DV + c;
+    *reinterpret_cast<uint2*>(out) = make_uint2(pack_bf16(o.x * inv, o.y * inv), pack_bf16(o.z * inv, o.w * inv));
+  }
   if (p.lse && threadIdx.x == 0)
     p.lse[(int64_t)t * p.H + h] = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
 }
@@ -586,7 +601,46 @@ cudaError_t launch_variant(const SparseAttnParams& p, cudaStream_t stream, bool 
   return launch_kernel(lse_combine_kernel<DV>, dim3(p.T, p.H), dim3(DV / 4), 0, stream, true, p);
 }
 
+// ---------------------------------------------------------------------------------------------
+// Merge of the partial outputs of G context slices: slice g attended over the selected positions
+// it holds and gave o_g (normalised over its own rows) and lse_g (natural log; -inf when it held
+// none).  With M = max_g lse_g:  out = sum_g e^(lse_g - M) o_g / sum_g e^(lse_g - M) and
+// lse = M + ln sum_g e^(lse_g - M).  One CTA per (query, head), four value columns per thread.
+__global__ void __launch_bounds__(128) slice_combine_kernel(const SliceCombineParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int t = blockIdx.x, h = blockIdx.y;
+  const int64_t row = (int64_t)t * p.H + h;
+  float M = -INFINITY;
+  for (int g = 0; g < p.G; ++g) M = fmaxf(M, p.lse_parts[g * p.lse_stride + row]);
+  const float Mu = (M == -INFINITY) ? 0.f : M;
+  float wsum = 0.f;
+  for (int g = 0; g < p.G; ++g) wsum += expf(p.lse_parts[g * p.lse_stride + row] - Mu);
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  for (int c = 4 * threadIdx.x; c < p.D_v; c += 4 * blockDim.x) {
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int g = 0; g < p.G; ++g) {
+      const float lg = p.lse_parts[g * p.lse_stride + row];
+      if (lg == -INFINITY) continue;  // a slice with no selected row contributes nothing
+      const float wg = expf(lg - Mu);
+      const float4 v = *reinterpret_cast<const float4*>(p.o_parts + g * p.o_stride + row * p.D_v + c);
+      o.x = fmaf(wg, v.x, o.x);
+      o.y = fmaf(wg, v.y, o.y);
+      o.z = fmaf(wg, v.z, o.z);
+      o.w = fmaf(wg, v.w, o.w);
+    }
+    __nv_bfloat16* out = p.out + row * p.D_v + c;
+    *reinterpret_cast<uint2*>(out) = make_uint2(pack_bf16(o.x * inv, o.y * inv), pack_bf16(o.z * inv, o.w * inv));
+  }
+  if (p.lse && threadIdx.x == 0) p.lse[row] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+}
+
 }  // namespace
+
+cudaError_t launch_slice_combine(const SliceCombineParams& p, cudaStream_t stream, bool pdl) {
+  if (p.T <= 0 || p.H <= 0) return cudaSuccess;
+  return launch_kernel(slice_combine_kernel, dim3(p.T, p.H), dim3(128), 0, stream, pdl, p);
+}
 
 int sparse_attn_splits(int T, int H, int K) {
   // About one CTA per two SMs of a 152-SM part.  A CTA's time is mostly the gather's round trips

@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkParams
   pdl_wait();
   const int n = visible_len(t + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid);
   const float* scr = p.scores + (int64_t)t * p.ld_scores;
-  int32_t* out = p.idx + (int64_t)t * p.K;
+  int32_t* out = p.idx + (int64_t)t * p.idx_ld;
   uint32_t* ws = p.work + (int64_t)t * ws_words(C);
   uint32_t* gh0 = p.hist ? p.hist + (int64_t)t * kHistBins : ws + kWsGh0;
   uint32_t* gh1 = ws + kWsGh1;
@@ -865,7 +865,7 @@ __global__ void __launch_bounds__(kThreads) topk_wide_emit_kernel(const TopkPara
   const int c = blockIdx.x, t = blockIdx.y, tid = threadIdx.x;
   pdl_wait();
   const int n = visible_len(t + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid);
-  int32_t* out = p.idx + (int64_t)t * p.K;
+  int32_t* out = p.idx + (int64_t)t * p.idx_ld;
   const int64_t seq = (t + p.t_off) / p.q_per_seq;
   const bool paged = p.pages.table != nullptr;
   const uint8_t* pf_kv = p.kv ? p.kv + (paged ? 0 : seq * p.kv_seq_stride) : nullptr;
@@ -1056,6 +1056,7 @@ cudaError_t launch_topk(const TopkParams& p, void* ws, cudaStream_t stream, bool
   if (p.K > kMaxK) return cudaErrorNotSupported;
   TopkParams q = p;
   q.work = reinterpret_cast<uint32_t*>(ws);
+  if (q.idx_ld <= 0) q.idx_ld = q.K;
   const WidePlan w = wide_plan(p.T, p.L);
   if (allow_wide && w.use) return launch_wide(q, w, stream, pdl);
   auto kern = topk_cluster_kernel;
@@ -1083,6 +1084,159 @@ cudaError_t launch_topk(const TopkParams& p, void* ws, cudaStream_t stream, bool
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, q);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Context split over G slices (a query's positions cut into G ranges, e.g. one per GPU).  Every
+// position of the global Top-K is among the Top-K of its own slice, so the global selection is the
+// Top-K of the union of the slices' selections, taken in the same order (score descending, exact
+// ties toward the lower position).  Each slice turns its selection into (score, position) pairs
+// (topk_pairs_kernel), the pairs of all slices are put side by side, and topk_merge_kernel selects
+// K of them.
+
+namespace {
+
+constexpr int kMergePer = 16;                    // candidates per thread
+constexpr int kMergeMax = kThreads * kMergePer;  // candidates per query
+
+// After the slice's Top-K wrote local positions into cand_pos: the score of each selected position
+// into cand_scores, and the position moved by the slice's first position (-1 entries stay -1).
+__global__ void __launch_bounds__(256) topk_pairs_kernel(const PairsParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int t = blockIdx.y;
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= p.K) return;
+  int32_t* cp = p.cand_pos + (int64_t)t * p.ld_cand + j;
+  const int32_t pos = *cp;
+  float s = 0.f;
+  if (pos >= 0) {
+    s = p.scores[(int64_t)t * p.ld_scores + pos];
+    *cp = pos + p.pos_offset;
+  }
+  p.cand_scores[(int64_t)t * p.ld_cand + j] = s;
+}
+
+// The key T and the count `take` with (entries above T) + take = kr, over the entries of this
+// thread marked in `mask` (all threads together hold at least kr of them).  Radix levels of 12, 10
+// and 10 bits with shared-memory histograms.
+__device__ uint32_t merge_threshold(const uint32_t (&k)[kMergePer], uint32_t mask, uint32_t kr,
+                                    uint32_t* hist, uint32_t* sc, uint32_t* take) {
+  for (int b = threadIdx.x; b < kHistBins; b += kThreads) hist[b] = 0;
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < kMergePer; ++i)
+    if ((mask >> i) & 1u) atomicAdd(&hist[k[i] >> 20], 1u);
+  __syncthreads();
+  uint32_t c0[kBins0];
+#pragma unroll
+  for (int j = 0; j < kBins0; ++j) c0[j] = hist[kBins0 * threadIdx.x + j];
+  uint32_t above;
+  uint32_t prefix = find_digit<kBins0>(c0, kr, sc, &above);  // ends with a barrier: hist is free
+  kr -= above;
+#pragma unroll 1
+  for (int lv = 0; lv < 2; ++lv) {
+    const int shift = 10 - 10 * lv;  // the digit: bits 19..10, then 9..0
+    for (int b = threadIdx.x; b < kLevelBins; b += kThreads) hist[b] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kMergePer; ++i)
+      if (((mask >> i) & 1u) && (k[i] >> (shift + 10)) == prefix)
+        atomicAdd(&hist[(k[i] >> shift) & (kLevelBins - 1)], 1u);
+    __syncthreads();
+    uint32_t c1[kBins1];
+#pragma unroll
+    for (int j = 0; j < kBins1; ++j) c1[j] = hist[kBins1 * threadIdx.x + j];
+    const uint32_t d = find_digit<kBins1>(c1, kr, sc, &above);
+    kr -= above;
+    prefix = (prefix << 10) | d;
+  }
+  *take = kr;
+  return prefix;
+}
+
+// One CTA per query; thread i holds candidates [i * per, i * per + per) of the query's list.
+__global__ void __launch_bounds__(kThreads, 1) topk_merge_kernel(const MergeParams p) {
+  __shared__ uint32_t hist[kHistBins];
+  __shared__ uint32_t sc[256];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int t = blockIdx.x, tid = threadIdx.x;
+  const int n_cand = p.parts * p.per_part;
+  int32_t* out = p.idx + (int64_t)t * p.K;
+  const int per = (n_cand + kThreads - 1) / kThreads;
+  const int lo = tid * per;
+  // element offset of candidate j of this query
+  auto at = [&](int j) -> int64_t {
+    const int g = j / p.per_part;
+    return (int64_t)g * p.part_stride + (int64_t)t * p.ld + (j - g * p.per_part);
+  };
+  const float* s = p.scores;
+  const int32_t* ps = p.pos;
+  uint32_t k[kMergePer];
+  uint32_t valid = 0;
+#pragma unroll
+  for (int i = 0; i < kMergePer; ++i) {
+    k[i] = 0u;
+    const int j = lo + i;
+    if (i < per && j < n_cand && __ldg(ps + at(j)) >= 0) {
+      k[i] = float_key(__ldg(s + at(j)));
+      valid |= 1u << i;
+    }
+  }
+  uint64_t tot;
+  block_excl_scan((uint64_t)__popc(valid), sc, &tot);
+  uint32_t sel = valid;
+  if (tot > (uint64_t)p.K) {
+    uint32_t take;
+    const uint32_t T = merge_threshold(k, valid, (uint32_t)p.K, hist, sc, &take);
+    uint32_t gt = 0, eq = 0;
+#pragma unroll
+    for (int i = 0; i < kMergePer; ++i) {
+      const bool v = (valid >> i) & 1u;
+      gt |= (uint32_t)(v && k[i] > T) << i;
+      eq |= (uint32_t)(v && k[i] == T) << i;
+    }
+    block_excl_scan((uint64_t)__popc(eq), sc, &tot);
+    sel = gt;
+    if ((uint64_t)take == tot) {
+      sel |= eq;
+    } else {
+      // the `take` lowest positions among the entries equal to T: the take largest of ~position
+#pragma unroll
+      for (int i = 0; i < kMergePer; ++i) k[i] = ((eq >> i) & 1u) ? ~(uint32_t)__ldg(ps + at(lo + i)) : 0u;
+      uint32_t take2;
+      const uint32_t P = merge_threshold(k, eq, take, hist, sc, &take2);
+#pragma unroll
+      for (int i = 0; i < kMergePer; ++i) sel |= (uint32_t)(((eq >> i) & 1u) && k[i] >= P) << i;
+    }
+  }
+  // kept candidates in list order, then -1
+  const uint32_t ex = (uint32_t)block_excl_scan((uint64_t)__popc(sel), sc, &tot);
+  uint32_t slot = ex;
+#pragma unroll
+  for (int i = 0; i < kMergePer; ++i)
+    if ((sel >> i) & 1u) {
+      if (slot < (uint32_t)p.K) out[slot] = __ldg(ps + at(lo + i));  // (duplicate positions: extra dropped)
+      ++slot;
+    }
+  for (int j = (int)min(tot, (uint64_t)p.K) + tid; j < p.K; j += kThreads) out[j] = -1;
+}
+
+}  // namespace
+
+int topk_merge_max_candidates() { return kMergeMax; }
+
+cudaError_t launch_topk_pairs(const TopkParams& p, void* ws, const PairsParams& pp, cudaStream_t stream) {
+  cudaError_t e = launch_topk(p, ws, stream, false);
+  if (e != cudaSuccess || p.T <= 0) return e;
+  return launch_kernel(topk_pairs_kernel, dim3((pp.K + 255) / 256, pp.T), dim3(256), 0, stream, true, pp);
+}
+
+cudaError_t launch_topk_merge(const MergeParams& p, cudaStream_t stream, bool pdl) {
+  if (p.T <= 0) return cudaSuccess;
+  if ((int64_t)p.parts * p.per_part > kMergeMax || p.K > kMaxK) return cudaErrorNotSupported;
+  return launch_kernel(topk_merge_kernel, dim3(p.T), dim3(kThreads), 0, stream, pdl, p);
 }
 
 // ---------------------------------------------------------------------------------------------
