@@ -147,7 +147,8 @@ PagedCache pages_of(const dsa_args& a) {
 }
 
 cudaError_t run_index_score(const dsa_args& a, int t_off, int T, float* scores, int64_t ld,
-                            uint32_t* hist, bool* hist_filled, cudaStream_t st, bool pdl) {
+                            uint32_t* hist, bool* hist_filled, cudaStream_t st, bool pdl,
+                            bool share_sms = false) {
   const int64_t row_bytes = (int64_t)a.d_idx * (a.idx_dtype == DSA_BF16 ? 2 : 1);
   IndexScoreParams p = {};
   p.w = a.w + (int64_t)t_off * a.H_idx;
@@ -167,6 +168,7 @@ cudaError_t run_index_score(const dsa_args& a, int t_off, int T, float* scores, 
   p.err = device_error_ptr();
   p.hist = hist;
   p.pages = pages_of(a);
+  p.share_sms = share_sms;
   const uint8_t* qi = reinterpret_cast<const uint8_t*>(a.q_idx) + (int64_t)t_off * a.H_idx * row_bytes;
   return launch_index_score(qi, a.k_idx, a.k_seq_stride, a.T / a.q_per_seq, a.d_idx,
                             a.idx_dtype == DSA_MXFP8_E4M3, p, st, pdl, hist_filled);
@@ -323,7 +325,7 @@ dsa_status run_chain(const dsa_args* a, void* ws, size_t ws_bytes, void* stream,
     bool filled = false;
     // every launch may overlap its predecessor's tail (programmatic dependent launch); each
     // kernel waits for its predecessor before reading anything that predecessor could write
-    if (a->L > 0) e = run_index_score(*a, t0, tn, scores, ld, hist, &filled, st, true);
+    if (a->L > 0) e = run_index_score(*a, t0, tn, scores, ld, hist, &filled, st, true, /*share_sms=*/true);
     if (e == cudaSuccess)
       e = run_topk(*a, t0, tn, scores, ld, idx_slice, filled ? hist : nullptr, base + l.topk, st, true);
     if (e == cudaSuccess)

@@ -63,6 +63,7 @@ struct IndexScoreParams {
   uint32_t* hist;          // [T][4096] histograms of the top 12 key bits of the scores (added
                            // to; zero on entry), or null
   PagedCache pages;        // k_idx / k_sf pools (table null: contiguous per sequence)
+  bool share_sms;          // fused chain: a short launch leaves half the resident slots free
 };
 
 constexpr int kHistBins = 4096;

@@ -594,7 +594,15 @@ cudaError_t launch_cfg(const void* q_idx, const void* k_idx, int64_t k_seq_strid
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t units = (int64_t)((p.T + G - 1) / G) * p.tiles;
   if (units >= (1ll << 31)) return cudaErrorNotSupported;
-  const int64_t slots = (int64_t)sms * C::CTAS_PER_SM;
+  // In the fused chain a short launch (fewer than 16 units per resident slot: a decode batch of
+  // tens of thousands of positions per query) runs one CTA per SM, so half the slots stay free for
+  // the Top-K and attention CTAs of other batches in flight: decode B = 8, L = 32K with six batches
+  // in flight, 19.97 -> 18.63 us per step (bf16) and 20.47 -> 18.04 us (MXFP8), at 2-3 us more for
+  // one batch alone (grids of 3/4 and 2/3 of the slots fell in between).  Long launches (one query
+  // over a million positions) need both CTAs of every SM to reach the memory bandwidth, and a
+  // launch on its own (dsa_index_score) takes every slot.
+  int64_t slots = (int64_t)sms * C::CTAS_PER_SM;
+  if (p.share_sms && C::CTAS_PER_SM == 2 && units < 16 * slots) slots = sms;
   const int grid = (int)(units < slots ? units : slots);
   if (grid <= 0) return cudaSuccess;
   return launch_kernel(kern, dim3(grid), dim3(C::THREADS), C::SMEM, stream, pdl, tm, tq,

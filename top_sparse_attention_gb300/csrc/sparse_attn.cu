@@ -29,6 +29,9 @@ namespace dsa {
 namespace {
 
 constexpr int kHeads = 16;    // heads per CTA (M of m16n8k16)
+#ifndef DSA_ATTN_CTA_TARGET
+#define DSA_ATTN_CTA_TARGET 76  // attention CTAs aimed for when K is split (about one per two SMs)
+#endif
 constexpr int kRows = 64;     // gathered rows per block
 constexpr int kMaxRows = 4096;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -651,7 +654,7 @@ int sparse_attn_splits(int T, int H, int K) {
   const int blocks = (K + kRows - 1) / kRows;
   const int ctas_per_split = T * ((H + kHeads - 1) / kHeads);
   if (ctas_per_split <= 0) return 1;
-  int s = (76 + ctas_per_split - 1) / ctas_per_split;
+  int s = (DSA_ATTN_CTA_TARGET + ctas_per_split - 1) / ctas_per_split;
   s = s < 1 ? 1 : (s > 64 ? 64 : s);
   if (s > blocks) s = blocks;
   // whole blocks per split, and no empty split
