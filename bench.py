@@ -487,6 +487,8 @@ def run_ours(args, wl):
             "hbm_frac_of_measured": chain_gbs / peak,
             "roofline": roofline,
             "kernels_us": kern,
+            "kernels_note": "each component entry timed alone (CUDA graph of launches, rotating input sets); "
+                            "the index score on every resident slot, as dsa_index_score runs it",
             "next_rows": ({"quant_append": quant_append_time(dsa, wl, stream),
                            "paged_chain": paged_chain_time(dsa, wl, dev_sets, stream)} if wl.q_pos0 < 0 else {}),
             "serial": serial,
@@ -508,7 +510,10 @@ def kernel_times(dsa, wl, dev_sets, stream, reps):
     """Average device time of each step's kernel(s), launched alone through the component entry
     points on the same inputs, rotating over the input sets (so the keys come from DRAM).  Each
     component's `reps` launches are captured in one CUDA graph and timed with CUDA events on the
-    launching stream around its replay, so the figure is device time without host launch gaps."""
+    launching stream around its replay, so the figure is device time without host launch gaps.
+    The index score runs here as dsa_index_score does, on every resident slot; inside the fused
+    chain a short decode launch takes one CTA per SM (see index_score.cu), which is slower alone
+    and faster with batches in flight."""
     n = len(dev_sets)
     L = wl.L
     dev = dev_sets[0]["q"].device

@@ -35,7 +35,10 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 1024;
+#ifndef DSA_TOPK_THREADS
+#define DSA_TOPK_THREADS 1024
+#endif
+constexpr int kThreads = DSA_TOPK_THREADS;
 constexpr int kWarps = kThreads / 32;
 constexpr int kChunk = 4 * kThreads;  // keys per block-wide step
 constexpr int kCachedKeys = 16384;    // largest slice kept in shared memory
@@ -43,7 +46,10 @@ constexpr int kCachedKeys = 16384;    // largest slice kept in shared memory
 // cluster of fewer, fuller CTAs costs less SM time; with independent batches in flight the
 // freed SMs run other batches' kernels (decode B = 8, L = 32K: 4-CTA clusters gave 8 % more
 // queries/s than 8-CTA ones, at 4 % more latency for one batch alone).
-constexpr int kKeysPerCta = 8192;
+#ifndef DSA_TOPK_KEYS_PER_CTA
+#define DSA_TOPK_KEYS_PER_CTA 8192
+#endif
+constexpr int kKeysPerCta = DSA_TOPK_KEYS_PER_CTA;
 constexpr int kCand = 4096;           // own candidate list capacity (shared memory)
 constexpr int kRegion = kThreads;     // workspace list entries per CTA (one per thread)
 constexpr int kMaxK = 4096;
