@@ -642,7 +642,8 @@ dsa_status dsa_launch_count(const dsa_args* a, int prefill, int* launches) {
     const bool filled =
         a->L > 0 && index_score_builds_hist(tn, a->H_idx, a->q_per_seq, a->idx_dtype == DSA_MXFP8_E4M3);
     n += (a->L > 0 ? 1 : 0) + topk_launches(tn, a->L, filled) +
-         (sparse_attn_splits(tn, a->H, a->K) > 1 ? 2 : 1);
+         sparse_attn_launches(tn, a->H, a->K, a->D_qk, a->D_v, a->kv_dtype != DSA_BF16, a->kv_v != nullptr,
+                              a->kv_dtype == DSA_FP8_E4M3_T128, /*chain=*/true);
   }
   *launches = n;
   return DSA_OK;

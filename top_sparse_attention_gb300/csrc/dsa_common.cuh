@@ -311,6 +311,20 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand in 128-byte swizzle atoms: within an atom
+// 64 consecutive 16-bit elements of the M (or N) dimension fill a 128-byte row and 8 such rows,
+// 128 bytes apart, are 8 consecutive K indices; atoms follow each other `mn_stride` bytes apart
+// along M/N (leading byte offset) and `k_stride` bytes apart per 8 K indices (stride byte offset).
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t saddr, uint32_t mn_stride, uint32_t k_stride) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);          // start address
+  d |= (uint64_t)((mn_stride >> 4) & 0x3FFFu) << 16;  // leading byte offset: next atom along M/N
+  d |= (uint64_t)((k_stride >> 4) & 0x3FFFu) << 32;   // stride byte offset: next 8 K indices
+  d |= (uint64_t)1u << 46;                            // descriptor version for tcgen05
+  d |= (uint64_t)2u << 61;                            // 128-byte swizzle
+  return d;
+}
+
 // Instruction descriptor: dense, D = f32, K-major A and B, shape M x N.
 // a_fmt/b_fmt: kind::f16 -> 1 = bf16;  kind::f8f6f4 -> 0 = E4M3.
 __host__ __device__ constexpr uint32_t make_idesc(uint32_t a_fmt, uint32_t b_fmt, int M, int N) {

@@ -157,6 +157,7 @@ struct SparseAttnParams {
   int* err;                // device error word
   // Set by the fused chain, whose index rows hold the min(K, n_t) selected positions first and
   // -1 after them: a split then stops at the query's last valid row (q_pos0 / n_valid give n_t).
+  // It also selects the chain's choice of attention kernel.
   bool valid_prefix;
   int q_pos0;
   const int32_t* n_valid;
@@ -181,6 +182,9 @@ struct SliceCombineParams {
 cudaError_t launch_slice_combine(const SliceCombineParams& p, cudaStream_t stream, bool pdl);
 
 int sparse_attn_splits(int T, int H, int K);
+// kernels one attention step launches (the attention, plus the combine when K is split over CTAs);
+// chain: inside the fused chain (whose index rows hold each query's valid positions first)
+int sparse_attn_launches(int T, int H, int K, int D_qk, int D_v, bool fp8, bool sepv, bool tiled, bool chain);
 size_t sparse_attn_ws_bytes(int T, int H, int K, int D_v);
 // tiled: FP8 rows with one scale per 128-element tile (kv_scale [rows][ceil(D_qk / 128)])
 cudaError_t launch_sparse_attn(SparseAttnParams p, int D_qk, int D_v, bool fp8, bool sepv,

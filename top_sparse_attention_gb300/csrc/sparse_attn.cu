@@ -22,6 +22,14 @@
 //
 // When K is split over S > 1 CTAs (so a small batch still covers every SM), each CTA writes its
 // partial (o, m, l) and a second kernel merges them with a log-sum-exp combine.
+//
+// The 576 / 512 latent row also has a kernel on the 5th-generation tensor cores
+// (sparse_attn_tc_kernel below: 128 rows per CTA gathered into a swizzled bf16 tile, the two
+// contractions as tcgen05.mma with accumulators in tensor memory).  A call on its own runs E4M3
+// rows there (faster alone); the fused chain keeps the kernel above, which costs less SM time when
+// several batches are in flight (see DSA_ATTN_TC_MASK).
+#include <algorithm>
+
 #include "dsa_internal.h"
 
 namespace dsa {
@@ -29,6 +37,20 @@ namespace dsa {
 namespace {
 
 constexpr int kHeads = 16;    // heads per CTA (M of m16n8k16)
+// Which 576 / 512 latent rows run on the tensor-memory kernel (bit 0 bf16, bit 1 E4M3 rows with row
+// scales, bit 2 E4M3 rows with tile scales), for a call on its own and inside the fused chain.
+// Measured on B = 8, K = 2048 (alone / one batch of the chain / six batches in flight):
+//   E4M3 rows: 15.9 us / 44.0 us / 22.0 us per step against 18.8 / 47.9 / 18.2 for the mma.sync
+//   kernel; bf16 rows: 15.6 / 44.3 / 23.7 against 13.6 / 43.7 / 18.8.  The tensor-memory kernel takes
+//   128 rows per CTA (twice the CTAs) at 182 KB of shared memory, so with batches in flight its
+//   CTAs wait for whole SMs; alone, its E4M3 rows cost one widening per element instead of
+//   selection MMAs on the legacy pipe.  The fused chain serves batches in flight.
+#ifndef DSA_ATTN_TC_MASK
+#define DSA_ATTN_TC_MASK 6
+#endif
+#ifndef DSA_ATTN_TC_MASK_CHAIN
+#define DSA_ATTN_TC_MASK_CHAIN 0
+#endif
 #ifndef DSA_ATTN_CTA_TARGET
 #define DSA_ATTN_CTA_TARGET 76  // attention CTAs aimed for when K is split (about one per two SMs)
 #endif
@@ -591,6 +613,355 @@ __global__ void __launch_bounds__(DV / 4) lse_combine_kernel(const SparseAttnPar
     p.lse[(int64_t)t * p.H + h] = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
 }
 
+// ---------------------------------------------------------------------------------------------
+// The 576 / 512 latent row on the 5th-generation tensor cores.  One CTA = 128 selected rows of one
+// query (the M = 128 side of tcgen05.mma) and 16 heads:
+//   * the rows are gathered into one 128-byte-swizzled, K-major bf16 tile (9 boxes of 64 columns):
+//     bf16 rows by 16-byte cp.async chunks placed at their swizzled addresses; E4M3 rows loaded 16
+//     codes at a time and widened exactly to bf16 in registers on the way;
+//   * S^T[128 rows x 16 heads] = K q^T: 36 MMAs (M = 128, N = 16, K = 16) into tensor memory
+//     (one accumulator per 128-element scale tile for tile-scaled FP8 rows);
+//   * four warps (one row per thread, the tensor-memory lane of that row) take the softmax of the
+//     tile: per-head maxima and sums over the 128 rows with warp butterflies and a 4-warp exchange,
+//     and write P^T (bf16, scaled per row or per value tile) as the K-major B operand;
+//   * O^T[512 values x 16 heads] = V^T P: the same tile read as an MN-major A operand (values along
+//     M, rows along K), 4 accumulators of 128 values x 8 K steps;
+//   * the four warps read O^T back (one value column per thread) and write this split's partial
+//     (o, m, l), merged over the splits by lse_combine_kernel (or the output when K <= 128).
+// No warp-level mma.sync: the E4M3 rows cost one ALU widening per element, not tensor-core work.
+constexpr int kTcRows = 128;
+
+template <bool FP8, bool TILED>
+struct TcCfg {
+  static constexpr int DQK = 576, DV = 512;
+  static constexpr int BOXES = DQK / 64;                 // 64 bf16 columns = one 128-byte atom row
+  static constexpr int NSC = TILED ? (DQK + 127) / 128 : (FP8 ? 1 : 0);
+  static constexpr int SACC = TILED ? NSC : 1;           // S accumulators (one per scale tile)
+  static constexpr int PCOPIES = TILED ? DV / 128 : 1;   // P per value tile
+  static constexpr int THREADS = 256;
+  static constexpr int TILE_BOX = kTcRows * 128;         // 16 KB per box of the row tile
+  static constexpr int Q_BOX = kHeads * 128;             // 2 KB per box of q
+  static constexpr int P_BYTES = 2 * Q_BOX;              // P^T: 16 heads x 128 rows bf16
+  static constexpr int OFF_TILE = 0;
+  static constexpr int OFF_Q = OFF_TILE + BOXES * TILE_BOX;
+  static constexpr int OFF_P = OFF_Q + BOXES * Q_BOX;
+  static constexpr int OFF_RED = OFF_P + PCOPIES * P_BYTES;  // [2][4 warps][16] fp32
+  static constexpr int OFF_IDX = OFF_RED + 2 * 4 * kHeads * 4;
+  static constexpr int OFF_SC = OFF_IDX + kTcRows * 4;
+  static constexpr int OFF_BAR = OFF_SC + kTcRows * 4 * (NSC > 0 ? NSC : 1);
+  static constexpr int SMEM = OFF_BAR + 64 + 1024;       // + alignment slack (1024-byte atoms)
+  static constexpr int TMEM_COLS = 256;                  // S at [0, 16 SACC), O^T at [128, 192)
+  static constexpr int O_COL = 128;
+  static_assert(16 * SACC <= O_COL, "S accumulators");
+};
+
+// Two E4M3 codes (the bytes of x picked by `sel` into bits 8..15 and 24..31) as two bf16, exactly.
+// The code s.eeee.mmm placed as the bf16 pattern s.0000eeee.mmm0000 has 2^-120 times the code's
+// value: for e >= 1 both read 2^(e - bias) (1 + m/8), with biases 127 and 7; for e = 0 both are
+// subnormal, m/8 x 2^-126 and m/8 x 2^-6.  Scaling by 2^120 is exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t x, uint32_t sel) {
+  const uint32_t t = __byte_perm(x, 0u, sel);
+  const uint32_t pat = (t & 0x80008000u) | ((t & 0x7F007F00u) >> 4);
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(pat), "r"(0x7B807B80u));  // x 2^120
+  return r;
+}
+
+// Butterfly over a warp: v[0..15] are this lane's values for heads 0..15; afterwards v[0] holds the
+// reduction over all 32 lanes of head (lane >> 1) & 15.
+template <bool MAX>
+__device__ __forceinline__ void warp_reduce16(float (&v)[16]) {
+  const int lane = threadIdx.x & 31;
+  auto op = [](float a, float b) { return MAX ? fmaxf(a, b) : a + b; };
+#pragma unroll
+  for (int n = 8; n >= 1; n >>= 1) {  // offsets 16, 8, 4, 2: halve the heads per lane
+    const int off = 2 * n;
+    const bool hi = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < n; ++i) {
+      const float keep = hi ? v[i + n] : v[i];
+      const float send = hi ? v[i] : v[i + n];
+      v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, off));
+    }
+  }
+  v[0] = op(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1));
+}
+
+template <bool FP8, bool TILED>
+__global__ void __launch_bounds__(256, 1) sparse_attn_tc_kernel(const SparseAttnParams p) {
+  using C = TcCfg<FP8, TILED>;
+  constexpr int DQK = C::DQK, DV = C::DV;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* tile = smem + C::OFF_TILE;
+  uint8_t* q_s = smem + C::OFF_Q;
+  uint8_t* p_s = smem + C::OFF_P;
+  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);  // [0]: max, [1]: sum; [warp][head]
+  int* idx_s = reinterpret_cast<int*>(smem + C::OFF_IDX);
+  float* scale_s = reinterpret_cast<float*>(smem + C::OFF_SC);  // [row][NSC]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);  // [0] S done, [1] O done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 2);
+  pdl_launch_dependents();
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int split = blockIdx.x, t = blockIdx.y, h0 = blockIdx.z * kHeads;
+  const int seq = (t + p.t_off) / p.q_per_seq;
+  const int row_begin = split * kTcRows;
+  const int k_rows = p.valid_prefix
+                         ? min(p.K, visible_len(t + p.t_off, p.L, p.q_per_seq, p.q_pos0, p.n_valid))
+                         : p.K;
+  const int nrows = max(0, min(kTcRows, k_rows - row_begin));
+  const bool paged = p.pages.table != nullptr;
+  const uint8_t* kv_base = p.kv + (paged ? 0 : (int64_t)seq * p.kv_seq_stride);
+  const float* scale_base = FP8 ? p.kv_scale + (paged ? 0 : (int64_t)seq * p.L * C::NSC) : nullptr;
+
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_mbar_init();
+  }
+  // q rows h0 .. h0+15 (a caller input, so read before waiting for the previous kernel) into the
+  // swizzled K-major B layout; rows past H are zero
+  for (int i = tid; i < kHeads * (DQK / 8); i += C::THREADS) {
+    const int h = i / (DQK / 8), c = i - h * (DQK / 8);
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (h0 + h < p.H) v = *reinterpret_cast<const uint4*>(p.q + ((int64_t)t * p.H + h0 + h) * DQK + 8 * c);
+    *reinterpret_cast<uint4*>(q_s + (c >> 3) * C::Q_BOX + h * 128 + (((c & 7) ^ (h & 7)) << 4)) = v;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the index rows come from the previous kernel in the stream
+
+  // ---- this CTA's index rows (checked against [-1, L), or taken from this slice of the context)
+  // and their scales
+  if (tid < kTcRows) {
+    int i = -1;
+    if (tid < nrows) {
+      i = p.idx[(int64_t)t * p.K + row_begin + tid];
+      if (p.slice_rows) {
+        i -= p.pos_lo;
+        if (i < 0 || i >= p.L) i = -1;
+      } else if (i < -1 || i >= p.L) {
+        record_error(p.err, DSA_DEVERR_INDEX_RANGE);
+        i = -1;
+      }
+      if (i >= 0 && paged) i = (int)page_row(p.pages, seq, i);
+    }
+    idx_s[tid] = i;
+    if constexpr (C::NSC > 0) {
+#pragma unroll
+      for (int c = 0; c < C::NSC; ++c) scale_s[tid * C::NSC + c] = i >= 0 ? scale_base[(int64_t)i * C::NSC + c] : 0.f;
+    }
+  }
+  __syncthreads();
+
+  // ---- gather the rows into the swizzled bf16 tile: element (r, col) at box col / 64, byte
+  // r * 128 + ((col % 64 / 8) ^ (r % 8)) * 16 + (col % 8) * 2
+  if constexpr (!FP8) {
+    for (int i = tid; i < kTcRows * (DQK / 8); i += C::THREADS) {
+      const int r = i / (DQK / 8), c = i - r * (DQK / 8);  // 16-byte chunk c of row r
+      const int row = idx_s[r];
+      uint8_t* dst = tile + (c >> 3) * C::TILE_BOX + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+      cp_async16(dst, kv_base + (int64_t)(row >= 0 ? row : 0) * p.kv_row_stride + 16 * c, row >= 0);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+  } else {
+    constexpr int CH = DQK / 16;  // 16-code chunks per row
+    constexpr int BATCH = 6;      // loads in flight per thread
+    constexpr int TOTAL = kTcRows * CH;
+    static_assert(TOTAL % (BATCH * C::THREADS) == 0, "whole batches");
+#pragma unroll 1
+    for (int i0 = tid; i0 < TOTAL; i0 += BATCH * C::THREADS) {
+      uint4 raw[BATCH];
+#pragma unroll
+      for (int b = 0; b < BATCH; ++b) {
+        const int i = i0 + b * C::THREADS;
+        const int r = i / CH, c = i - r * CH;
+        const int row = idx_s[r];
+        raw[b] = row >= 0 ? __ldg(reinterpret_cast<const uint4*>(kv_base + (int64_t)row * p.kv_row_stride + 16 * c))
+                          : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int b = 0; b < BATCH; ++b) {
+        const int i = i0 + b * C::THREADS;
+        const int r = i / CH, c = i - r * CH;  // codes 16c .. 16c + 15: bf16 chunks 2c and 2c + 1
+        const uint4 lo = make_uint4(e4m3x2_to_bf16x2(raw[b].x, 0x1404), e4m3x2_to_bf16x2(raw[b].x, 0x3424),
+                                    e4m3x2_to_bf16x2(raw[b].y, 0x1404), e4m3x2_to_bf16x2(raw[b].y, 0x3424));
+        const uint4 hi = make_uint4(e4m3x2_to_bf16x2(raw[b].z, 0x1404), e4m3x2_to_bf16x2(raw[b].z, 0x3424),
+                                    e4m3x2_to_bf16x2(raw[b].w, 0x1404), e4m3x2_to_bf16x2(raw[b].w, 0x3424));
+        const int c0 = 2 * c, c1 = 2 * c + 1;
+        *reinterpret_cast<uint4*>(tile + (c0 >> 3) * C::TILE_BOX + r * 128 + (((c0 & 7) ^ (r & 7)) << 4)) = lo;
+        *reinterpret_cast<uint4*>(tile + (c1 >> 3) * C::TILE_BOX + r * 128 + (((c1 & 7) ^ (r & 7)) << 4)) = hi;
+      }
+    }
+  }
+  fence_proxy_async_smem();  // the generic-proxy writes of tile and q are seen by the tensor cores
+  __syncthreads();
+
+  // ---- S^T = K q^T (one elected thread issues; completion arrives on bar[0])
+  if (warp == 0) {
+    tc_fence_after();
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc(1, 1, kTcRows, kHeads);
+      const uint32_t tb = smem_u32(tile), qb = smem_u32(q_s);
+#pragma unroll 1
+      for (int b = 0; b < C::BOXES; ++b) {
+        const int acc = TILED ? b / 2 : 0;  // 128-element scale tile of this box
+        const bool first = TILED ? (b % 2 == 0) : (b == 0);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_f16(tmem + 16 * acc, smem_desc_sw128(tb + b * C::TILE_BOX + 32 * k),
+                  smem_desc_sw128(qb + b * C::Q_BOX + 32 * k), idesc, (first && k == 0) ? 0u : 1u);
+      }
+      tc_commit(&bar[0]);
+    }
+    __syncwarp();
+  }
+
+  float m_fin = -INFINITY, l_fin = 0.f;  // head (tid & 15) of warp 0: this split's (m, l)
+  if (warp < 4) {
+    // ---- softmax over the tile's 128 rows: thread = row r = tensor-memory lane r
+    const int r = tid;
+    bool ok = mbar_wait(&bar[0], 0, p.err);
+    tc_fence_after();
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+    float x[16];
+    const bool valid = idx_s[r] >= 0;
+    if constexpr (TILED) {
+#pragma unroll
+      for (int h = 0; h < 16; ++h) x[h] = 0.f;
+#pragma unroll
+      for (int c = 0; c < C::SACC; ++c) {
+        float s[16];
+        tmem_ld_sync(lane_base + 16 * c, s);
+        const float sc = scale_s[r * C::NSC + c];
+#pragma unroll
+        for (int h = 0; h < 16; ++h) x[h] = fmaf(sc, s[h], x[h]);
+      }
+#pragma unroll
+      for (int h = 0; h < 16; ++h) x[h] = valid && ok ? x[h] * p.scale_log2 : -INFINITY;
+    } else {
+      tmem_ld_sync(lane_base, x);
+      const float f = p.scale_log2 * (FP8 ? scale_s[r] : 1.f);
+#pragma unroll
+      for (int h = 0; h < 16; ++h) x[h] = valid && ok ? x[h] * f : -INFINITY;
+    }
+    // per-head maxima over the 128 rows
+    float v[16];
+#pragma unroll
+    for (int h = 0; h < 16; ++h) v[h] = x[h];
+    warp_reduce16<true>(v);
+    if ((lane & 1) == 0) red[warp * kHeads + ((lane >> 1) & 15)] = v[0];
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    float mu[16];
+#pragma unroll
+    for (int h = 0; h < 16; ++h) {
+      const float m = fmaxf(fmaxf(red[h], red[kHeads + h]), fmaxf(red[2 * kHeads + h], red[3 * kHeads + h]));
+      mu[h] = m == -INFINITY ? 0.f : m;
+      x[h] = exp2f(x[h] - mu[h]);  // the probability of this row, unnormalised
+      v[h] = x[h];
+    }
+    if (lane < 16 && warp == 0) m_fin = fmaxf(fmaxf(red[lane], red[kHeads + lane]), fmaxf(red[2 * kHeads + lane], red[3 * kHeads + lane]));
+    warp_reduce16<false>(v);
+    if ((lane & 1) == 0) red[4 * kHeads + warp * kHeads + ((lane >> 1) & 15)] = v[0];
+    // P^T as the K-major B operand: element (head h, row r) at box r / 64, byte
+    // h * 128 + ((r % 64 / 8) ^ (h % 8)) * 16 + (r % 8) * 2; one copy per value tile when scaled by tile
+#pragma unroll
+    for (int pc = 0; pc < C::PCOPIES; ++pc) {
+      const float sc = TILED ? scale_s[r * C::NSC + pc] : (FP8 ? scale_s[r] : 1.f);  // V carries the row's scale
+      uint8_t* pb = p_s + pc * C::P_BYTES + (r >> 6) * C::Q_BOX + (r & 7) * 2;
+#pragma unroll
+      for (int h = 0; h < 16; ++h)
+        *reinterpret_cast<__nv_bfloat16*>(pb + h * 128 + ((((r & 63) >> 3) ^ (h & 7)) << 4)) = __float2bfloat16_rn(x[h] * sc);
+    }
+    fence_proxy_async_smem();
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (lane < 16 && warp == 0)
+      l_fin = red[4 * kHeads + lane] + red[5 * kHeads + lane] + red[6 * kHeads + lane] + red[7 * kHeads + lane];
+
+    // ---- O^T = V^T P: values along M (4 blocks of 128), rows along K (8 steps of 16)
+    if (warp == 0) {
+      tc_fence_after();
+      if (lane == 0 && ok) {
+        constexpr uint32_t idesc_pv = make_idesc(1, 1, kTcRows, kHeads) | (1u << 15);  // A MN-major
+        const uint32_t tb = smem_u32(tile), pbase = smem_u32(p_s);
+#pragma unroll 1
+        for (int j = 0; j < DV / 128; ++j) {
+          const uint32_t pj = pbase + (TILED ? j : 0) * C::P_BYTES;
+#pragma unroll
+          for (int ks = 0; ks < kTcRows / 16; ++ks)
+            mma_f16(tmem + C::O_COL + 16 * j, smem_desc_sw128_mn(tb + 2 * j * C::TILE_BOX + ks * 2048, C::TILE_BOX, 1024),
+                    smem_desc_sw128(pj + (ks >> 2) * C::Q_BOX + 32 * (ks & 3)), idesc_pv, ks > 0 ? 1u : 0u);
+        }
+      }
+      if (lane == 0) tc_commit(&bar[1]);  // (arrives at once when nothing was issued)
+      __syncwarp();
+    }
+    ok = mbar_wait(&bar[1], 0, p.err) && ok;
+    tc_fence_after();
+    // ---- this split's output: thread = value column 128 j + 32 warp + lane of every head
+    float inv[16];
+    if (p.splits == 1) {
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        const float l = red[4 * kHeads + h] + red[5 * kHeads + h] + red[6 * kHeads + h] + red[7 * kHeads + h];
+        inv[h] = l > 0.f ? 1.f / l : 0.f;
+      }
+    }
+#pragma unroll 1
+    for (int j = 0; j < DV / 128; ++j) {
+      float o[16];
+      tmem_ld_sync(lane_base + C::O_COL + 16 * j, o);
+      const int v = 128 * j + 32 * warp + lane;
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        if (h0 + h >= p.H) continue;
+        const int64_t hr = (int64_t)t * p.H + h0 + h;
+        const float oh = ok ? o[h] : 0.f;
+        if (p.splits == 1) {
+          if (p.out_f32) p.out_f32[hr * DV + v] = oh * inv[h];
+          else p.out[hr * DV + v] = __float2bfloat16_rn(oh * inv[h]);
+        } else {
+          p.part_o[(hr * p.splits + split) * DV + v] = oh;
+        }
+      }
+    }
+    if (warp == 0 && lane < 16 && h0 + lane < p.H) {
+      const int64_t hr = (int64_t)t * p.H + h0 + lane;
+      if (p.splits == 1) {
+        if (p.lse) p.lse[hr] = l_fin > 0.f ? (m_fin + log2f(l_fin)) * kLn2 : -INFINITY;
+      } else {
+        *reinterpret_cast<float2*>(p.part_ml + (hr * p.splits + split) * 2) = make_float2(m_fin, l_fin);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <bool FP8, bool TILED>
+cudaError_t launch_tc(const SparseAttnParams& p, cudaStream_t stream, bool pdl) {
+  using C = TcCfg<FP8, TILED>;
+  auto kern = sparse_attn_tc_kernel<FP8, TILED>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.splits, p.T, (p.H + kHeads - 1) / kHeads);
+  e = launch_kernel(kern, grid, dim3(C::THREADS), C::SMEM, stream, pdl, p);
+  if (e != cudaSuccess || p.splits == 1) return e;
+  return launch_kernel(lse_combine_kernel<512>, dim3(p.T, p.H), dim3(512 / 4), 0, stream, true, p);
+}
+
 template <int DQK, int DV, bool FP8, bool SEPV, bool TILED = false>
 cudaError_t launch_variant(const SparseAttnParams& p, cudaStream_t stream, bool pdl) {
   using C = Cfg<DQK, DV, FP8, SEPV, TILED>;
@@ -667,8 +1038,27 @@ static int rows_per_split(int K, int splits) {
   return ((blocks + splits - 1) / splits) * kRows;
 }
 
+// Which rows go to the tensor-memory kernel: the 576 / 512 latent row, per storage format (bit 0
+// bf16, bit 1 E4M3 with row scales, bit 2 E4M3 with 128-element tile scales).
+bool attn_uses_tc(int D_qk, int D_v, bool fp8, bool sepv, bool tiled, bool chain) {
+  if (D_qk != 576 || D_v != 512 || sepv) return false;
+  const int bit = tiled ? 4 : (fp8 ? 2 : 1);
+  return ((chain ? DSA_ATTN_TC_MASK_CHAIN : DSA_ATTN_TC_MASK) & bit) != 0;
+}
+
+static int routed_splits(int T, int H, int K, bool tc) {
+  return tc ? (K + kTcRows - 1) / kTcRows : sparse_attn_splits(T, H, K);
+}
+
+int sparse_attn_launches(int T, int H, int K, int D_qk, int D_v, bool fp8, bool sepv, bool tiled, bool chain) {
+  return routed_splits(T, H, K, attn_uses_tc(D_qk, D_v, fp8, sepv, tiled, chain)) > 1 ? 2 : 1;
+}
+
 size_t sparse_attn_ws_bytes(int T, int H, int K, int D_v) {
-  const int splits = sparse_attn_splits(T, H, K);
+  // sized for either kernel (the storage format is not an argument here)
+  int splits = sparse_attn_splits(T, H, K);
+  if (D_v == 512 && (DSA_ATTN_TC_MASK | DSA_ATTN_TC_MASK_CHAIN) != 0)
+    splits = std::max(splits, routed_splits(T, H, K, true));
   if (splits <= 1) return 0;
   const size_t rows = (size_t)T * H * splits;
   return align_up(rows * D_v * sizeof(float), 256) + align_up(rows * 2 * sizeof(float), 256);
@@ -676,14 +1066,19 @@ size_t sparse_attn_ws_bytes(int T, int H, int K, int D_v) {
 
 cudaError_t launch_sparse_attn(SparseAttnParams p, int D_qk, int D_v, bool fp8, bool sepv, void* ws,
                                cudaStream_t stream, bool pdl, bool tiled) {
-  p.splits = sparse_attn_splits(p.T, p.H, p.K);
-  p.rows_per_split = rows_per_split(p.K, p.splits);
+  const bool tc = attn_uses_tc(D_qk, D_v, fp8, sepv, tiled, p.valid_prefix);
+  p.splits = routed_splits(p.T, p.H, p.K, tc);
+  p.rows_per_split = tc ? kTcRows : rows_per_split(p.K, p.splits);
   if (p.rows_per_split > kMaxRows) return cudaErrorNotSupported;
   if (p.splits > 1) {
     if (!ws) return cudaErrorInvalidValue;
     const size_t rows = (size_t)p.T * p.H * p.splits;
     p.part_o = reinterpret_cast<float*>(ws);
     p.part_ml = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + align_up(rows * D_v * sizeof(float), 256));
+  }
+  if (tc) {
+    if (tiled) return launch_tc<true, true>(p, stream, pdl);
+    return fp8 ? launch_tc<true, false>(p, stream, pdl) : launch_tc<false, false>(p, stream, pdl);
   }
   if (tiled) {  // FP8 with one scale per 128-element tile: the 576/512 latent row only
     if (!fp8 || D_qk != 576 || D_v != 512 || sepv) return cudaErrorNotSupported;
