@@ -195,6 +195,17 @@ def test_topk_uncached_cluster_rows(dsa):
     _topk_case(dsa, s, 2048, 270001)
 
 
+def test_topk_many_queries(dsa):
+    # 64 or more queries in one launch take fewer, fuller CTAs per query: two CTAs of 35,001
+    # positions each (slices past the shared-memory key cache), and one CTA for a short row
+    rng = np.random.default_rng(26)
+    s = (rng.standard_normal((64, 70001)) * 30 + 140).astype(np.float32)
+    s[7] = np.round(s[7] / 8) * 8  # heavy ties in one row
+    _topk_case(dsa, s, 2048, 70001, n_valid=[70001 - 37 * t for t in range(64)])
+    s = (np.round(rng.standard_normal((80, 5000)) * 3) / 4).astype(np.float32)
+    _topk_case(dsa, s, 700, 5000)
+
+
 def test_topk_causal_rows(dsa):
     rng = np.random.default_rng(15)
     s = rng.standard_normal((6, 2600)).astype(np.float32)
