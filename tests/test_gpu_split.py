@@ -150,3 +150,35 @@ def test_split_decode_matches_the_fused_chain_and_the_oracle(dsa, name, G):
         assert err <= ATTN_GUARD[wl.kv_dtype], f"t={t}: max-abs {err}"
         fin = np.isfinite(ref_lse)
         assert np.all(np.abs(lse[t][fin] - ref_lse[fin]) <= LSE_TOL)
+
+
+# ------------------------------------------------------------------------------------------------
+# context-parallel prefill: the zigzag segments of the 4096-query chunk, run one after another on
+# this device as G ranks would run them, against the single fused prefill call
+
+
+@pytest.mark.parametrize("G", [2, 4])
+def test_zigzag_prefill_segments_match_the_whole_chunk(dsa, G):
+    from top_sparse_attention_gb300 import split
+
+    wl = synth.WORKLOADS["prefill_t4096_l128k_bf16"]
+    cpu = synth.make_inputs(wl)
+    dev = to_device(cpu)
+    whole = dsa.call_from_tensors(dev, K=wl.K, sm_scale=wl.sm_scale, q_per_seq=wl.q_per_seq, q_pos0=wl.q_pos0)
+    w_out, w_lse, w_idx = [x.clone() for x in whole()]
+    del whole
+    out = torch.empty_like(w_out)
+    lse = torch.empty_like(w_lse)
+    idx = torch.empty_like(w_idx)
+    for g in range(G):
+        for a, b in split.zigzag_segments(wl.T, G, g):
+            o, l, i = split.prefill_segment(dev, a, b, K=wl.K, sm_scale=wl.sm_scale, q_pos0=wl.q_pos0)
+            out[a:b], lse[a:b], idx[a:b] = o, l, i
+    torch.cuda.synchronize()
+    assert torch.equal(idx, w_idx)  # a query's scores do not depend on the other queries of its launch
+    assert float((out.float() - w_out.float()).abs().max()) <= ATTN_GUARD["bf16"]
+    assert float((lse - w_lse).abs().max()) <= LSE_TOL
+    ch, _ = oracle_chain(wl, cpu)
+    for t in (0, 1023, 1024, 2047, 3000, 4095):
+        ref, _ = ch.attention(t, idx[t].cpu().numpy(), wl.D_v)
+        assert np.max(np.abs(out[t].float().cpu().numpy() - ref)) <= ATTN_GUARD["bf16"]

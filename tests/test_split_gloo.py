@@ -123,3 +123,71 @@ def test_split_decode_ranks_exchange_candidates_and_partials(world, case):
         ref, ref_lse = ch.attention(t, idx[t], wl.D_v)
         np.testing.assert_allclose(res[t], ref, rtol=0, atol=1e-6)   # fp32 partials exchanged
         np.testing.assert_allclose(lse[t], ref_lse, rtol=0, atol=1e-5)
+
+
+# ------------------------------------------------------------------------------------------------
+# context-parallel prefill with zigzag segments
+
+
+def test_zigzag_segments_balance_the_causal_work():
+    from top_sparse_attention_gb300 import split
+
+    for G in (1, 2, 4, 8):
+        segs = [split.zigzag_segments(4096, G, g) for g in range(G)]
+        covered = sorted(x for s in segs for a, b in s for x in range(a, b))
+        assert covered == list(range(4096))  # every query exactly once
+        work = [split.zigzag_work(4096, G, g, 126976) for g in range(G)]
+        assert max(work) == min(work)
+    with pytest.raises(ValueError):
+        split.zigzag_segments(100, 3, 0)
+
+
+def _prefill_rank_main(rank, world, port, out):
+    import sys
+
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import oracle
+    import synth
+    from top_sparse_attention_gb300 import split
+
+    wl = synth.small_workload("prefill_t4096_l128k_bf16", T=16, q_per_seq=16, L=700, K=128, q_pos0=600)
+    cpu = synth.make_inputs(wl)
+    ch = oracle.Chain(synth.to_numpy_bits(cpu), L=wl.L, K=wl.K, q_per_seq=wl.q_per_seq, q_pos0=wl.q_pos0,
+                      idx_dtype=wl.idx_dtype, kv_dtype=wl.kv_dtype, sm_scale=wl.sm_scale)
+    seen = []
+
+    def run_segment(a, b):  # the oracle in place of this rank's dsa_prefill on queries [a, b)
+        seen.append((a, b))
+        rows = [oracle.chain_query(ch, t, wl.D_v) for t in range(a, b)]
+        return (torch.from_numpy(np.stack([r["out"] for r in rows])), torch.from_numpy(np.stack([r["lse"] for r in rows])),
+                torch.from_numpy(np.stack([r["idx"] for r in rows])))
+
+    o, l, i = split.zigzag_prefill_rank(run_segment, wl.T)
+    out[rank] = (o.numpy(), l.numpy(), i.numpy(), seen)
+    dist.destroy_process_group()
+
+
+def test_zigzag_prefill_ranks_gather_rows_back_in_query_order():
+    import oracle
+    import synth
+    from top_sparse_attention_gb300 import build
+
+    build.build()
+    world = 2
+    port = _free_port()
+    manager = mp.get_context("spawn").Manager()
+    out = manager.dict()
+    mp.start_processes(_prefill_rank_main, args=(world, port, out), nprocs=world, start_method="spawn", join=True)
+    assert out[0][3] == [(0, 4), (12, 16)] and out[1][3] == [(4, 8), (8, 12)]
+    wl = synth.small_workload("prefill_t4096_l128k_bf16", T=16, q_per_seq=16, L=700, K=128, q_pos0=600)
+    ch = oracle.Chain(synth.to_numpy_bits(synth.make_inputs(wl)), L=wl.L, K=wl.K, q_per_seq=wl.q_per_seq,
+                      q_pos0=wl.q_pos0, idx_dtype=wl.idx_dtype, kv_dtype=wl.kv_dtype, sm_scale=wl.sm_scale)
+    for r in range(world):
+        o, l, i, _ = out[r]
+        for t in range(wl.T):
+            want = oracle.chain_query(ch, t, wl.D_v)
+            np.testing.assert_array_equal(i[t], want["idx"])
+            np.testing.assert_array_equal(o[t], want["out"])
+            np.testing.assert_array_equal(l[t], want["lse"])

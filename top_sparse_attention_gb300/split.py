@@ -19,6 +19,10 @@ and moves the two small exchanges (for K = 2048: 16 KB of pairs and 16 x 512 fp3
 query and slice).  `SplitDecode` runs all slices on one device, writing the parts side by side
 (the exchanges are then plain layout); `split_decode_rank` runs one slice per rank of a
 torch.distributed group and exchanges the parts with all_gather.
+
+A prefill chunk splits the other way, by query: `zigzag_prefill_rank` gives rank g the query
+segments g and 2G - 1 - g of 2G equal segments, so every rank scores the same number of causal
+positions, and gathers the rows back into query order.
 """
 from __future__ import annotations
 
@@ -29,7 +33,8 @@ import torch
 
 from . import api
 
-__all__ = ["SplitPlan", "SliceSteps", "SplitDecode", "slice_caches", "split_decode_rank"]
+__all__ = ["SplitPlan", "SliceSteps", "SplitDecode", "slice_caches", "split_decode_rank", "zigzag_segments",
+           "zigzag_work", "prefill_segment", "zigzag_prefill_rank"]
 
 CACHE_KEYS = ("k_idx", "k_idx_sf", "kv", "kv_scale", "kv_v")
 
@@ -184,3 +189,64 @@ def split_decode_rank(steps, q_idx, q_idx_sf, w, q, *, K: int, H: int, D_v: int,
     dist.all_gather(list(lse_parts.unbind(0)), lse_part, group=group)
     out, lse = combine(o_parts, lse_parts)
     return out, lse, idx
+
+
+# ------------------------------------------------------------------------------------------------
+# Context-parallel prefill with zigzag segments ("Day 0 Support for New LLM Architectures", Key
+# Optimization 3: the later a query sits in a causal chunk, the more history it scores, so rank g
+# takes segments g and 2G - 1 - g of 2G equal segments; one gather then puts the rows back in
+# order).  Each rank runs the fused prefill chain on its own queries against the whole context.
+
+
+def zigzag_segments(T: int, G: int, rank: int):
+    """Query ranges [a, b) of a T-query chunk that rank `rank` of G handles: segments rank and
+    2G - 1 - rank of 2G equal segments (T a multiple of 2G)."""
+    if T % (2 * G):
+        raise ValueError("the chunk must split into 2G equal segments")
+    seg = T // (2 * G)
+    return [(rank * seg, (rank + 1) * seg), ((2 * G - 1 - rank) * seg, (2 * G - rank) * seg)]
+
+
+def zigzag_work(T: int, G: int, rank: int, q_pos0: int) -> int:
+    """Causal work of a rank: the positions its queries see, sum of (q_pos0 + t + 1)."""
+    return sum(q_pos0 + t + 1 for a, b in zigzag_segments(T, G, rank) for t in range(a, b))
+
+
+def prefill_segment(tensors: Dict[str, Optional[torch.Tensor]], a: int, b: int, *, K: int, sm_scale: float,
+                    q_pos0: int, stream=None):
+    """The fused prefill chain (dsa_prefill) on queries [a, b) of a chunk whose query 0 sits at
+    position q_pos0: the query-side inputs are the rows a .. b - 1, the caches the whole context."""
+    from . import call_from_tensors
+
+    seg = dict(tensors)
+    for k in ("q_idx", "q_idx_sf", "w", "q"):
+        if seg.get(k) is not None:
+            seg[k] = seg[k][a:b]
+    call = call_from_tensors(seg, K=K, sm_scale=sm_scale, q_per_seq=b - a, q_pos0=q_pos0 + a)
+    out, lse, idx = call(stream)
+    return out, lse, idx
+
+
+def zigzag_prefill_rank(run_segment, T: int, *, group=None):
+    """One rank's part of a context-parallel prefill chunk of T queries: run_segment(a, b) computes
+    (out [b-a, H, D_v], lse [b-a, H], idx [b-a, K]) for queries [a, b) on this rank; the rows of all
+    ranks are exchanged with one all_gather each and returned in query order on every rank."""
+    import torch.distributed as dist
+
+    G = dist.get_world_size(group)
+    rank = dist.get_rank(group)
+    segs = zigzag_segments(T, G, rank)
+    parts = [run_segment(a, b) for a, b in segs]
+    mine = [torch.cat([p[i] for p in parts], dim=0).contiguous() for i in range(3)]  # [T/G, ...]
+    result = []
+    for x in mine:
+        gathered = [torch.empty_like(x) for _ in range(G)]
+        dist.all_gather(gathered, x, group=group)
+        full = torch.empty((T,) + tuple(x.shape[1:]), dtype=x.dtype, device=x.device)
+        for g, y in enumerate(gathered):
+            off = 0
+            for a, b in zigzag_segments(T, G, g):
+                full[a:b] = y[off:off + (b - a)]
+                off += b - a
+        result.append(full)
+    return tuple(result)
