@@ -54,6 +54,10 @@ constexpr int kHeads = 16;    // heads per CTA (M of m16n8k16)
 #ifndef DSA_ATTN_CTA_TARGET
 #define DSA_ATTN_CTA_TARGET 76  // attention CTAs aimed for when K is split (about one per two SMs)
 #endif
+// 1: the attention kernels signal the combine kernel after their row blocks, 0: at their start.
+#ifndef DSA_PDL_LATE_ATTN
+#define DSA_PDL_LATE_ATTN 1
+#endif
 constexpr int kRows = 64;     // gathered rows per block
 constexpr int kMaxRows = 4096;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -138,7 +142,7 @@ __global__ void __launch_bounds__(Cfg<DQK, DV, FP8, SEPV, TILED>::THREADS, 1)
 sparse_attn_kernel(const SparseAttnParams p) {
   using C = Cfg<DQK, DV, FP8, SEPV, TILED>;
   extern __shared__ __align__(128) uint8_t smem[];
-  pdl_launch_dependents();  // the combine kernel may launch now; it waits for this grid's results
+  if (!DSA_PDL_LATE_ATTN) pdl_launch_dependents();  // the combine kernel may launch now
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -491,6 +495,7 @@ sparse_attn_kernel(const SparseAttnParams p) {
     group_sync<C::GT>(g);  // the slot and P are rewritten next
     if (ok && b + 2 < nblk) issue(b + 2);
   }
+  if (DSA_PDL_LATE_ATTN) pdl_launch_dependents();
   // ---- merge the second group into the first
   {
     __syncthreads();  // all slots are idle: reuse slot 1 as staging
@@ -701,7 +706,7 @@ __global__ void __launch_bounds__(256, 1) sparse_attn_tc_kernel(const SparseAttn
   float* scale_s = reinterpret_cast<float*>(smem + C::OFF_SC);  // [row][NSC]
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);  // [0] S done, [1] O done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 2);
-  pdl_launch_dependents();
+  if (!DSA_PDL_LATE_ATTN) pdl_launch_dependents();
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int split = blockIdx.x, t = blockIdx.y, h0 = blockIdx.z * kHeads;
@@ -948,6 +953,7 @@ __global__ void __launch_bounds__(256, 1) sparse_attn_tc_kernel(const SparseAttn
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+  if (DSA_PDL_LATE_ATTN) pdl_launch_dependents();
 }
 
 template <bool FP8, bool TILED>

@@ -50,6 +50,12 @@ constexpr int kCachedKeys = 16384;    // largest slice kept in shared memory
 #define DSA_TOPK_KEYS_PER_CTA 8192
 #endif
 constexpr int kKeysPerCta = DSA_TOPK_KEYS_PER_CTA;
+// When the cluster kernel signals the attention kernel (griddepcontrol.launch_dependents): 0 at its
+// start, 1 once the threshold is known (before the output pass), 2 at its exit.  1 keeps the
+// attention CTAs (174 KB of shared memory each) off the SMs while the selection runs.
+#ifndef DSA_PDL_LATE_TOPK
+#define DSA_PDL_LATE_TOPK 1
+#endif
 constexpr int kManyQueries = 64;        // launches with at least this many queries ...
 constexpr int kManyKeysPerCta = 65536;  // ... use clusters of about this many keys per CTA
 constexpr int kCand = 4096;           // own candidate list capacity (shared memory)
@@ -217,7 +223,7 @@ __device__ __forceinline__ void cluster_wait() {
 
 __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkParams p) {
   extern __shared__ __align__(16) uint32_t sm[];
-  pdl_launch_dependents();
+  if (DSA_PDL_LATE_TOPK == 0) pdl_launch_dependents();
   const int t = blockIdx.y;
   const int tid = threadIdx.x;
   const int C = (int)cluster_size();
@@ -532,6 +538,7 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkParams
     eq_before = sc[kScEq];
   }
 
+  if (DSA_PDL_LATE_TOPK == 1) pdl_launch_dependents();
   // ---- output, ascending positions: slot = (keys > T before) + min(keys == T before, kr).
   // One 64-bit scan per chunk: low half = (ties << 16 | keys above T) prefix in the chunk, high
   // half = the list counts before this slice (first chunk only; summed over the block).
@@ -1024,17 +1031,7 @@ WidePlan wide_plan(int T, int L) {
 
 template <typename Kern>
 cudaError_t launch_plain(Kern kern, dim3 grid, const TopkParams& p, cudaStream_t stream, bool pdl) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  return launch_kernel(kern, grid, dim3(kThreads), 0, stream, pdl, p);
 }
 
 cudaError_t launch_wide(TopkParams q, const WidePlan& w, cudaStream_t stream, bool pdl) {
