@@ -429,14 +429,23 @@ index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     const int et = threadIdx.x - 64;
     int ai = 0, cur_t0 = -1;
     bool ok = true;
-    // flushes the shared histogram of query t into the global one (non-zero bins only)
+    // flushes the shared histogram of query t into the global one and clears it: 16-byte reads
+    // (all of a thread's in flight at once), then one 64-bit atomic add per pair of bins with a
+    // non-zero count (the low word of a pair never carries: a row has fewer than 2^32 positions)
     auto flush_hist = [&](int t) {
-      for (int b = et; b < kHistBins; b += ET) {
-        const uint32_t v = hist_s[b];
-        if (v) {
-          atomicAdd(&p.hist[(int64_t)t * kHistBins + b], v);
-          hist_s[b] = 0;
-        }
+      static_assert(kHistBins % (4 * ET) == 0, "whole 16-byte groups of bins per thread");
+      constexpr int NV = kHistBins / (4 * ET);
+      uint4* h4 = reinterpret_cast<uint4*>(hist_s);
+      unsigned long long* g2 = reinterpret_cast<unsigned long long*>(p.hist + (int64_t)t * kHistBins);
+      uint4 v[NV];
+#pragma unroll
+      for (int k = 0; k < NV; ++k) v[k] = h4[et + k * ET];
+#pragma unroll
+      for (int k = 0; k < NV; ++k) {
+        const int pair = 2 * (et + k * ET);  // bins 2 pair .. 2 pair + 3
+        if (v[k].x | v[k].y) atomicAdd(g2 + pair, (unsigned long long)v[k].y << 32 | v[k].x);
+        if (v[k].z | v[k].w) atomicAdd(g2 + pair + 1, (unsigned long long)v[k].w << 32 | v[k].z);
+        h4[et + k * ET] = make_uint4(0u, 0u, 0u, 0u);
       }
     };
     if (build_hist)
