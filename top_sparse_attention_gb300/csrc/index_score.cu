@@ -172,6 +172,27 @@ template <int G>
 __device__ __forceinline__ void unit_share(const IndexScoreParams& p, int* share) {
   const int lane = threadIdx.x & 31;
   const int n_groups = (p.T + G - 1) / G;
+  if (p.q_pos0 < 0 && p.n_valid == nullptr) {
+    // every query sees all L positions: every group has the same `tiles` visible units, so the
+    // share is a closed form (32-bit arithmetic when V * gridDim.x fits)
+    if (lane == 0) {
+      const uint32_t vt = (uint32_t)p.tiles, B = gridDim.x, b = blockIdx.x;
+      const uint64_t V = (uint64_t)n_groups * vt;
+      uint32_t b0, b1;
+      if (V * B < (1ull << 32)) {
+        b0 = (uint32_t)V * b / B;
+        b1 = (uint32_t)V * (b + 1) / B;
+      } else {
+        b0 = (uint32_t)(V * b / B);
+        b1 = (uint32_t)(V * (b + 1) / B);
+      }
+      const uint32_t g = vt ? b0 / vt : 0;
+      share[0] = (int)min(g, (uint32_t)max(n_groups - 1, 0));
+      share[1] = (int)(b0 - g * vt);
+      share[2] = (int)(b1 - b0);
+    }
+    return;
+  }
   const int g_lo = (int)((int64_t)n_groups * lane / 32), g_hi = (int)((int64_t)n_groups * (lane + 1) / 32);
   int64_t mine = 0;
   for (int g = g_lo; g < g_hi; ++g) mine += UnitWalk<G>::visible_tiles(p, g);
