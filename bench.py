@@ -258,12 +258,15 @@ def dist_env():
 GRAPH_MAX_STEPS = 240  # steps held by one captured graph (a multiple of the input-set count is used)
 
 
-def capture_steps(first, count, stream, streams, enqueue):
+def capture_steps(first, count, stream, streams, enqueue, events=None):
     """One CUDA graph holding steps first .. first+count-1: step i is enqueued by enqueue(i, st)
     on streams[i % len(streams)], all forked from and joined back into `stream`.  Everything the
-    steps read stays owned by the caller (a graph keeps raw pointers only)."""
+    steps read stays owned by the caller (a graph keeps raw pointers only).  `events` = (start,
+    end) timing events recorded as the graph's first and last nodes (external events)."""
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
+        if events is not None:
+            events[0].record(stream)
         fork = torch.cuda.Event()
         fork.record(stream)
         for st in streams:
@@ -276,6 +279,8 @@ def capture_steps(first, count, stream, streams, enqueue):
         for st in streams:
             if st is not stream:
                 stream.wait_stream(st)
+        if events is not None:
+            events[1].record(stream)
     return g
 
 
@@ -292,34 +297,43 @@ def step_plan(steps, n_sets):
 def timed_steps(steps, n_sets, stream, streams, enqueue, barrier, graphs=True, clocks=None):
     """Device milliseconds per step for exactly `steps` steps, step i enqueued by enqueue(i, st)
     on streams[i % len(streams)].  With graphs, the steps are replayed from CUDA graphs of up to
-    GRAPH_MAX_STEPS steps each (captured and replayed once before timing), so the host launches a
+    GRAPH_MAX_STEPS steps each (captured and replayed before timing), so the host launches a
     handful of graphs and the figure does not depend on the host's launch rate; CUDA events on
     `stream` bracket the region, with a barrier and a device synchronisation on both sides.
     `clocks` (a ClockSampler) samples the GPU clocks while the timed region runs."""
     import contextlib
 
     sampling = clocks if clocks is not None else contextlib.nullcontext()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if graphs:
         period, full, tail = step_plan(steps, n_sets)
-        g_period = capture_steps(0, period, stream, streams, enqueue)
+        single = full == 1 and not tail
+        # a single graph carries its own timing events as its first and last nodes, so the figure
+        # is the device time of exactly its steps (without the host's graph-launch latency, which
+        # a few-step window would not amortise); several graphs are timed around their replays
+        ev0 = torch.cuda.Event(enable_timing=True, external=single)
+        ev1 = torch.cuda.Event(enable_timing=True, external=single)
+        g_period = capture_steps(0, period, stream, streams, enqueue, events=(ev0, ev1) if single else None)
         g_tail = capture_steps(full * period, tail, stream, streams, enqueue) if tail else None
-        with torch.cuda.stream(stream):  # untimed replay: every node has run once
-            g_period.replay()
+        with torch.cuda.stream(stream):  # untimed replays: every node has run, the graph is resident
+            for _ in range(3 if single else 1):
+                g_period.replay()
             if g_tail is not None:
                 g_tail.replay()
         torch.cuda.synchronize()
         barrier()
         torch.cuda.synchronize()
         with sampling, torch.cuda.stream(stream):
-            ev0.record(stream)
+            if not single:
+                ev0.record(stream)
             for _ in range(full):
                 g_period.replay()
             if g_tail is not None:
                 g_tail.replay()
-            ev1.record(stream)
+            if not single:
+                ev1.record(stream)
             torch.cuda.synchronize()
     else:
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
         torch.cuda.synchronize()
         sampling.__enter__()

@@ -174,6 +174,14 @@ cudaError_t run_index_score(const dsa_args& a, int t_off, int T, float* scores, 
                             a.idx_dtype == DSA_MXFP8_E4M3, p, st, pdl, hist_filled);
 }
 
+// 1: the chain's Top-K issues an L2 prefetch of every selected cache row as it writes the position.
+// Off: since the Top-K lets the attention kernel launch at its output pass, the prefetch requests
+// (one bulk prefetch per row) cost the Top-K more than they save the gather (B = 8, L = 32K, six
+// batches in flight: bf16 18.1 -> 17.2 us per step, MXFP8 17.2 -> 16.8 us; one batch at a time
+// 41.2 -> 40.4 us and 44.4 -> 43.3 us; L = 1M and varying lengths gained as well).
+#ifndef DSA_TOPK_KV_PREFETCH
+#define DSA_TOPK_KV_PREFETCH 0
+#endif
 cudaError_t run_topk(const dsa_args& a, int t_off, int T, const float* scores, int64_t ld,
                      int32_t* idx, uint32_t* hist, void* ws, cudaStream_t st, bool pdl) {
   TopkParams p = {};
@@ -189,8 +197,8 @@ cudaError_t run_topk(const dsa_args& a, int t_off, int T, const float* scores, i
   p.t_off = t_off;
   p.err = device_error_ptr();
   p.hist = hist;
-  // the chain prefetches the selected cache rows for the attention step
-  p.kv = reinterpret_cast<const uint8_t*>(a.kv);
+  // the selected cache rows can be prefetched into L2 for the attention step (DSA_TOPK_KV_PREFETCH)
+  p.kv = DSA_TOPK_KV_PREFETCH ? reinterpret_cast<const uint8_t*>(a.kv) : nullptr;
   p.kv_row_stride = a.kv_row_stride;
   p.kv_seq_stride = a.kv_seq_stride;
   p.kv_bytes = a.D_qk * (a.kv_dtype == DSA_BF16 ? 2 : 1);  // (E4M3 rows: one byte per element)

@@ -25,9 +25,9 @@
 //  * Output, ascending positions: the slot of a kept key is (keys > T before it) + min(keys == T
 //    before it, ties to take), so exact ties go to the lower positions; each CTA writes its keys
 //    straight to the index row.
-// The workspace histograms are zeroed again before the kernel ends.  In the fused chain the kernel
-// also starts the attention step's cache reads: every selected row is prefetched into L2 as its
-// position is written, so the reads overlap the kernel boundary.
+// The workspace histograms are zeroed again before the kernel ends.  When given the attention
+// cache (TopkParams::kv; the fused chain's build switch DSA_TOPK_KV_PREFETCH, off by default) the
+// kernel also prefetches every selected row into L2 as its position is written.
 #include <mutex>
 
 #include "dsa_internal.h"
