@@ -1033,7 +1033,9 @@ int sparse_attn_splits(int T, int H, int K) {
   if (ctas_per_split <= 0) return 1;
   int s = (DSA_ATTN_CTA_TARGET + ctas_per_split - 1) / ctas_per_split;
   s = s < 1 ? 1 : (s > 64 ? 64 : s);
-  if (s > blocks) s = blocks;
+  // at least two blocks per split: a CTA's two warp groups take alternate blocks, so a one-block
+  // split leaves one group idle (one query, K = 2048: 16 CTAs of 128 rows instead of 32 of 64)
+  if (s > blocks / 2) s = blocks / 2 > 1 ? blocks / 2 : 1;
   // whole blocks per split, and no empty split
   const int rows = ((blocks + s - 1) / s) * kRows;
   return (K + rows - 1) / rows;
