@@ -1009,8 +1009,15 @@ size_t topk_cluster_ws_bytes(int T, int L) {
 namespace {
 
 // Row-split plan: rows longer than a 16-CTA cluster can keep in shared memory are cut into
-// chunks of a multiple of kChunk positions, sized so that all rows together take about one CTA
-// per SM of a 152-SM part (a fixed figure, so that workspace sizing needs no device query).
+// chunks of a multiple of kChunk positions, sized so that all rows together take about
+// DSA_TOPK_WIDE_CTAS CTAs (a fixed figure, so that workspace sizing needs no device query).  Each
+// CTA of the scan and emit kernels holds a whole SM (1024 threads x 64 registers), so fewer, longer
+// chunks leave more SMs to other batches' kernels: one query at L = 1M, six batches in flight,
+// 128 / 86 / 64 / 32 chunks gave 30.2 / 29.65 / 29.55 / 30.6 us per step, one batch at a time
+// 59.3 / 59.4 / 60.4 / 67.4 us.
+#ifndef DSA_TOPK_WIDE_CTAS
+#define DSA_TOPK_WIDE_CTAS 100
+#endif
 struct WidePlan {
   bool use;
   int chunk, nch;
@@ -1020,7 +1027,7 @@ WidePlan wide_plan(int T, int L) {
   WidePlan w = {false, 0, 0};
   // (decode-sized batches only: the candidate lists take 8 bytes per position of every row)
   if (T <= 0 || T > 32 || (int64_t)L <= 16ll * kCachedKeys) return w;
-  const int64_t target = T >= 152 ? 1 : 152 / T;  // chunks per row
+  const int64_t target = T >= DSA_TOPK_WIDE_CTAS ? 1 : DSA_TOPK_WIDE_CTAS / T;  // chunks per row
   int64_t chunk = ((L + target - 1) / target + kChunk - 1) / kChunk * kChunk;
   while ((L + chunk - 1) / chunk > kWideMaxChunks) chunk += kChunk;
   w.use = true;
