@@ -41,6 +41,13 @@ constexpr int kTileM = 128;
 // SMs long before they can start (decode B = 8, L = 32K, one batch at a time: the three kernels
 // signalling late took the step from 43.5 to 41.8 us for bf16 and from 49.6 to 46.3 us for MXFP8;
 // six batches in flight: unchanged within 1 %).
+// Inside the fused chain a long one-query launch takes this many quarters of the two-CTA slots, so
+// that the next batch's scoring starts while this one streams (its ramp, about 3 us to the first
+// tile, overlaps): L = 1M, six batches in flight, 4 / 3 / 2 quarters gave 29.8 / 28.5 / 27.7 us
+// per step, one batch at a time 59.1 / 65.7 / 72.2 us.
+#ifndef DSA_IDX_LONG_SLOTS_Q
+#define DSA_IDX_LONG_SLOTS_Q 3
+#endif
 #ifndef DSA_PDL_LATE_IDX
 #define DSA_PDL_LATE_IDX 1
 #endif
@@ -640,11 +647,12 @@ cudaError_t launch_cfg(const void* q_idx, const void* k_idx, int64_t k_seq_strid
   // tens of thousands of positions per query) runs one CTA per SM, so half the slots stay free for
   // the Top-K and attention CTAs of other batches in flight: decode B = 8, L = 32K with six batches
   // in flight, 19.97 -> 18.63 us per step (bf16) and 20.47 -> 18.04 us (MXFP8), at 2-3 us more for
-  // one batch alone (grids of 3/4 and 2/3 of the slots fell in between).  Long launches (one query
-  // over a million positions) need both CTAs of every SM to reach the memory bandwidth, and a
-  // launch on its own (dsa_index_score) takes every slot.
+  // one batch alone (grids of 3/4 and 2/3 of the slots fell in between).  Long chain launches (one
+  // query over a million positions) take DSA_IDX_LONG_SLOTS_Q quarters of the slots; a launch on
+  // its own (dsa_index_score) takes every slot.
   int64_t slots = (int64_t)sms * C::CTAS_PER_SM;
   if (p.share_sms && C::CTAS_PER_SM == 2 && units < 16 * slots) slots = sms;
+  else if (p.share_sms && C::CTAS_PER_SM == 2) slots = slots * DSA_IDX_LONG_SLOTS_Q / 4;
   const int grid = (int)(units < slots ? units : slots);
   if (grid <= 0) return cudaSuccess;
   return launch_kernel(kern, dim3(grid), dim3(C::THREADS), C::SMEM, stream, pdl, tm, tq,
