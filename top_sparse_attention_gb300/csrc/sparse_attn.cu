@@ -119,6 +119,18 @@ __device__ __forceinline__ uint32_t bf16x2_of_e4m3_f32(float lo, float hi) {
   return __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);
 }
 
+// Two E4M3 codes (the bytes of x picked by `sel` into bits 8..15 and 24..31) as two bf16, exactly.
+// The code s.eeee.mmm placed as the bf16 pattern s.0000eeee.mmm0000 has 2^-120 times the code's
+// value: for e >= 1 both read 2^(e - bias) (1 + m/8), with biases 127 and 7; for e = 0 both are
+// subnormal, m/8 x 2^-126 and m/8 x 2^-6.  Scaling by 2^120 is exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t x, uint32_t sel) {
+  const uint32_t t = __byte_perm(x, 0u, sel);
+  const uint32_t pat = (t & 0x80008000u) | ((t & 0x7F007F00u) >> 4);
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(pat), "r"(0x7B807B80u));  // x 2^120
+  return r;
+}
+
 // Bulk copy of `bytes` (a multiple of 16) from global to shared memory on the TMA engine.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
@@ -272,6 +284,18 @@ sparse_attn_kernel(const SparseAttnParams p) {
     sel8 |= (4 * (lane & 3) + i == (lane >> 2) + 8 ? 0x38u : 0u) << (8 * i);
   }
   bool ok = mbar_wait(&bars[2], 0, p.err);  // q is in shared memory
+  if constexpr (FP8) {
+    // E4M3 rows: within each group of 16 columns, q is stored in the column order 0,1,4,5,8,9,12,13,
+    // 2,3,6,7,10,11,14,15 (32-bit word p <- word {0,2,4,6,1,3,5,7}[p]), the order in which the
+    // widened raw rows form B fragments above; the sum over columns does not depend on it
+    for (int i = tid; i < kHeads * (DQK / 16); i += C::THREADS) {
+      uint4* g = reinterpret_cast<uint4*>(q_s + (i / (DQK / 16)) * C::ROW + (i % (DQK / 16)) * 32);
+      const uint4 x = g[0], y = g[1];
+      g[0] = make_uint4(x.x, x.z, y.x, y.z);
+      g[1] = make_uint4(x.y, x.w, y.y, y.w);
+    }
+    __syncthreads();
+  }
 
   // per-thread softmax state for heads r0 = lane/4 and r1 = lane/4 + 8
   const int r0 = lane >> 2, r1 = r0 + 8;
@@ -304,25 +328,21 @@ sparse_attn_kernel(const SparseAttnParams p) {
 #pragma unroll
         for (int j = 0; j < NJ; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
         if constexpr (FP8) {
-          // the warp's 16 raw rows x 32 columns as E4M3 A fragments (matrices: rows 0-7 | 8-15 x
-          // bytes 0-15 | 16-31); the selections at column offsets 0, 8, 16, 24 give the B
-          // fragments of the chunk's two k-steps for both n-tiles
+          // the warp's 16 raw rows x 32 columns (matrices: rows 0-7 | 8-15 x bytes 0-15 | 16-31):
+          // each register holds the codes of columns 4j .. 4j+3 (j = lane % 4) of row lane / 4, and
+          // widened exactly to bf16 pairs (4j, 4j+1) and (4j+2, 4j+3) it is the B fragment of a
+          // k-step whose columns run in the order q_s was stored in (see the q permutation)
           const uint32_t ka = smem_u32(kv_s) + (gw * 16 + rr + (mat & 1) * 8) * C::RAWROW + (mat >> 1) * 16;
 #pragma unroll 2
           for (int cc = c0; cc < c1; ++cc) {
             uint32_t a0, a1, a2, a3, q0, q1, q2, q3;
             ldsm_x4(ka + cc * 32, a0, a1, a2, a3);
-            float e0[4], e8[4], e16[4], e24[4];
-            mma_e4m3_16832(e0, a0, a1, a2, a3, sel0, 0u);
-            mma_e4m3_16832(e8, a0, a1, a2, a3, sel8, 0u);
-            mma_e4m3_16832(e16, a0, a1, a2, a3, 0u, sel0);
-            mma_e4m3_16832(e24, a0, a1, a2, a3, 0u, sel8);
             ldsm_x4(qa + (2 * cc) * 32, q0, q1, q2, q3);
-            mma_bf16_16816(o[0], q0, q1, q2, q3, bf16x2_of_e4m3_f32(e0[0], e0[1]), bf16x2_of_e4m3_f32(e8[0], e8[1]));
-            mma_bf16_16816(o[1], q0, q1, q2, q3, bf16x2_of_e4m3_f32(e0[2], e0[3]), bf16x2_of_e4m3_f32(e8[2], e8[3]));
+            mma_bf16_16816(o[0], q0, q1, q2, q3, e4m3x2_to_bf16x2(a0, 0x1404), e4m3x2_to_bf16x2(a0, 0x3424));
+            mma_bf16_16816(o[1], q0, q1, q2, q3, e4m3x2_to_bf16x2(a1, 0x1404), e4m3x2_to_bf16x2(a1, 0x3424));
             ldsm_x4(qa + (2 * cc + 1) * 32, q0, q1, q2, q3);
-            mma_bf16_16816(o[0], q0, q1, q2, q3, bf16x2_of_e4m3_f32(e16[0], e16[1]), bf16x2_of_e4m3_f32(e24[0], e24[1]));
-            mma_bf16_16816(o[1], q0, q1, q2, q3, bf16x2_of_e4m3_f32(e16[2], e16[3]), bf16x2_of_e4m3_f32(e24[2], e24[3]));
+            mma_bf16_16816(o[0], q0, q1, q2, q3, e4m3x2_to_bf16x2(a2, 0x1404), e4m3x2_to_bf16x2(a2, 0x3424));
+            mma_bf16_16816(o[1], q0, q1, q2, q3, e4m3x2_to_bf16x2(a3, 0x1404), e4m3x2_to_bf16x2(a3, 0x3424));
           }
         } else {
           // matrices of one k-step: (rows 0-7 | 8-15) x (k 0-7 | 8-15)
@@ -659,18 +679,6 @@ struct TcCfg {
   static constexpr int O_COL = 128;
   static_assert(16 * SACC <= O_COL, "S accumulators");
 };
-
-// Two E4M3 codes (the bytes of x picked by `sel` into bits 8..15 and 24..31) as two bf16, exactly.
-// The code s.eeee.mmm placed as the bf16 pattern s.0000eeee.mmm0000 has 2^-120 times the code's
-// value: for e >= 1 both read 2^(e - bias) (1 + m/8), with biases 127 and 7; for e = 0 both are
-// subnormal, m/8 x 2^-126 and m/8 x 2^-6.  Scaling by 2^120 is exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t x, uint32_t sel) {
-  const uint32_t t = __byte_perm(x, 0u, sel);
-  const uint32_t pat = (t & 0x80008000u) | ((t & 0x7F007F00u) >> 4);
-  uint32_t r;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(pat), "r"(0x7B807B80u));  // x 2^120
-  return r;
-}
 
 // Butterfly over a warp: v[0..15] are this lane's values for heads 0..15; afterwards v[0] holds the
 // reduction over all 32 lanes of head (lane >> 1) & 15.
