@@ -95,6 +95,10 @@ struct Cfg {
   static constexpr int OFF_IDX = OFF_BAR + 64;
   static int bytes(int rows) { return OFF_IDX + rows * 4 * (1 + NSC); }
   static_assert(!TILED || (FP8 && DV == 512 && DQK % 16 == 0), "tiled scales: the 576/512 latent row");
+  // E4M3 rows with whole 32-column chunks per warp: P.V takes V through a transposed ldmatrix of the
+  // raw rows, and the accumulators hold even / odd value columns (acc[2g], acc[2g+1] for the warp's
+  // 16-column group g)
+  static constexpr bool EOV = FP8 && CPW % 32 == 0;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -476,10 +480,26 @@ sparse_attn_kernel(const SparseAttnParams p) {
       for (int kk = 0; kk < kRows / 16; ++kk) {
         uint32_t a0, a1, a2, a3;
         ldsm_x4(p_base + swz(rr + (mat & 1) * 8, 2 * kk + (mat >> 1), C::P_CHUNKS), a0, a1, a2, a3);
-        if constexpr (FP8) {
-          // raw rows 16kk .. 16kk+15 x 32 value columns as E4M3 B fragments (matrices: rows 0-7 |
-          // 8-15 x bytes 0-15 | 16-31); the selections on the left (value columns 0-15 or 16-31
-          // of the chunk) give the V fragments of four n-tiles, rows 0-7 and 8-15 in turn
+        if constexpr (C::EOV) {
+          // raw rows 16kk .. 16kk+15 read transposed as 16-bit pairs of value columns (matrices:
+          // rows 0-7 | 8-15 x bytes 0-15 | 16-31 of the chunk): a register holds rows 2j and 2j+1
+          // (j = lane % 4) of value columns 2c and 2c+1 (c = lane / 4).  Widened exactly, bytes
+          // (0, 2) are the B fragment of column 2c and bytes (1, 3) that of column 2c+1, so 16
+          // value columns form two n-tiles: the even columns (acc[2g]) and the odd ones (acc[2g+1])
+          const uint32_t vb = smem_u32(kv_s) + (16 * kk + rr + (mat & 1) * 8) * C::RAWROW + (mat >> 1) * 16;
+#pragma unroll
+          for (int ch = 0; ch < C::CPW / 32; ++ch) {
+            uint32_t v0, v1, v2, v3;
+            ldsm_x4_t(vb + gw * C::CPW + 32 * ch, v0, v1, v2, v3);
+            mma_bf16_16816(acc[4 * ch], a0, a1, a2, a3, e4m3x2_to_bf16x2(v0, 0x2404), e4m3x2_to_bf16x2(v1, 0x2404));
+            mma_bf16_16816(acc[4 * ch + 1], a0, a1, a2, a3, e4m3x2_to_bf16x2(v0, 0x3414), e4m3x2_to_bf16x2(v1, 0x3414));
+            mma_bf16_16816(acc[4 * ch + 2], a0, a1, a2, a3, e4m3x2_to_bf16x2(v2, 0x2404), e4m3x2_to_bf16x2(v3, 0x2404));
+            mma_bf16_16816(acc[4 * ch + 3], a0, a1, a2, a3, e4m3x2_to_bf16x2(v2, 0x3414), e4m3x2_to_bf16x2(v3, 0x3414));
+          }
+        } else if constexpr (FP8) {
+          // 16-column warps (64-wide rows): raw rows 16kk .. 16kk+15 x 32 value columns as E4M3 B
+          // fragments (matrices: rows 0-7 | 8-15 x bytes 0-15 | 16-31); the selections on the left
+          // (value columns 0-15 or 16-31 of the chunk) give the V fragments of two n-tiles
           const uint32_t vb = smem_u32(kv_s) + (16 * kk + rr + (mat >> 1) * 8) * C::RAWROW + (mat & 1) * 16;
           constexpr int CH = C::CPW >= 32 ? C::CPW / 32 : 1;  // chunks of the warp's columns
 #pragma unroll
@@ -552,6 +572,9 @@ sparse_attn_kernel(const SparseAttnParams p) {
   }
 
   const int col0 = gw * C::CPW + (lane & 3) * 2;
+  // even / odd accumulators (C::EOV): slot s of acc[2g] is value column 16g + 2s, of acc[2g + 1]
+  // column 16g + 2s + 1, so a thread holds 4 consecutive columns of each group
+  const int colq = gw * C::CPW + (lane & 3) * 4;
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
     const int h = h0 + (hh ? r1 : r0);
@@ -560,23 +583,46 @@ sparse_attn_kernel(const SparseAttnParams p) {
       const float inv = l_run[hh] > 0.f ? 1.f / l_run[hh] : 0.f;
       if (p.out_f32) {
         float* o = p.out_f32 + ((int64_t)t * p.H + h) * DV;
+        if constexpr (C::EOV) {
 #pragma unroll
-        for (int i = 0; i < NT; ++i)
-          *reinterpret_cast<float2*>(o + col0 + i * 8) = make_float2(acc[i][2 * hh] * inv, acc[i][2 * hh + 1] * inv);
+          for (int g2 = 0; g2 < NT / 2; ++g2)
+            *reinterpret_cast<float4*>(o + colq + 16 * g2) =
+                make_float4(acc[2 * g2][2 * hh] * inv, acc[2 * g2 + 1][2 * hh] * inv, acc[2 * g2][2 * hh + 1] * inv,
+                            acc[2 * g2 + 1][2 * hh + 1] * inv);
+        } else {
+#pragma unroll
+          for (int i = 0; i < NT; ++i)
+            *reinterpret_cast<float2*>(o + col0 + i * 8) = make_float2(acc[i][2 * hh] * inv, acc[i][2 * hh + 1] * inv);
+        }
       } else {
         __nv_bfloat16* o = p.out + ((int64_t)t * p.H + h) * DV;
+        if constexpr (C::EOV) {
 #pragma unroll
-        for (int i = 0; i < NT; ++i)
-          *reinterpret_cast<uint32_t*>(o + col0 + i * 8) = pack_bf16(acc[i][2 * hh] * inv, acc[i][2 * hh + 1] * inv);
+          for (int g2 = 0; g2 < NT / 2; ++g2)
+            *reinterpret_cast<uint2*>(o + colq + 16 * g2) =
+                make_uint2(pack_bf16(acc[2 * g2][2 * hh] * inv, acc[2 * g2 + 1][2 * hh] * inv),
+                           pack_bf16(acc[2 * g2][2 * hh + 1] * inv, acc[2 * g2 + 1][2 * hh + 1] * inv));
+        } else {
+#pragma unroll
+          for (int i = 0; i < NT; ++i)
+            *reinterpret_cast<uint32_t*>(o + col0 + i * 8) = pack_bf16(acc[i][2 * hh] * inv, acc[i][2 * hh + 1] * inv);
+        }
       }
       if (p.lse && (lane & 3) == 0 && gw == 0)
         p.lse[(int64_t)t * p.H + h] = l_run[hh] > 0.f ? (m_run[hh] + log2f(l_run[hh])) * kLn2 : -INFINITY;
     } else {
       const int64_t row = ((int64_t)t * p.H + h) * p.splits + split;
       float* o = p.part_o + row * DV;
+      if constexpr (C::EOV) {
 #pragma unroll
-      for (int i = 0; i < NT; ++i)
-        *reinterpret_cast<float2*>(o + col0 + i * 8) = make_float2(acc[i][2 * hh], acc[i][2 * hh + 1]);
+        for (int g2 = 0; g2 < NT / 2; ++g2)
+          *reinterpret_cast<float4*>(o + colq + 16 * g2) =
+              make_float4(acc[2 * g2][2 * hh], acc[2 * g2 + 1][2 * hh], acc[2 * g2][2 * hh + 1], acc[2 * g2 + 1][2 * hh + 1]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < NT; ++i)
+          *reinterpret_cast<float2*>(o + col0 + i * 8) = make_float2(acc[i][2 * hh], acc[i][2 * hh + 1]);
+      }
       if ((lane & 3) == 0 && gw == 0)
         *reinterpret_cast<float2*>(p.part_ml + row * 2) = make_float2(m_run[hh], l_run[hh]);
     }
