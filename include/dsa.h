@@ -181,7 +181,8 @@ dsa_status dsa_topk_noalloc(const float* scores, int64_t ld_scores, int T, int q
  * Supported: kv_dtype DSA_BF16 or DSA_FP8_E4M3 with (D_qk, D_v) in {(576, 512), (64, 64)};
  * DSA_FP8_E4M3_T128 with (576, 512) and kv_v NULL; H <= 128; row strides multiples of 16
  * bytes; pointers 16-byte aligned.  E4M3 caches hold finite codes only (the quantisers below
- * saturate): a NaN code (0x7F / 0xFF) in a gathered row makes the results NaN.
+ * saturate): a NaN code (0x7F / 0xFF) in a gathered row is not detected and gives unspecified
+ * results (the 576/512 row widens it to a finite value).
  * ------------------------------------------------------------------------------------------ */
 dsa_status dsa_sparse_attn(const void* q, const void* kv, const void* kv_v, const float* kv_scale,
                            int64_t kv_row_stride, int64_t kv_seq_stride, int64_t v_row_stride,
