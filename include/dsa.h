@@ -37,7 +37,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 2
+#define DSA_ABI_VERSION 3
 
 typedef enum dsa_status {
   DSA_OK = 0,
@@ -190,6 +190,22 @@ dsa_status dsa_sparse_attn(const void* q, const void* kv, const void* kv_v, cons
                            int K, int H, int D_qk, int D_v, float sm_scale, dsa_dtype kv_dtype,
                            void* out, float* lse, void* ws, size_t ws_bytes, void* stream);
 size_t dsa_sparse_attn_workspace_size(int T, int H, int K, int D_v);
+
+/* Which kernel computes the attention over the 576 / 512 latent row (process-wide; takes effect
+ * for calls made after it returns, so do not change it while calls are in flight).
+ *   DSA_ATTN_AUTO     the library's choice (warp-level mma.sync over gathered 64-row blocks, E4M3
+ *                     rows widened exactly in registers); the default
+ *   DSA_ATTN_TCGEN05  the tensor-memory kernel (128 rows per CTA in one swizzled bf16 tile, both
+ *                     contractions on tcgen05.mma) for the entries that take it on their own
+ *                     (dsa_sparse_attn, dsa_sparse_attn_partial); the fused dsa_decode / dsa_prefill
+ *                     keep the library's choice
+ * Other values return DSA_ERR_INVALID_ARG.  Results agree within the attention tolerance, not
+ * bit for bit (the contractions add in different orders).  The workspace sizes
+ * (dsa_sparse_attn_workspace_size, dsa_workspace_size) cover the kernel selected when they are
+ * queried: query them after selecting. */
+#define DSA_ATTN_AUTO 0
+#define DSA_ATTN_TCGEN05 1
+dsa_status dsa_set_attn_kernel(int kernel);
 
 /* --------------------------------------------------------------------------------------------
  * Context split over slices: the pieces of a decode whose context is cut into G position ranges

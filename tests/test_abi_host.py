@@ -66,13 +66,25 @@ def test_header_compiles_as_cxx(tmp_path):
 
 
 def test_status_strings_and_version(native):
-    assert native.lib.dsa_abi_version() == 2
+    assert native.lib.dsa_abi_version() == 3
     for s in range(6):
         assert native.status_string(s).startswith("DSA_")
     assert "unknown" in native.status_string(99)
 
 
 F = 16  # a fake, 16-byte aligned device address; validation rejects before it is ever used
+
+
+def test_attention_kernel_switch(native):
+    # host-only: the switch accepts the two documented kernels and rejects anything else
+    assert native.lib.dsa_set_attn_kernel(7) == 1
+    assert native.lib.dsa_set_attn_kernel(-1) == 1
+    assert native.lib.dsa_set_attn_kernel(native.DSA_ATTN_TCGEN05) == 0
+    # the workspace query covers the selected kernel: 128-row splits for the tensor-memory one
+    tc = native.lib.dsa_sparse_attn_workspace_size(64, 16, 2048, 512)
+    assert native.lib.dsa_set_attn_kernel(native.DSA_ATTN_AUTO) == 0
+    auto = native.lib.dsa_sparse_attn_workspace_size(64, 16, 2048, 512)
+    assert tc >= 64 * 16 * 16 * 512 * 4 and auto <= tc
 
 
 def test_validation_rejects_before_any_launch(native):

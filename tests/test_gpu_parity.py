@@ -216,6 +216,17 @@ def test_topk_causal_rows(dsa):
 # step 3: sparse attention on identical indices
 
 
+@pytest.fixture(params=["auto", "tcgen05"])
+def attn_kernel(request, dsa):
+    """Runs a test on the library's attention kernel and again with the tensor-memory kernel
+    selected (dsa_set_attn_kernel; it takes the 576 / 512 latent row, others keep the default)."""
+    from top_sparse_attention_gb300 import _native as N
+
+    dsa.dsa_set_attn_kernel(N.DSA_ATTN_TCGEN05 if request.param == "tcgen05" else N.DSA_ATTN_AUTO)
+    yield request.param
+    dsa.dsa_set_attn_kernel(N.DSA_ATTN_AUTO)
+
+
 def _attn_case(dsa, wl, idx_np, kv_kind, guard=True):
     cpu = synth.make_inputs(wl)
     dev = to_device(cpu)
@@ -249,7 +260,7 @@ def _random_idx(T, K, L, seed, pad=0):
 
 @pytest.mark.parametrize("kv", ["bf16", "fp8", "fp8_t128"])
 @pytest.mark.parametrize("K,pad", [(2048, 0), (2048, 37), (100, 0), (64, 64)])
-def test_sparse_attn_mla(dsa, kv, K, pad):
+def test_sparse_attn_mla(dsa, attn_kernel, kv, K, pad):
     base = {"bf16": "decode_b8_l32k_bf16", "fp8": "decode_b8_l32k_mxfp8", "fp8_t128": "decode_b8_l32k_mxfp8_kvt128"}[kv]
     wl = synth.small_workload(base, T=3, L=4000, K=K)
     _attn_case(dsa, wl, _random_idx(3, K, 4000, K + pad, pad), kv)
@@ -274,7 +285,7 @@ def test_sparse_attn_repeated_rows(dsa):
 
 
 @pytest.mark.parametrize("D,D_v,tiled", [(576, 512, False), (576, 512, True), (64, 64, False)])
-def test_sparse_attn_fp8_rows_widen_exactly_for_every_code(dsa, D, D_v, tiled):
+def test_sparse_attn_fp8_rows_widen_exactly_for_every_code(dsa, attn_kernel, D, D_v, tiled):
     # One selected row: its softmax weight is exactly 1, so with power-of-two scales the output is
     # each value column's E4M3 value times its scale, exactly representable in bf16.  The rows
     # cycle through all 254 finite codes (subnormals and both zeros included) at shifted columns;

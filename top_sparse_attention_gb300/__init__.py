@@ -12,7 +12,7 @@ _API = ("DsaCall", "dsa_decode", "dsa_get_device_error", "dsa_index_score", "dsa
         "dsa_quantize_mxfp8", "dsa_quantize_fp8_rows", "dsa_quantize_fp8_tiles",
         "dsa_selftest_wait_timeout", "dsa_sparse_attn", "dsa_topk", "dsa_topk_noalloc", "dsa_workspace_size",
         "dsa_topk_pairs", "dsa_topk_merge", "dsa_sparse_attn_partial", "dsa_attn_combine",
-        "ld_scores_for")
+        "dsa_set_attn_kernel", "ld_scores_for")
 _NATIVE = ("DsaError", "LIB_PATH", "EXPORTS")
 
 INPUT_KEYS = ("q_idx", "q_idx_sf", "w", "k_idx", "k_idx_sf", "q", "kv", "kv_scale", "kv_v", "n_valid")

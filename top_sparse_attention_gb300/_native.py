@@ -14,6 +14,7 @@ LIB_PATH = os.path.join(PKG, "libdsa.so")
 
 DSA_OK = 0
 DSA_BF16, DSA_FP8_E4M3, DSA_MXFP8_E4M3, DSA_FP8_E4M3_T128 = 0, 1, 2, 3
+DSA_ATTN_AUTO, DSA_ATTN_TCGEN05 = 0, 1
 DEVERR = {0: "none", 1: "index out of range", 2: "wait timeout", 3: "row-split Top-K counts disagree"}
 
 EXPORTS = (
@@ -22,7 +23,7 @@ EXPORTS = (
     "dsa_quantize_mxfp8", "dsa_quantize_fp8_rows", "dsa_quantize_fp8_tiles",
     "dsa_workspace_size", "dsa_launch_count", "dsa_decode", "dsa_prefill", "dsa_topk_noalloc",
     "dsa_selftest_wait_timeout", "dsa_topk_pairs", "dsa_topk_merge", "dsa_sparse_attn_partial",
-    "dsa_attn_combine",
+    "dsa_attn_combine", "dsa_set_attn_kernel",
 )
 
 
@@ -64,6 +65,7 @@ def _load():
     sig = {
         "dsa_status_string": (ctypes.c_char_p, [I]),
         "dsa_abi_version": (I, []),
+        "dsa_set_attn_kernel": (I, [I]),
         "dsa_get_device_error": (I, [ctypes.POINTER(I), P]),
         "dsa_selftest_wait_timeout": (I, [P]),
         "dsa_index_score": (I, [P, P, P, P, P, I64, I64, I, I, I, P, I, I, I, I, P, I64, P]),

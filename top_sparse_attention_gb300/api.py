@@ -336,6 +336,12 @@ def dsa_prefill(**kw):
     return DsaCall(**kw)()
 
 
+def dsa_set_attn_kernel(kernel: int) -> None:
+    """Select the attention kernel for the 576/512 latent row (N.DSA_ATTN_AUTO or
+    N.DSA_ATTN_TCGEN05; process-wide, for calls made afterwards)."""
+    N.check(N.lib.dsa_set_attn_kernel(int(kernel)), "dsa_set_attn_kernel")
+
+
 def dsa_get_device_error(stream=None) -> int:
     code = ctypes.c_int(0)
     N.check(N.lib.dsa_get_device_error(ctypes.byref(code), _stream(stream)), "dsa_get_device_error")

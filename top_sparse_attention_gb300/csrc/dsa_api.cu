@@ -591,6 +591,8 @@ dsa_status dsa_attn_combine(const float* o_parts, const float* lse_parts, int G,
   return from_cuda(launch_slice_combine(p, reinterpret_cast<cudaStream_t>(stream), false));
 }
 
+dsa_status dsa_set_attn_kernel(int kernel) { return set_attn_kernel(kernel) ? DSA_OK : DSA_ERR_INVALID_ARG; }
+
 size_t dsa_sparse_attn_workspace_size(int T, int H, int K, int D_v) {
   if (T <= 0 || H <= 0 || K <= 0 || D_v <= 0) return 0;
   return sparse_attn_ws_bytes(T, H, K, D_v);

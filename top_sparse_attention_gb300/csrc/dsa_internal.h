@@ -181,7 +181,8 @@ struct SliceCombineParams {
 };
 cudaError_t launch_slice_combine(const SliceCombineParams& p, cudaStream_t stream, bool pdl);
 
-int sparse_attn_splits(int T, int H, int K);
+int sparse_attn_splits(int T, int H, int K, bool chain);
+bool set_attn_kernel(int kernel);  // false for an unknown kernel id
 // kernels one attention step launches (the attention, plus the combine when K is split over CTAs);
 // chain: inside the fused chain (whose index rows hold each query's valid positions first)
 int sparse_attn_launches(int T, int H, int K, int D_qk, int D_v, bool fp8, bool sepv, bool tiled, bool chain);

@@ -29,6 +29,7 @@
 // rows there (faster alone); the fused chain keeps the kernel above, which costs less SM time when
 // several batches are in flight (see DSA_ATTN_TC_MASK).
 #include <algorithm>
+#include <atomic>
 
 #include "dsa_internal.h"
 
@@ -37,22 +38,25 @@ namespace dsa {
 namespace {
 
 constexpr int kHeads = 16;    // heads per CTA (M of m16n8k16)
-// Which 576 / 512 latent rows run on the tensor-memory kernel (bit 0 bf16, bit 1 E4M3 rows with row
-// scales, bit 2 E4M3 rows with tile scales), for a call on its own and inside the fused chain.
-// Measured on B = 8, K = 2048 (alone / one batch of the chain / six batches in flight):
-//   E4M3 rows: 15.9 us / 44.0 us / 22.0 us per step against 18.8 / 47.9 / 18.2 for the mma.sync
-//   kernel; bf16 rows: 15.6 / 44.3 / 23.7 against 13.6 / 43.7 / 18.8.  The tensor-memory kernel takes
-//   128 rows per CTA (twice the CTAs) at 182 KB of shared memory, so with batches in flight its
-//   CTAs wait for whole SMs; alone, its E4M3 rows cost one widening per element instead of
-//   selection MMAs on the legacy pipe.  The fused chain serves batches in flight.
+// Which 576 / 512 latent rows run on the tensor-memory kernel by default (bit 0 bf16, bit 1 E4M3
+// rows with row scales, bit 2 E4M3 rows with tile scales), for a call on its own and inside the
+// fused chain; dsa_set_attn_kernel(DSA_ATTN_TCGEN05) routes a call on its own there regardless.
+// Measured on B = 8, K = 2048, alone: the mma.sync kernel with E4M3 rows widened in registers and
+// one CTA per SM takes 12.9 us (tile scales 13.6, one query at L = 1M 11.6) against 15.6 (17.3,
+// 13.4) for the tensor-memory kernel, bf16 12.0 against 15.6; in the chain with six batches in
+// flight the tensor-memory kernel's 128-row CTAs at 172 KB of shared memory wait for whole SMs
+// (earlier: 22.0 against 18.2 us per step).
 #ifndef DSA_ATTN_TC_MASK
-#define DSA_ATTN_TC_MASK 6
+#define DSA_ATTN_TC_MASK 0
 #endif
 #ifndef DSA_ATTN_TC_MASK_CHAIN
 #define DSA_ATTN_TC_MASK_CHAIN 0
 #endif
 #ifndef DSA_ATTN_CTA_TARGET
 #define DSA_ATTN_CTA_TARGET 76  // attention CTAs aimed for when K is split (about one per two SMs)
+#endif
+#ifndef DSA_ATTN_CTA_TARGET_ALONE
+#define DSA_ATTN_CTA_TARGET_ALONE 152  // the same for a call on its own (dsa_sparse_attn)
 #endif
 // 1: the attention kernels signal the combine kernel after their row blocks, 0: at their start.
 #ifndef DSA_PDL_LATE_ATTN
@@ -1076,16 +1080,18 @@ cudaError_t launch_slice_combine(const SliceCombineParams& p, cudaStream_t strea
   return launch_kernel(slice_combine_kernel, dim3(p.T, p.H), dim3(128), 0, stream, pdl, p);
 }
 
-int sparse_attn_splits(int T, int H, int K) {
-  // About one CTA per two SMs of a 152-SM part.  A CTA's time is mostly the gather's round trips
-  // (index rows, then the selected rows), not its MMAs, so fewer CTAs with more blocks each cost
-  // less SM time; with independent batches in flight the other SMs score the next batches
-  // (measured on the decode chain, B = 8, L = 32K: 64 CTAs of 256 rows gave 7 % more queries/s
-  // than 128 CTAs of 128 rows, at 3 % more latency for one batch alone).
+int sparse_attn_splits(int T, int H, int K, bool chain) {
+  // Inside the fused chain about one CTA per two SMs of a 152-SM part.  A CTA's time is mostly the
+  // gather's round trips (index rows, then the selected rows), not its MMAs, so fewer CTAs with
+  // more blocks each cost less SM time; with independent batches in flight the other SMs score the
+  // next batches (measured on the decode chain, B = 8, L = 32K: 64 CTAs of 256 rows gave 7 % more
+  // queries/s than 128 CTAs of 128 rows, at 3 % more latency for one batch alone).  A call on its
+  // own aims at one CTA per SM: each CTA's rows arrive in one round.
   const int blocks = (K + kRows - 1) / kRows;
   const int ctas_per_split = T * ((H + kHeads - 1) / kHeads);
   if (ctas_per_split <= 0) return 1;
-  int s = (DSA_ATTN_CTA_TARGET + ctas_per_split - 1) / ctas_per_split;
+  const int target = chain ? DSA_ATTN_CTA_TARGET : DSA_ATTN_CTA_TARGET_ALONE;
+  int s = (target + ctas_per_split - 1) / ctas_per_split;
   s = s < 1 ? 1 : (s > 64 ? 64 : s);
   // at least two blocks per split: a CTA's two warp groups take alternate blocks, so a one-block
   // split leaves one group idle (one query, K = 2048: 16 CTAs of 128 rows instead of 32 of 64)
@@ -1102,25 +1108,36 @@ static int rows_per_split(int K, int splits) {
 
 // Which rows go to the tensor-memory kernel: the 576 / 512 latent row, per storage format (bit 0
 // bf16, bit 1 E4M3 with row scales, bit 2 E4M3 with 128-element tile scales).
+std::atomic<int> g_attn_kernel{0};  // DSA_ATTN_AUTO or DSA_ATTN_TCGEN05 (dsa_set_attn_kernel)
+
 bool attn_uses_tc(int D_qk, int D_v, bool fp8, bool sepv, bool tiled, bool chain) {
   if (D_qk != 576 || D_v != 512 || sepv) return false;
+  if (!chain && g_attn_kernel.load(std::memory_order_relaxed) == 1) return true;
   const int bit = tiled ? 4 : (fp8 ? 2 : 1);
   return ((chain ? DSA_ATTN_TC_MASK_CHAIN : DSA_ATTN_TC_MASK) & bit) != 0;
 }
 
-static int routed_splits(int T, int H, int K, bool tc) {
-  return tc ? (K + kTcRows - 1) / kTcRows : sparse_attn_splits(T, H, K);
+bool set_attn_kernel(int kernel) {
+  if (kernel != 0 && kernel != 1) return false;
+  g_attn_kernel.store(kernel, std::memory_order_relaxed);
+  return true;
+}
+
+static int routed_splits(int T, int H, int K, bool tc, bool chain) {
+  return tc ? (K + kTcRows - 1) / kTcRows : sparse_attn_splits(T, H, K, chain);
 }
 
 int sparse_attn_launches(int T, int H, int K, int D_qk, int D_v, bool fp8, bool sepv, bool tiled, bool chain) {
-  return routed_splits(T, H, K, attn_uses_tc(D_qk, D_v, fp8, sepv, tiled, chain)) > 1 ? 2 : 1;
+  return routed_splits(T, H, K, attn_uses_tc(D_qk, D_v, fp8, sepv, tiled, chain), chain) > 1 ? 2 : 1;
 }
 
 size_t sparse_attn_ws_bytes(int T, int H, int K, int D_v) {
-  // sized for either kernel (the storage format is not an argument here)
-  int splits = sparse_attn_splits(T, H, K);
-  if (D_v == 512 && (DSA_ATTN_TC_MASK | DSA_ATTN_TC_MASK_CHAIN) != 0)
-    splits = std::max(splits, routed_splits(T, H, K, true));
+  // sized for every kernel a call can be routed to now (the storage format is not an argument
+  // here): the mma.sync kernel's splits, in the chain and alone, and the tensor-memory kernel's
+  // 128-row splits when it can be selected
+  int splits = std::max(sparse_attn_splits(T, H, K, true), sparse_attn_splits(T, H, K, false));
+  if (D_v == 512 && ((DSA_ATTN_TC_MASK | DSA_ATTN_TC_MASK_CHAIN) != 0 || g_attn_kernel.load() == 1))
+    splits = std::max(splits, routed_splits(T, H, K, true, false));
   if (splits <= 1) return 0;
   const size_t rows = (size_t)T * H * splits;
   return align_up(rows * D_v * sizeof(float), 256) + align_up(rows * 2 * sizeof(float), 256);
@@ -1129,7 +1146,7 @@ size_t sparse_attn_ws_bytes(int T, int H, int K, int D_v) {
 cudaError_t launch_sparse_attn(SparseAttnParams p, int D_qk, int D_v, bool fp8, bool sepv, void* ws,
                                cudaStream_t stream, bool pdl, bool tiled) {
   const bool tc = attn_uses_tc(D_qk, D_v, fp8, sepv, tiled, p.valid_prefix);
-  p.splits = routed_splits(p.T, p.H, p.K, tc);
+  p.splits = routed_splits(p.T, p.H, p.K, tc, p.valid_prefix);
   p.rows_per_split = tc ? kTcRows : rows_per_split(p.K, p.splits);
   if (p.rows_per_split > kMaxRows) return cudaErrorNotSupported;
   if (p.splits > 1) {
