@@ -144,44 +144,6 @@ __device__ __forceinline__ uint64_t block_excl_scan(uint64_t v, uint32_t* sc, ui
   return r;
 }
 
-// block_excl_scan of v, plus the block sum of a 32-bit u (packed 16-bit fields whose sums stay
-// below 2^16) in the same barriers.  sc: 3 * kWarps + 3 words.
-__device__ __forceinline__ uint64_t block_excl_scan_sum(uint64_t v, uint32_t u, uint32_t* sc, uint64_t* total,
-                                                        uint32_t* usum) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint64_t x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint64_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  const uint32_t uw = __reduce_add_sync(0xffffffffu, u);
-  uint64_t* s64 = reinterpret_cast<uint64_t*>(sc);
-  uint32_t* su = sc + 2 * kWarps + 2;
-  if (lane == 31) s64[warp] = x;
-  if (lane == 0) su[warp] = uw;
-  __syncthreads();
-  if (warp == 0) {
-    const uint64_t w = lane < kWarps ? s64[lane] : 0ull;
-    uint64_t s = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint64_t y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
-    }
-    if (lane < kWarps) s64[lane] = s - w;
-    if (lane == 31) s64[kWarps] = s;
-    const uint32_t ut = __reduce_add_sync(0xffffffffu, lane < kWarps ? su[lane] : 0u);
-    if (lane == 0) su[kWarps] = ut;
-  }
-  __syncthreads();
-  const uint64_t r = x - v + s64[warp];
-  *total = s64[kWarps];
-  *usum = su[kWarps];
-  __syncthreads();
-  return r;
-}
-
 // Thread i holds the counts c[0..PER) of bins i*PER .. i*PER+PER-1 (ascending digits).  Finds the
 // digit d with count(> d) < kr <= count(>= d); returns d and sets *above = count(> d).
 template <int PER>
@@ -384,18 +346,26 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkParams
   const uint32_t b0 = find_digit<kBins0>(c0, kr, sc, &above);
   kr -= above;
 
-  // ---- pass A: this CTA's candidates (bin b0) and its count of keys above b0
+  // ---- pass A: this CTA's candidates (bin b0) and its count of keys above b0.  A thread takes its
+  // keys of up to two chunks per step (the list order does not matter to the steps after it)
   {
     uint32_t n_above = 0;
     const int lane = tid & 31;
-    for (int base = 0; base < cnt; base += kChunk) {
+    for (int base = 0; base < cnt; base += 2 * kChunk) {
       const int i = base + 4 * tid;
-      uint32_t k[4];
-      load4(i, k);
+      uint32_t k[8];
+      {
+        uint32_t a[4], b[4];
+        load4(i, a);
+        load4(i + kChunk, b);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) k[j] = a[j], k[4 + j] = b[j];
+      }
       uint32_t cm = 0;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const bool ok = i + j < cnt;
+      for (int j = 0; j < 8; ++j) {
+        const int pos = i + (j < 4 ? j : kChunk + j - 4);
+        const bool ok = pos < cnt;
         const uint32_t d = k[j] >> 20;
         n_above += ok && d > b0;
         cm |= (uint32_t)(ok && d == b0) << j;
@@ -412,9 +382,10 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkParams
       if (lane == 31 && x) at = atomicAdd(&sc[kScCand], x);
       at = __shfl_sync(0xffffffffu, at, 31) + x - nc;
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
+      for (int j = 0; j < 8; ++j)
         if ((cm >> j) & 1u) {
-          if (at < (uint32_t)S.own_cap) own[at] = make_uint2(k[j], (uint32_t)(lo + i + j));
+          const int pos = i + (j < 4 ? j : kChunk + j - 4);
+          if (at < (uint32_t)S.own_cap) own[at] = make_uint2(k[j], (uint32_t)(lo + pos));
           ++at;
         }
     }
@@ -589,52 +560,10 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkParams
 
   if (DSA_PDL_LATE_TOPK == 1) pdl_launch_dependents();
   // ---- output, ascending positions: slot = (keys > T before) + min(keys == T before, kr).
-  // writes this thread's four keys at local positions i.. given the counts before the first
-  auto emit4 = [&](int i, const uint32_t (&k)[4], uint32_t gb, uint32_t eb) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const bool ok = i + j < cnt;
-      const bool is_gt = ok && k[j] > T, is_eq = ok && k[j] == T;
-      if (is_gt || (is_eq && eb < kr)) {
-        const uint32_t slot = gb + min(eb, kr);
-        if (slot < (uint32_t)p.K) out[slot] = lo + i + j;
-        if (pf_kv) prefetch_row((uint32_t)(lo + i + j));
-      }
-      gb += is_gt;
-      eb += is_eq;
-    }
-  };
-  if (cnt <= 2 * kChunk) {
-    // a slice of at most two chunks (the usual decode slice): one scan of both chunks' counts,
-    // 16-bit fields (keys above T, ties) x (chunk 0, chunk 1), plus the sum of the list counts
-    // before this slice (the high half of bf)
-    const int i0 = 4 * tid, i1 = kChunk + 4 * tid;
-    uint32_t k0[4], k1[4];
-    load4(i0, k0);
-    load4(i1, k1);
-    uint32_t ng0 = 0, ne0 = 0, ng1 = 0, ne1 = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      ng0 += i0 + j < cnt && k0[j] > T;
-      ne0 += i0 + j < cnt && k0[j] == T;
-      ng1 += i1 + j < cnt && k1[j] > T;
-      ne1 += i1 + j < cnt && k1[j] == T;
-    }
-    uint64_t tot;
-    uint32_t lists;
-    const uint64_t ex = block_excl_scan_sum((uint64_t)ng0 | (uint64_t)ne0 << 16 | (uint64_t)ng1 << 32 |
-                                                (uint64_t)ne1 << 48,
-                                            (uint32_t)(bf >> 32), sc, &tot, &lists);
-    gt_before += lists >> 16;
-    eq_before += lists & 0xFFFFu;
-    emit4(i0, k0, gt_before + ((uint32_t)ex & 0xFFFFu), eq_before + ((uint32_t)(ex >> 16) & 0xFFFFu));
-    emit4(i1, k1, gt_before + ((uint32_t)tot & 0xFFFFu) + ((uint32_t)(ex >> 32) & 0xFFFFu),
-          eq_before + ((uint32_t)(tot >> 16) & 0xFFFFu) + ((uint32_t)(ex >> 48) & 0xFFFFu));
-  }
-  // longer slices: one 64-bit scan per chunk: low half = (ties << 16 | keys above T) prefix in the
-  // chunk, high half = the list counts before this slice (first chunk only; summed over the block)
+  // One 64-bit scan per chunk: low half = (ties << 16 | keys above T) prefix in the chunk, high
+  // half = the list counts before this slice (first chunk only; summed over the block).
   uint32_t gt_in = 0, eq_in = 0;  // keys above T / ties of this slice before the chunk
-  for (int base = 0; cnt > 2 * kChunk && base < cnt; base += kChunk) {
+  for (int base = 0; base < cnt; base += kChunk) {
     const int i = base + 4 * tid;
     uint32_t k[4];
     load4(i, k);
@@ -650,7 +579,20 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkParams
       gt_before += (uint32_t)(tot >> 48);
       eq_before += (uint32_t)(tot >> 32) & 0xFFFFu;
     }
-    emit4(i, k, gt_before + gt_in + ((uint32_t)ex & 0xFFFFu), eq_before + eq_in + (((uint32_t)ex >> 16) & 0xFFFFu));
+    uint32_t gb = gt_before + gt_in + ((uint32_t)ex & 0xFFFFu);
+    uint32_t eb = eq_before + eq_in + (((uint32_t)ex >> 16) & 0xFFFFu);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const bool ok = i + j < cnt;
+      const bool is_gt = ok && k[j] > T, is_eq = ok && k[j] == T;
+      if (is_gt || (is_eq && eb < kr)) {
+        const uint32_t slot = gb + min(eb, kr);
+        if (slot < (uint32_t)p.K) out[slot] = lo + i + j;
+        if (pf_kv) prefetch_row((uint32_t)(lo + i + j));
+      }
+      gb += is_gt;
+      eb += is_eq;
+    }
     gt_in += (uint32_t)tot & 0xFFFFu;
     eq_in += ((uint32_t)tot >> 16) & 0xFFFFu;
   }
