@@ -459,7 +459,12 @@ def run_ours(args, wl):
 
     # ---- per-kernel durations (component entry points, same kernels and launch shapes), events
     # on the launching stream over `reps` launches each
+    if args.attn_kernel != "auto":  # the fused chain keeps the library's choice either way
+        from top_sparse_attention_gb300 import _native as N
+        dsa.dsa_set_attn_kernel(N.DSA_ATTN_TCGEN05)
     kern = kernel_times(dsa, wl, dev_sets, stream, reps=max(5, min(200, args.steps)))
+    if args.attn_kernel != "auto":
+        dsa.dsa_set_attn_kernel(N.DSA_ATTN_AUTO)
     if wl.q_pos0 < 0:
         peak, peak_kind = measured_hbm_peak()
         a_bytes = index_score_bytes(wl, wl.T)
@@ -502,7 +507,8 @@ def run_ours(args, wl):
             "roofline": roofline,
             "kernels_us": kern,
             "kernels_note": "each component entry timed alone (CUDA graph of launches, rotating input sets); "
-                            "the index score on every resident slot, as dsa_index_score runs it",
+                            "the index score on every resident slot, as dsa_index_score runs it"
+                            + ("; attention on the tensor-memory kernel" if args.attn_kernel != "auto" else ""),
             "next_rows": ({"quant_append": quant_append_time(dsa, wl, stream),
                            "paged_chain": paged_chain_time(dsa, wl, dev_sets, stream)} if wl.q_pos0 < 0 else {}),
             "serial": serial,
@@ -827,6 +833,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="launch through the C ABI each step, no CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--attn-kernel", default="auto", choices=["auto", "tcgen05"],
+                    help="attention kernel for the component timings of calls on their own (dsa_set_attn_kernel)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
