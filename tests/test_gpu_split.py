@@ -76,8 +76,18 @@ def test_topk_merge_fewer_candidates_than_k_and_empty(dsa):
     np.testing.assert_array_equal(got, [[5, 9, -1], [-1, -1, -1]])
 
 
+@pytest.fixture(params=["auto", "tcgen05"])
+def attn_kernel(request, dsa):
+    """The library's attention kernel, and again the tensor-memory kernel (dsa_set_attn_kernel)."""
+    from top_sparse_attention_gb300 import _native as N
+
+    dsa.dsa_set_attn_kernel(N.DSA_ATTN_TCGEN05 if request.param == "tcgen05" else N.DSA_ATTN_AUTO)
+    yield request.param
+    dsa.dsa_set_attn_kernel(N.DSA_ATTN_AUTO)
+
+
 @pytest.mark.parametrize("kv", ["bf16", "fp8", "fp8_t128"])
-def test_partial_attention_and_combine_match_the_oracle(dsa, kv):
+def test_partial_attention_and_combine_match_the_oracle(dsa, attn_kernel, kv):
     base = {"bf16": "decode_b8_l32k_bf16", "fp8": "decode_b8_l32k_mxfp8", "fp8_t128": "decode_b8_l32k_mxfp8_kvt128"}[kv]
     wl = synth.small_workload(base, T=3, L=6000, K=2048)
     cpu = synth.make_inputs(wl)
