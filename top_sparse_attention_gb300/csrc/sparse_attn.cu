@@ -103,6 +103,12 @@ struct Cfg {
   // raw rows, and the accumulators hold even / odd value columns (acc[2g], acc[2g+1] for the warp's
   // 16-column group g)
   static constexpr bool EOV = FP8 && CPW % 32 == 0;
+  // E4M3 rows with one scale per row: registers capped for two CTAs per SM (128 per thread, no
+  // spills), so that a CTA (about 100 KB of shared memory) fits on an SM beside one index-score
+  // CTA (192 threads x 168 registers, about 98 KB).  MXFP8 chain, B = 8, L = 32K, six batches in
+  // flight: 15.75 -> 14.95 us per step over 2,400 steps, unchanged over 20, one batch alone 40.8 ->
+  // 41.2 us.  With tile scales the cap was slower (16.41 -> 16.77 us per step), so they keep one.
+  static constexpr int MINB = FP8 && !TILED ? 2 : 1;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -158,7 +164,7 @@ __device__ __forceinline__ void group_sync(int g) {
 }
 
 template <int DQK, int DV, bool FP8, bool SEPV, bool TILED>
-__global__ void __launch_bounds__(Cfg<DQK, DV, FP8, SEPV, TILED>::THREADS, 1)
+__global__ void __launch_bounds__(Cfg<DQK, DV, FP8, SEPV, TILED>::THREADS, Cfg<DQK, DV, FP8, SEPV, TILED>::MINB)
 sparse_attn_kernel(const SparseAttnParams p) {
   using C = Cfg<DQK, DV, FP8, SEPV, TILED>;
   extern __shared__ __align__(128) uint8_t smem[];
