@@ -355,6 +355,28 @@ def timed_steps(steps, n_sets, stream, streams, enqueue, barrier, graphs=True, c
     return ev0.elapsed_time(ev1) / steps
 
 
+def input_sets(args, wl):
+    """(input sets rotated over, batches in flight) of the timed region: enough sets that their
+    compulsory bytes exceed L2 three times over (3 to 8), rounded up to a multiple of the batches in
+    flight so that set j always runs on stream j % inflight."""
+    n_sets = max(3, min(8, -(-3 * L2_BYTES // max(step_bytes(wl), 1))))
+    if args.sets:
+        n_sets = args.sets
+    inflight = max(1, args.inflight)
+    return -(-n_sets // inflight) * inflight, inflight
+
+
+def run_config(args, wl):
+    """The line's `config`: the workload and how the GPU arm runs it.  Both arms print this same
+    object, so the two lines describe one configuration."""
+    n_sets, inflight = input_sets(args, wl)
+    return {"workload": wl.name, "batch": wl.T, "L": wl.L, "K": wl.K, "H_idx": wl.H_idx,
+            "d_idx": wl.d_idx, "idx_dtype": wl.idx_dtype, "H": wl.H, "D_qk": wl.D_qk,
+            "D_v": wl.D_v, "kv_dtype": wl.kv_dtype, "cuda_graph": not args.no_graph,
+            "batches_in_flight": inflight,
+            "l2": f"rotating {n_sets} input sets, {n_sets * step_bytes(wl) / 1e6:.0f} MB compulsory bytes > 129 MB L2"}
+
+
 def run_reference(args, wl):
     """The oracle as it stands, on the host cores: each step is one query of the workload through
     the whole chain (fp64 scores, full-sort Top-K, exact attention)."""
@@ -379,7 +401,7 @@ def run_reference(args, wl):
         "impl": "reference", "metric": METRIC, "value": rate, "unit": "queries/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded)", "config": {"workload": wl.name},
+        "data": "synthetic (seeded)", "config": run_config(args, wl),
         "cpu_baseline": {"value": rate, "unit": "queries/s", "cores": cores, "kind": "oracle",
                          "sample": f"one query of {wl.name} per step, {args.steps} steps "
                                    f"(fp64 numpy oracle, BLAS threads={cores})"},
@@ -407,11 +429,7 @@ def run_ours(args, wl):
 
     # input sets: each rank draws its own (seed offset by rank) and rotates over R of them
     per_step = step_bytes(wl)
-    n_sets = max(3, min(8, -(-3 * L2_BYTES // max(per_step, 1))))
-    if args.sets:
-        n_sets = args.sets
-    inflight = max(1, args.inflight)
-    n_sets = -(-n_sets // inflight) * inflight  # set j always runs on stream j % inflight
+    n_sets, inflight = input_sets(args, wl)
     cpu_sets = [synth.make_inputs(wl, seed_offset=rank_seed_offset(rank, i)) for i in range(n_sets)]
     dev_sets = [{k: (v.to(dev) if v is not None else None) for k, v in s.items()} for s in cpu_sets]
     calls = [dsa.call_from_tensors(s, K=wl.K, sm_scale=wl.sm_scale, q_per_seq=wl.q_per_seq,
@@ -497,11 +515,7 @@ def run_ours(args, wl):
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if wl.idx_dtype == "bf16" else "fp8(e4m3)+bf16",
             "data": "synthetic (seeded N(0,1) inputs, U(0,1) head weights)",
-            "config": {"workload": wl.name, "batch": wl.T, "L": wl.L, "K": wl.K, "H_idx": wl.H_idx,
-                       "d_idx": wl.d_idx, "idx_dtype": wl.idx_dtype, "H": wl.H, "D_qk": wl.D_qk,
-                       "D_v": wl.D_v, "kv_dtype": wl.kv_dtype, "cuda_graph": not args.no_graph,
-                       "batches_in_flight": inflight,
-                       "l2": f"rotating {n_sets} input sets, {n_sets * per_step / 1e6:.0f} MB compulsory bytes > 129 MB L2"},
+            "config": run_config(args, wl),
             "hbm_gbs": chain_gbs, "hbm_frac_of_8tbs": chain_gbs / NOMINAL_HBM_GBS,
             "hbm_frac_of_measured": chain_gbs / peak,
             "roofline": roofline,

@@ -74,3 +74,25 @@ def test_traffic_is_reported_only_for_the_profiled_source(tmp_path, monkeypatch)
     (src / "index_score.cu").write_text("// kernel revision B\n")
     assert bench.profiled_traffic("w") is None  # the kernel changed since the capture
 
+
+
+def test_reference_arm_prints_the_gpu_arms_config(capsys, monkeypatch):
+    """The oracle arm's line carries the same config, metric, unit and direction as the GPU arm's,
+    with its own cpu_baseline and an e2e of no copies."""
+    import argparse
+    import json
+
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    wl = _wl("tiny_decode_l2k")
+    args = argparse.Namespace(gpus=1, inflight=6, steps=3, warmup=3, impl="reference", workload=wl.name,
+                              sets=0, no_graph=False, no_cpu_baseline=False, cpu_seconds=1.0, attn_kernel="auto")
+    assert bench.run_reference(args, wl) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert line["config"] == bench.run_config(args, wl)
+    assert (line["metric"], line["unit"], line["higher_is_better"]) == (bench.METRIC, "queries/s", True)
+    assert line["steps"] == 3 and line["warmup"] == 3 and line["value"] > 0
+    assert line["cpu_baseline"]["value"] == line["value"] and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"] == {"value": line["value"], "unit": "queries/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
